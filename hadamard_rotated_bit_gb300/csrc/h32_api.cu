@@ -1,0 +1,83 @@
+// Library-wide entry points: device checks, status reporting, wait bounds.
+#include <atomic>
+#include <mutex>
+
+#include "h32_common.cuh"
+
+namespace h32 {
+namespace {
+
+std::atomic<uint64_t> g_wait_polls{kDefaultWaitPolls};
+
+struct DeviceInfo {
+    int checked = 0;  // 0 = not yet, 1 = sm_103, -1 = not supported
+    int sm_count = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_dev_mutex;
+
+}  // namespace
+
+uint64_t wait_limit() { return g_wait_polls.load(std::memory_order_relaxed); }
+
+h32_status launch_status(cudaError_t e) { return e == cudaSuccess ? H32_OK : H32_ERR_CUDA; }
+
+h32_status check_device(int *sm_count) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return H32_ERR_UNSUPPORTED;
+    }
+    if (dev >= kMaxDevices) return H32_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &info = g_devices[dev];
+    if (info.checked == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return H32_ERR_UNSUPPORTED;
+        }
+        info.checked = (major == 10 && minor == 3) ? 1 : -1;
+        info.sm_count = sms;
+    }
+    if (info.checked != 1) return H32_ERR_UNSUPPORTED;
+    if (sm_count) *sm_count = info.sm_count;
+    return H32_OK;
+}
+
+}  // namespace h32
+
+extern "C" h32_status h32_device_status(void *stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    H32_TRY(h32::check_device(nullptr));
+    if (cudaStreamSynchronize(s) != cudaSuccess) return H32_ERR_CUDA;
+    h32_status a = h32::quant_read_and_clear_status(s);
+    h32_status b = h32::gemm_read_and_clear_status(s);
+    if (a == H32_ERR_CUDA || b == H32_ERR_CUDA) return H32_ERR_CUDA;
+    if (a == H32_ERR_TIMEOUT || b == H32_ERR_TIMEOUT) return H32_ERR_TIMEOUT;
+    if (a != H32_OK) return a;
+    return b;
+}
+
+extern "C" const char *h32_status_string(h32_status st) {
+    switch (st) {
+        case H32_OK: return "ok";
+        case H32_ERR_INVALID_ARG: return "invalid argument";
+        case H32_ERR_ALIGNMENT: return "pointer or row pitch not 16-byte aligned";
+        case H32_ERR_UNSUPPORTED: return "no sm_103 CUDA device";
+        case H32_ERR_CUDA: return "CUDA runtime error";
+        case H32_ERR_TIMEOUT: return "a bounded device wait gave up";
+        case H32_ERR_DEVICE_GUARD: return "device-side range check failed";
+    }
+    return "unknown status";
+}
+
+extern "C" void h32_set_wait_limit(uint64_t polls) {
+    h32::g_wait_polls.store(polls == 0 ? h32::kDefaultWaitPolls : polls, std::memory_order_relaxed);
+}
+
+extern "C" int h32_version(void) { return 100; }

@@ -1,0 +1,287 @@
+// Rotate + quantize kernels of the Hadamard route (sm_103a).
+//
+//  * h32_quantize_act_q4 / _q8: the activation quantizer of "509 tokens a
+//    second of prompt: the Hadamard route ships", section "The rotation":
+//    each block of 32 activations is rotated by the 32-point Walsh-Hadamard
+//    transform and rounded to 4-bit codes with one fp32 scale (8-bit codes on
+//    the exact route of "Prompt processing: 4-bit activations, rotated
+//    first").
+//  * h32_rotate_quantize_weights_q4_0: the offline weight step of "Making the
+//    file is part of the engine" (rotate the projections, quantize to Q4_0).
+//
+// Layout on the device: one thread owns one whole 32-block.  It loads the
+// block with 128-bit loads, runs all five butterfly stages (strides 1, 2, 4,
+// 8, 16) in registers, takes the block's amax, one IEEE divide and one IEEE
+// reciprocal, and writes the packed codes with one 128-bit store (4-bit) or
+// two (8-bit).  Adjacent lanes own adjacent blocks, so each warp's stores are
+// contiguous.  The pages run the rotation as two in-thread butterfly steps
+// and three lane shuffles on a 32-wide AMD wave; owning the whole block in one
+// thread removes the shuffles and the per-lane redundant divide, which keeps
+// the kernel's instruction count under the HBM roofline on GB300.
+//
+// Rounding: every add, multiply, divide and reciprocal is IEEE round-to-
+// nearest-even (explicit _rn intrinsics; the library is built without
+// fast-math and with denormals kept), so codes and scales are bit-identical
+// to a plain sequential fp32 evaluation of the same steps.
+#include <cuda_fp16.h>
+
+#include "h32_common.cuh"
+
+namespace h32 {
+namespace {
+
+// fp32 nearest to 1/sqrt(32) (bit pattern 0x3E3504F3)
+constexpr float kInvSqrt32 = 0x1.6a09e6p-3f;
+// 1.5 * 2^23: adding it to |t| < 2^22 leaves round-half-even(t) in the low
+// mantissa bits as a two's-complement integer
+constexpr float kRoundMagic = 12582912.0f;
+
+// ----------------------------------------------------------------------------
+// loading one block as 32 fp32 values
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void load_block_bf16(const uint16_t *__restrict__ p, float (&v)[32]) {
+    const uint4 *q = reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint4 u = __ldg(q + c);
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[8 * c + 2 * i] = __uint_as_float(w[i] << 16);
+            v[8 * c + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+}
+
+__device__ __forceinline__ void load_block_f32(const float *__restrict__ p, float (&v)[32]) {
+    const float4 *q = reinterpret_cast<const float4 *>(p);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        float4 f = __ldg(q + c);
+        v[4 * c] = f.x;
+        v[4 * c + 1] = f.y;
+        v[4 * c + 2] = f.z;
+        v[4 * c + 3] = f.w;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// the rotation: butterfly with strides 1, 2, 4, 8, 16, then the 1/sqrt(32) scale
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void rotate32(float (&v)[32]) {
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if ((i & h) == 0) {
+                const float a = v[i], c = v[i + h];
+                v[i] = __fadd_rn(a, c);
+                v[i + h] = __fsub_rn(a, c);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], kInvSqrt32);
+}
+
+// low byte of each of four words -> one word
+__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    const uint32_t ab = __byte_perm(a, b, 0x0040);
+    const uint32_t cd = __byte_perm(c, d, 0x0040);
+    return __byte_perm(ab, cd, 0x5410);
+}
+
+// ----------------------------------------------------------------------------
+// activation quantizer
+// ----------------------------------------------------------------------------
+template <bool kBf16, int kBits, bool kRotate>
+__global__ void __launch_bounds__(256) quant_act_kernel(const void *__restrict__ x, uint32_t nblk,
+                                                       uint32_t nb, int64_t ldx,
+                                                       uint8_t *__restrict__ xq,
+                                                       float *__restrict__ xd) {
+    constexpr float kQmax = (kBits == 4) ? 7.0f : 127.0f;
+    constexpr float kQmin = (kBits == 4) ? -8.0f : -127.0f;
+    // block g = row * nb + b; the grid stride is split once into whole rows
+    // and a remainder so the walk needs no division per block
+    const uint32_t stride = gridDim.x * blockDim.x;
+    const uint32_t srow = stride / nb, sb = stride % nb;
+    uint32_t g = blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t row = g / nb, b = g % nb;
+    for (; g < nblk; g += stride) {
+        float v[32];
+        if constexpr (kBf16) {
+            load_block_bf16(reinterpret_cast<const uint16_t *>(x) + int64_t(row) * ldx + 32 * b, v);
+        } else {
+            load_block_f32(reinterpret_cast<const float *>(x) + int64_t(row) * ldx + 32 * b, v);
+        }
+        if constexpr (kRotate) rotate32(v);
+
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const float d = __fdiv_rn(amax, kQmax);
+        const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+
+        // codes: round-half-even(clamp(y * id)); with a finite id the product
+        // is within [-qmax, qmax] up to rounding, so the clamp only matters
+        // when 1/d overflowed (a block of subnormal size)
+        uint32_t bits[32];
+        if (isinf(id)) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float t = __fmul_rn(v[i], id);
+                t = fminf(fmaxf(t, kQmin), kQmax);
+                bits[i] = __float_as_uint(__fadd_rn(t, kRoundMagic));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                bits[i] = __float_as_uint(__fadd_rn(__fmul_rn(v[i], id), kRoundMagic));
+        }
+
+        if constexpr (kBits == 4) {
+            // Q4_0 nibble order: byte j = element j (low) | element j + 16 (high)
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t lo =
+                    pack_low_bytes(bits[4 * k], bits[4 * k + 1], bits[4 * k + 2], bits[4 * k + 3]);
+                const uint32_t hi = pack_low_bytes(bits[16 + 4 * k], bits[17 + 4 * k],
+                                                   bits[18 + 4 * k], bits[19 + 4 * k]);
+                w[k] = (lo & 0x0F0F0F0Fu) | ((hi << 4) & 0xF0F0F0F0u);
+            }
+            *reinterpret_cast<uint4 *>(xq + (int64_t(g) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                w[k] = pack_low_bytes(bits[4 * k], bits[4 * k + 1], bits[4 * k + 2], bits[4 * k + 3]);
+            uint4 *dst = reinterpret_cast<uint4 *>(xq + (int64_t(g) << 5));
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        xd[g] = d;
+        row += srow;
+        b += sb;
+        if (b >= nb) {
+            b -= nb;
+            ++row;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// offline weights: rotate, then the Q4_0 rule
+// ----------------------------------------------------------------------------
+template <bool kRotate>
+__global__ void __launch_bounds__(256) quant_w_kernel(const float *__restrict__ w, uint32_t nblk,
+                                                     uint8_t *__restrict__ wq,
+                                                     uint16_t *__restrict__ wd) {
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < nblk; g += stride) {
+        float v[32];
+        load_block_f32(w + int64_t(g) * 32, v);
+        if constexpr (kRotate) rotate32(v);
+        // signed value of largest magnitude, first one on ties
+        float amax = 0.0f, mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float a = fabsf(v[i]);
+            if (a > amax) {
+                amax = a;
+                mx = v[i];
+            }
+        }
+        const float d = __fdiv_rn(mx, -8.0f);
+        const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+        uint32_t c[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            float u = __fadd_rn(__fmul_rn(v[i], id), 8.5f);
+            u = fminf(fmaxf(u, 0.0f), 15.0f);
+            c[i] = static_cast<uint32_t>(__float2int_rz(u));
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t lo = pack_low_bytes(c[4 * k], c[4 * k + 1], c[4 * k + 2], c[4 * k + 3]);
+            const uint32_t hi =
+                pack_low_bytes(c[16 + 4 * k], c[17 + 4 * k], c[18 + 4 * k], c[19 + 4 * k]);
+            o[k] = lo | (hi << 4);
+        }
+        *reinterpret_cast<uint4 *>(wq + (int64_t(g) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        wd[g] = __half_as_ushort(__float2half_rn(d));
+    }
+}
+
+int grid_for(uint32_t nblk, int sm_count) {
+    const uint32_t want = (nblk + 255) / 256;
+    const uint32_t cap = static_cast<uint32_t>(sm_count) * 8;
+    return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+template <int kBits>
+h32_status quantize_act(const void *x, h32_in_dtype dt, int64_t M, int64_t K, int64_t ldx,
+                        void *xq, float *xd, int rotate, void *stream) {
+    if (M < 0 || K <= 0 || (K % 32) != 0 || ldx < K) return H32_ERR_INVALID_ARG;
+    if (dt != H32_IN_F32 && dt != H32_IN_BF16) return H32_ERR_INVALID_ARG;
+    if (M == 0) return H32_OK;
+    if (!x || !xq || !xd) return H32_ERR_INVALID_ARG;
+    const int64_t esize = (dt == H32_IN_BF16) ? 2 : 4;
+    if (!aligned16(x) || !aligned16(xq) || !aligned16(xd) || ((ldx * esize) % 16) != 0)
+        return H32_ERR_ALIGNMENT;
+    const int64_t nb = K / 32;
+    if (M * nb > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
+    int sms = 0;
+    H32_TRY(check_device(&sms));
+    const uint32_t nblk = static_cast<uint32_t>(M * nb);
+    const uint32_t f = static_cast<uint32_t>(nb);
+    const int grid = grid_for(nblk, sms);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *q = reinterpret_cast<uint8_t *>(xq);
+    if (dt == H32_IN_BF16) {
+        if (rotate) quant_act_kernel<true, kBits, true><<<grid, 256, 0, s>>>(x, nblk, f, ldx, q, xd);
+        else quant_act_kernel<true, kBits, false><<<grid, 256, 0, s>>>(x, nblk, f, ldx, q, xd);
+    } else {
+        if (rotate) quant_act_kernel<false, kBits, true><<<grid, 256, 0, s>>>(x, nblk, f, ldx, q, xd);
+        else quant_act_kernel<false, kBits, false><<<grid, 256, 0, s>>>(x, nblk, f, ldx, q, xd);
+    }
+    return launch_status(cudaGetLastError());
+}
+
+}  // namespace
+
+h32_status quant_read_and_clear_status(cudaStream_t) { return H32_OK; }
+
+}  // namespace h32
+
+extern "C" h32_status h32_quantize_act_q4(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
+                                          int64_t ldx, uint8_t *xq, float *xd, int rotate,
+                                          void *stream) {
+    return h32::quantize_act<4>(x, dt, M, K, ldx, xq, xd, rotate, stream);
+}
+
+extern "C" h32_status h32_quantize_act_q8(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
+                                          int64_t ldx, int8_t *xq, float *xd, int rotate,
+                                          void *stream) {
+    return h32::quantize_act<8>(x, dt, M, K, ldx, xq, xd, rotate, stream);
+}
+
+extern "C" h32_status h32_rotate_quantize_weights_q4_0(const float *w, int64_t N, int64_t K,
+                                                       int rotate, uint8_t *wq, uint16_t *wd,
+                                                       void *stream) {
+    using namespace h32;
+    if (N < 0 || K <= 0 || (K % 32) != 0) return H32_ERR_INVALID_ARG;
+    if (N == 0) return H32_OK;
+    if (!w || !wq || !wd) return H32_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(wq) || !aligned16(wd)) return H32_ERR_ALIGNMENT;
+    if (N * (K / 32) > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
+    int sms = 0;
+    H32_TRY(check_device(&sms));
+    const uint32_t nblk = static_cast<uint32_t>(N * (K / 32));
+    const int grid = grid_for(nblk, sms);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (rotate) quant_w_kernel<true><<<grid, 256, 0, s>>>(w, nblk, wq, wd);
+    else quant_w_kernel<false><<<grid, 256, 0, s>>>(w, nblk, wq, wd);
+    return launch_status(cudaGetLastError());
+}

@@ -1,0 +1,170 @@
+/*
+ * h32.h -- C ABI of the Hadamard-route prompt path for one GB300 GPU (sm_103a).
+ *
+ * The method (pages: "509 tokens a second of prompt: the Hadamard route ships"
+ * and "Qwen3.8-27B at 45.7 tok/s ...", section "Prompt processing: 4-bit
+ * activations, rotated first"):
+ *   - activations are rounded in blocks of 32 values that share one scale;
+ *   - each block is first rotated by a 32-point Walsh-Hadamard transform,
+ *     which spreads a few large values over the block ("The rotation");
+ *   - the weights are rotated the same way once, offline, and stored as
+ *     Q4_0 (an fp16 scale and 32 4-bit codes q per block, value (q - 8) * d),
+ *     so every dot product is unchanged: x . w = (Hx) . (Hw);
+ *   - the matrix product runs on 4-bit (or, on the exact route, 8-bit)
+ *     activation codes against the Q4_0 codes, whose top bit flipped is the
+ *     two's-complement value q - 8 ("Why prompts are a matrix-unit problem").
+ *
+ * Conventions for every call:
+ *   Ownership  All array pointers are device pointers owned by the caller.
+ *              The library keeps no pointer after a call returns and allocates
+ *              no device memory.
+ *   Streams    `stream` is a cudaStream_t (0 = the legacy default stream).
+ *              Every compute call only enqueues work on it and returns.
+ *   Errors     Argument, shape and alignment errors are returned at once,
+ *              before anything is enqueued.  A failed launch returns
+ *              H32_ERR_CUDA.  Problems found on the device (a bounded wait
+ *              that gave up, a range guard) set a per-library device status
+ *              word instead; h32_device_status() synchronizes the stream and
+ *              reports (and clears) it.  There is no CPU fallback: a device
+ *              that is not sm_103 returns H32_ERR_UNSUPPORTED.
+ *   Layouts    Row-major.  K is the reduction length, a multiple of 32;
+ *              nb = K / 32 blocks per row.  4-bit codes are stored in the
+ *              Q4_0 nibble order: byte j (0..15) of a block holds element j in
+ *              its low nibble and element j + 16 in its high nibble.
+ *   Alignment  Every array pointer is 16-byte aligned; row pitches given in
+ *              elements must make the pitch in bytes a multiple of 16.
+ *   Empty      M = 0 (or R = 0) is valid and enqueues nothing.
+ */
+#ifndef H32_H
+#define H32_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum h32_status {
+    H32_OK = 0,
+    H32_ERR_INVALID_ARG = 1,  /* null pointer, bad shape or dtype               */
+    H32_ERR_ALIGNMENT = 2,    /* pointer or row pitch not 16-byte aligned       */
+    H32_ERR_UNSUPPORTED = 3,  /* no CUDA device, or the device is not sm_103    */
+    H32_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed    */
+    H32_ERR_TIMEOUT = 5,      /* device status: a bounded wait gave up          */
+    H32_ERR_DEVICE_GUARD = 6  /* device status: a device-side range check fired */
+} h32_status;
+
+typedef enum h32_in_dtype {
+    H32_IN_F32 = 0,  /* fp32 activations                                     */
+    H32_IN_BF16 = 1  /* bf16 activations, widened to fp32 exactly            */
+} h32_in_dtype;
+
+/*
+ * Rotate and quantize activations to 4-bit codes (the activation quantizer of
+ * "The rotation" / "Prompt processing: 4-bit activations, rotated first").
+ * For each row m and block b: y = H x_block / sqrt(32) (fp32 butterfly,
+ * strides 1, 2, 4, 8, 16, then one multiply by the fp32 nearest 1/sqrt(32));
+ * d = amax(|y|) / 7 in fp32; codes = round-half-even(clamp(y * (1/d), -8, 7)),
+ * all codes 0 when d = 0.
+ *   x      [M][ldx] activations of type `dt`, ldx >= K
+ *   xq     [M][K/2] out: two's-complement 4-bit codes, Q4_0 nibble order
+ *   xd     [M][K/32] out: fp32 scales d
+ *   rotate 1 = rotate first (the Hadamard route); 0 = plain 4-bit route
+ */
+h32_status h32_quantize_act_q4(const void *x, h32_in_dtype dt, int64_t M, int64_t K, int64_t ldx,
+                               uint8_t *xq, float *xd, int rotate, void *stream);
+
+/*
+ * The exact route's 8-bit activation quantizer ("Prompt processing ...": the
+ * exact int8 path).  As h32_quantize_act_q4 with d = amax / 127 and codes
+ * clamped to [-127, 127], stored as int8 in element order.
+ *   xq     [M][K] out: int8 codes;  xd [M][K/32] out: fp32 scales
+ */
+h32_status h32_quantize_act_q8(const void *x, h32_in_dtype dt, int64_t M, int64_t K, int64_t ldx,
+                               int8_t *xq, float *xd, int rotate, void *stream);
+
+/*
+ * Offline weight step ("Making the file is part of the engine": rotate the
+ * projections, then quantize to Q4_0).  Each 32-block of a weight row is
+ * rotated with the same transform as the activations (if rotate = 1), then
+ * rounded by the Q4_0 rule: the signed value of largest magnitude (first on
+ * ties) maps to code 0, d = max / -8, code = min(15, trunc(y * (1/d) + 8.5)),
+ * d stored as fp16 rounded to nearest even.
+ *   w      [N][K] fp32 weights (rows are output features)
+ *   wq     [N][K/2] out: codes 0..15 in Q4_0 nibble order
+ *   wd     [N][K/32] out: fp16 scales (bit patterns)
+ */
+h32_status h32_rotate_quantize_weights_q4_0(const float *w, int64_t N, int64_t K, int rotate,
+                                            uint8_t *wq, uint16_t *wd, void *stream);
+
+/*
+ * Block-scaled integer product of Q4_0 weights and 4-bit activations (the
+ * W4A4 matrix product of "Why prompts are a matrix-unit problem").
+ *   y[m][n] = sum over b = 0 .. nb-1, in that order, of
+ *             acc = fma(fp32(d_w[n][b] * d_x[m][b]), S[m][n][b], acc), acc0 = +0,
+ *   S[m][n][b] = sum_j x_code[m][32b+j] * (w_code[n][32b+j] - 8), exact.
+ *   wq, wd      Q4_0 weights as written by h32_rotate_quantize_weights_q4_0
+ *   xq, xd      4-bit activations as written by h32_quantize_act_q4
+ *   y           [M][ldy] fp32 out, ldy >= N
+ *   block_sums  nullable debug output: int32 [M][N][K/32], the exact S
+ * Requires N % 16 == 0.
+ */
+h32_status q4_0_x_q4_gemm(const uint8_t *wq, const uint16_t *wd, const uint8_t *xq,
+                          const float *xd, int64_t M, int64_t N, int64_t K, float *y,
+                          int64_t ldy, int32_t *block_sums, void *stream);
+
+/*
+ * The exact route: Q4_0 weights against 8-bit activation codes
+ * (h32_quantize_act_q8).  Same definition with x_code in [-127, 127].
+ */
+h32_status q4_0_x_q8_gemm(const uint8_t *wq, const uint16_t *wd, const int8_t *xq,
+                          const float *xd, int64_t M, int64_t N, int64_t K, float *y,
+                          int64_t ldy, int32_t *block_sums, void *stream);
+
+/*
+ * Expert-batched W4A4 product for mixture-of-experts layers ("4-bit
+ * activations reach the MoE experts").  Output rows are in grouped order:
+ * row r in [expert_off[e], expert_off[e+1]) uses expert e's weights and the
+ * activation row row_idx[r] (row_idx = NULL means row r itself).
+ *   wq          [E][N][K/2] Q4_0 codes;  wd [E][N][K/32] fp16 scales
+ *   xq, xd      4-bit activations [T][K/2], [T][K/32] (T rows, any T)
+ *   row_idx     device int32 [R] or NULL
+ *   expert_off  device int32 [E+1], non-decreasing, expert_off[0] = 0,
+ *               expert_off[E] = R (checked on the device: a violation sets
+ *               H32_ERR_DEVICE_GUARD and the kernel writes nothing)
+ *   y           [R][ldy] fp32 out;  block_sums nullable int32 [R][N][K/32]
+ * Requires N % 16 == 0.
+ */
+h32_status q4_0_x_q4_gemm_experts(const uint8_t *wq, const uint16_t *wd, int32_t E,
+                                  const uint8_t *xq, const float *xd, const int32_t *row_idx,
+                                  const int32_t *expert_off, int64_t R, int64_t N, int64_t K,
+                                  float *y, int64_t ldy, int32_t *block_sums, void *stream);
+
+/*
+ * Synchronize `stream`, then report and clear the device status word of every
+ * kernel this library launched on the current device since the last call:
+ * H32_OK, H32_ERR_TIMEOUT or H32_ERR_DEVICE_GUARD (or H32_ERR_CUDA when the
+ * synchronization itself fails).
+ */
+h32_status h32_device_status(void *stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *h32_status_string(h32_status status);
+
+/*
+ * Bound on every spin wait inside the kernels, in polling iterations
+ * (0 restores the default of about a second).  Kernels launched after the
+ * call use the new bound; a wait that exceeds it makes the kernel record
+ * H32_ERR_TIMEOUT, drain its own in-flight copies and return.  Meant for
+ * tests of the timeout path.
+ */
+void h32_set_wait_limit(uint64_t polls);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int h32_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H32_H */

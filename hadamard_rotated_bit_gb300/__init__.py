@@ -1,0 +1,244 @@
+"""Python binding of the h32 C-ABI library (the Hadamard-route prompt path).
+
+The functions below carry the names of the C entry points declared in
+``include/h32.h`` and only marshal arguments: they take CUDA torch tensors,
+allocate outputs with torch when none are given, pass raw device pointers and
+the current CUDA stream to the library, and raise ``H32Error`` on a non-OK
+status.  Every step of the path runs in the library's CUDA kernels; there is
+no CPU fallback, and calling any function without the built library raises.
+
+Build the library with ``python -m hadamard_rotated_bit_gb300._build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "H32Error", "lib", "library_path", "EXPORTED_SYMBOLS",
+    "h32_quantize_act_q4", "h32_quantize_act_q8", "h32_rotate_quantize_weights_q4_0",
+    "q4_0_x_q4_gemm", "q4_0_x_q8_gemm", "q4_0_x_q4_gemm_experts",
+    "h32_device_status", "h32_status_string", "h32_set_wait_limit", "h32_version",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "lib", "libh32.so")
+
+H32_OK, H32_ERR_INVALID_ARG, H32_ERR_ALIGNMENT, H32_ERR_UNSUPPORTED = 0, 1, 2, 3
+H32_ERR_CUDA, H32_ERR_TIMEOUT, H32_ERR_DEVICE_GUARD = 4, 5, 6
+H32_IN_F32, H32_IN_BF16 = 0, 1
+
+_P, _I64, _I32, _INT = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+
+# name -> (restype, argtypes); mirrors include/h32.h
+_SIGS = {
+    "h32_quantize_act_q4": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _INT, _P]),
+    "h32_quantize_act_q8": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _INT, _P]),
+    "h32_rotate_quantize_weights_q4_0": (_INT, [_P, _I64, _I64, _INT, _P, _P, _P]),
+    "q4_0_x_q4_gemm": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _P]),
+    "q4_0_x_q8_gemm": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _P]),
+    "q4_0_x_q4_gemm_experts": (_INT, [_P, _P, _I32, _P, _P, _P, _I64, _P, _I64, _I64, _I64,
+                                      _P, _I64, _P, _P]),
+    "h32_device_status": (_INT, [_P]),
+    "h32_status_string": (ctypes.c_char_p, [_INT]),
+    "h32_set_wait_limit": (None, [ctypes.c_uint64]),
+    "h32_version": (_INT, []),
+}
+EXPORTED_SYMBOLS = tuple(_SIGS)
+
+_lib = None
+_lock = threading.Lock()
+
+
+class H32Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {h32_status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(library_path):
+                raise ImportError(
+                    f"h32 CUDA library not built ({library_path} missing); run "
+                    "`python -m hadamard_rotated_bit_gb300._build` first")
+            L = ctypes.CDLL(library_path)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def h32_status_string(status: int) -> str:
+    return lib().h32_status_string(int(status)).decode()
+
+
+def h32_version() -> int:
+    return int(lib().h32_version())
+
+
+def h32_set_wait_limit(polls: int) -> None:
+    lib().h32_set_wait_limit(int(polls))
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(fn: str, st: int):
+    if st != H32_OK:
+        raise H32Error(fn, st)
+
+
+def _cuda(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t
+
+
+def _rows(t, name):
+    """2-D tensor with unit stride in its last dimension; returns its row pitch."""
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name} must be 2-D with a contiguous last dimension")
+    return t.stride(0) if t.shape[0] > 1 else t.shape[1]
+
+
+# --------------------------------------------------------------------------
+# quantizers
+# --------------------------------------------------------------------------
+def _quantize_act(fn_name, bits, x, rotate, xq, xd, stream):
+    torch = _torch()
+    _cuda(x, "x")
+    if x.dtype == torch.bfloat16:
+        dt = H32_IN_BF16
+    elif x.dtype == torch.float32:
+        dt = H32_IN_F32
+    else:
+        raise ValueError("x must be bf16 or fp32")
+    ldx = _rows(x, "x")
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K // 2 if bits == 4 else K),
+                         dtype=torch.uint8 if bits == 4 else torch.int8, device=x.device)
+    if xd is None:
+        xd = torch.empty((M, K // 32), dtype=torch.float32, device=x.device)
+    st = getattr(lib(), fn_name)(_ptr(x), dt, M, K, ldx, _ptr(xq), _ptr(xd), int(bool(rotate)),
+                                 _stream(stream))
+    _check(fn_name, st)
+    return xq, xd
+
+
+def h32_quantize_act_q4(x, rotate=True, xq=None, xd=None, stream=None):
+    """x [M][K] bf16/fp32 -> (xq [M][K/2] uint8, xd [M][K/32] fp32)."""
+    return _quantize_act("h32_quantize_act_q4", 4, x, rotate, xq, xd, stream)
+
+
+def h32_quantize_act_q8(x, rotate=True, xq=None, xd=None, stream=None):
+    """x [M][K] bf16/fp32 -> (xq [M][K] int8, xd [M][K/32] fp32)."""
+    return _quantize_act("h32_quantize_act_q8", 8, x, rotate, xq, xd, stream)
+
+
+def h32_rotate_quantize_weights_q4_0(w, rotate=True, wq=None, wd=None, stream=None):
+    """w [N][K] fp32 (contiguous) -> (wq [N][K/2] uint8, wd [N][K/32] int16 holding fp16 bits)."""
+    torch = _torch()
+    _cuda(w, "w")
+    if w.dtype != torch.float32 or not w.is_contiguous() or w.dim() != 2:
+        raise ValueError("w must be a contiguous 2-D fp32 tensor")
+    N, K = w.shape
+    if wq is None:
+        wq = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    if wd is None:
+        wd = torch.empty((N, K // 32), dtype=torch.int16, device=w.device)
+    st = lib().h32_rotate_quantize_weights_q4_0(_ptr(w), N, K, int(bool(rotate)), _ptr(wq),
+                                                _ptr(wd), _stream(stream))
+    _check("h32_rotate_quantize_weights_q4_0", st)
+    return wq, wd
+
+
+# --------------------------------------------------------------------------
+# GEMMs
+# --------------------------------------------------------------------------
+def _gemm(fn_name, wq, wd, xq, xd, y, block_sums, stream):
+    torch = _torch()
+    for t, n in ((wq, "wq"), (wd, "wd"), (xq, "xq"), (xd, "xd")):
+        _cuda(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    N = wq.shape[0]
+    K = wq.shape[1] * 2
+    M = xq.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=wq.device)
+    ldy = _rows(y, "y")
+    S = None
+    if block_sums is True:
+        S = torch.empty((M, N, K // 32), dtype=torch.int32, device=wq.device)
+    elif block_sums is not None and block_sums is not False:
+        S = block_sums
+    st = getattr(lib(), fn_name)(_ptr(wq), _ptr(wd), _ptr(xq), _ptr(xd), M, N, K, _ptr(y), ldy,
+                                 _ptr(S), _stream(stream))
+    _check(fn_name, st)
+    return (y, S) if S is not None else y
+
+
+def q4_0_x_q4_gemm(wq, wd, xq, xd, y=None, block_sums=None, stream=None):
+    """y [M][N] = block-scaled product of Q4_0 weights and 4-bit activations.
+
+    block_sums=True also returns the exact per-block sums int32 [M][N][K/32]."""
+    return _gemm("q4_0_x_q4_gemm", wq, wd, xq, xd, y, block_sums, stream)
+
+
+def q4_0_x_q8_gemm(wq, wd, xq, xd, y=None, block_sums=None, stream=None):
+    """The exact route: Q4_0 weights against 8-bit activation codes."""
+    return _gemm("q4_0_x_q8_gemm", wq, wd, xq, xd, y, block_sums, stream)
+
+
+def q4_0_x_q4_gemm_experts(wq, wd, xq, xd, row_idx, expert_off, R, y=None, block_sums=None,
+                           stream=None):
+    """Expert-batched product: wq [E][N][K/2], wd [E][N][K/32]; rows grouped by expert."""
+    torch = _torch()
+    for t, n in ((wq, "wq"), (wd, "wd"), (xq, "xq"), (xd, "xd"), (expert_off, "expert_off")):
+        _cuda(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    E, N, K = wq.shape[0], wq.shape[1], wq.shape[2] * 2
+    if y is None:
+        y = torch.empty((R, N), dtype=torch.float32, device=wq.device)
+    ldy = _rows(y, "y")
+    S = None
+    if block_sums is True:
+        S = torch.empty((R, N, K // 32), dtype=torch.int32, device=wq.device)
+    elif block_sums is not None and block_sums is not False:
+        S = block_sums
+    st = lib().q4_0_x_q4_gemm_experts(_ptr(wq), _ptr(wd), E, _ptr(xq), _ptr(xd), _ptr(row_idx),
+                                      xq.shape[0], _ptr(expert_off), R, N, K, _ptr(y), ldy,
+                                      _ptr(S), _stream(stream))
+    _check("q4_0_x_q4_gemm_experts", st)
+    return (y, S) if S is not None else y
+
+
+def h32_device_status(stream=None) -> int:
+    """Synchronize the stream and return (and clear) the library's device status."""
+    return int(lib().h32_device_status(_stream(stream)))

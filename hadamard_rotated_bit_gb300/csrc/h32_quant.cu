@@ -122,11 +122,12 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const void *__restrict__
         const float d = __fdiv_rn(amax, kQmax);
         const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
 
-        // codes: round-half-even(clamp(y * id)); with a finite id the product
-        // is within [-qmax, qmax] up to rounding, so the clamp only matters
-        // when 1/d overflowed (a block of subnormal size)
+        // codes: round-half-even(clamp(y * id)).  With a finite amax and a
+        // finite id every product lies in [-qmax, qmax] up to rounding, so the
+        // clamp only matters when 1/d overflowed (a block of subnormal size) or
+        // the rotation itself overflowed to +-inf (products inf * 0 = NaN)
         uint32_t bits[32];
-        if (isinf(id)) {
+        if (!(amax < INFINITY) || isinf(id)) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 float t = __fmul_rn(v[i], id);

@@ -127,17 +127,20 @@ h32_status q4_0_x_q8_gemm(const uint8_t *wq, const uint16_t *wd, const int8_t *x
  * row r in [expert_off[e], expert_off[e+1]) uses expert e's weights and the
  * activation row row_idx[r] (row_idx = NULL means row r itself).
  *   wq          [E][N][K/2] Q4_0 codes;  wd [E][N][K/32] fp16 scales
- *   xq, xd      4-bit activations [T][K/2], [T][K/32] (T rows, any T)
- *   row_idx     device int32 [R] or NULL
+ *   xq, xd      4-bit activations [T][K/2], [T][K/32]
+ *   row_idx     device int32 [R] or NULL; entries outside [0, T) set
+ *               H32_ERR_DEVICE_GUARD and read as an all-zero row
+ *   T           rows of xq / xd (with row_idx = NULL, T must be >= R)
  *   expert_off  device int32 [E+1], non-decreasing, expert_off[0] = 0,
  *               expert_off[E] = R (checked on the device: a violation sets
  *               H32_ERR_DEVICE_GUARD and the kernel writes nothing)
  *   y           [R][ldy] fp32 out;  block_sums nullable int32 [R][N][K/32]
- * Requires N % 16 == 0.
+ * Requires N % 16 == 0 and 1 <= E <= 1024.
  */
 h32_status q4_0_x_q4_gemm_experts(const uint8_t *wq, const uint16_t *wd, int32_t E,
                                   const uint8_t *xq, const float *xd, const int32_t *row_idx,
-                                  const int32_t *expert_off, int64_t R, int64_t N, int64_t K,
+                                  int64_t T, const int32_t *expert_off, int64_t R, int64_t N,
+                                  int64_t K,
                                   float *y, int64_t ldy, int32_t *block_sums, void *stream);
 
 /*

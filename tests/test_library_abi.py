@@ -1,0 +1,91 @@
+"""The C-ABI library loads without a GPU, exports every entry point that
+include/h32.h declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import hadamard_rotated_bit_gb300 as h32
+from hadamard_rotated_bit_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return h32.lib()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "h32.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(h32_\w+|q4_0_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_path(lib):
+    names = _declared_functions()
+    for n in ("h32_quantize_act_q4", "h32_quantize_act_q8", "h32_rotate_quantize_weights_q4_0",
+              "q4_0_x_q4_gemm", "q4_0_x_q8_gemm", "q4_0_x_q4_gemm_experts", "h32_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+        assert n in h32.EXPORTED_SYMBOLS, n
+
+
+def test_status_strings(lib):
+    assert h32.h32_status_string(0) == "ok"
+    assert "aligned" in h32.h32_status_string(2)
+    assert h32.h32_version() >= 100
+
+
+def _call(fn, *args):
+    return getattr(h32.lib(), fn)(*args)
+
+
+def test_bad_arguments_rejected_before_launch(lib):
+    p = ctypes.c_void_p(256)   # never dereferenced: validation fails first
+    bad = ctypes.c_void_p(258)  # not 16-byte aligned
+    s = ctypes.c_void_p(0)
+    # K not a multiple of 32
+    assert _call("h32_quantize_act_q4", p, 1, 4, 33, 33, p, p, 1, s) == h32.H32_ERR_INVALID_ARG
+    # ldx < K
+    assert _call("h32_quantize_act_q8", p, 1, 4, 64, 32, p, p, 1, s) == h32.H32_ERR_INVALID_ARG
+    # bad dtype
+    assert _call("h32_quantize_act_q4", p, 7, 4, 64, 64, p, p, 1, s) == h32.H32_ERR_INVALID_ARG
+    # null pointer
+    assert _call("h32_quantize_act_q4", None, 1, 4, 64, 64, p, p, 1, s) == h32.H32_ERR_INVALID_ARG
+    # misaligned pointer / pitch
+    assert _call("h32_quantize_act_q4", bad, 1, 4, 64, 64, p, p, 1, s) == h32.H32_ERR_ALIGNMENT
+    assert _call("h32_quantize_act_q4", p, 1, 4, 64, 68, p, p, 1, s) == h32.H32_ERR_ALIGNMENT
+    assert _call("h32_rotate_quantize_weights_q4_0", p, 4, 48, 1, p, p, s) == h32.H32_ERR_INVALID_ARG
+    # empty input is valid and enqueues nothing
+    assert _call("h32_quantize_act_q4", p, 1, 0, 64, 64, p, p, 1, s) == h32.H32_OK
+
+
+def test_gemm_bad_arguments(lib):
+    p = ctypes.c_void_p(256)
+    s = ctypes.c_void_p(0)
+    # K not a multiple of 32, N not a multiple of 16, ldy < N
+    assert _call("q4_0_x_q4_gemm", p, p, p, p, 4, 16, 48, p, 16, None, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm", p, p, p, p, 4, 20, 64, p, 20, None, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q8_gemm", p, p, p, p, 4, 16, 64, p, 8, None, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_experts", p, p, 0, p, p, None, 4, p, 4, 16, 64, p, 16, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_experts", p, p, 2, p, p, None, 4, None, 4, 16, 64, p, 16, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm", p, p, p, p, 0, 16, 64, p, 16, None, s) == h32.H32_OK
+
+
+def test_no_device_is_reported_not_hidden(lib):
+    """On a machine without a GPU a valid call reports 'unsupported': there is no CPU fallback."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    p = ctypes.c_void_p(256)
+    s = ctypes.c_void_p(0)
+    assert _call("h32_quantize_act_q4", p, 1, 4, 64, 64, p, p, 1, s) == h32.H32_ERR_UNSUPPORTED

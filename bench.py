@@ -1,0 +1,469 @@
+"""Benchmark of the Hadamard-route prompt path on GB300.
+
+One step = one pass of the pp512 GEMM chain on the rotated 4-bit route: for
+each projection of a dense transformer layer (attention 5120 -> 5120, FFN
+gate/up 5120 -> 2 x 17408, FFN down 17408 -> 5120) rotate+quantize the 512
+tokens' bf16 activations to 4-bit codes, then run the block-scaled W4A4 GEMM
+against rotated Q4_0 weights.  Metric: prompt tokens per second.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+        (N > 1: launched by torch.distributed.run, one replica per GPU)
+
+Prints one JSON line (rank 0).  Inputs are synthetic (seeded), resident in HBM
+when the timed region starts; two weight/activation sets alternate between
+steps so each step's 165 MB of weights and 28 MB of activations exceed the
+129 MB L2 and no step reuses the previous step's data from L2.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from hadamard_rotated_bit_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "prompt tokens/s (pp512 GEMM chain) + int-MMA TOPS and act-quant GB/s vs GB300 peak"
+UNIT = "tokens/s"
+CHAIN = [wl.ATTN, wl.FFN_GATE_UP, wl.FFN_DOWN]
+M_TOKENS = 512
+WORKLOAD = ("pp512 GEMM chain, rotated 4-bit route: 512 tokens through attention "
+            "5120->5120, FFN gate/up 5120->34816, FFN down 17408->5120 "
+            "(quantize activations + W4A4 GEMM per projection)")
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_w4a4_pp512_ffn_gate_up.md")
+GEMM_SOURCE = os.path.join(ROOT, "hadamard_rotated_bit_gb300", "csrc", "h32_gemm.cu")
+SMS = 152
+FP32_LANES_PER_SM = 128   # FP32 FMA/FMUL lanes per SM per clock
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+# --------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """The slowest rank's time: every replica's work counts only when all finished."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# peaks and profile bookkeeping
+# --------------------------------------------------------------------------
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+def source_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(source sha256/16:\s*([0-9a-f]+)\)",
+                  text)
+    if not m or m.group(2) != source_sha(GEMM_SOURCE):
+        return None
+    return float(m.group(1))
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="h32clk", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# --------------------------------------------------------------------------
+# the chain on the device
+# --------------------------------------------------------------------------
+class Chain:
+    """Resident inputs, outputs and intermediate buffers of the pp512 chain."""
+
+    def __init__(self, torch, h32, device, sets=2, seed=0):
+        self.torch, self.h32, self.device = torch, h32, device
+        self.sets = []
+        base = []
+        for p in CHAIN:
+            cid = wl.CFG_ATTN if p is wl.ATTN else wl.CFG_FFN
+            w = torch.from_numpy(p.weights(seed, cid)).to(device)
+            wq, wd = h32.h32_rotate_quantize_weights_q4_0(w)
+            del w
+            xb = p.activations(M_TOKENS, seed, cid)
+            x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(device)
+            base.append((wq, wd, x))
+        for s in range(sets):
+            projs = []
+            for (wq, wd, x) in base:
+                projs.append({
+                    "wq": wq if s == 0 else wq.clone(), "wd": wd if s == 0 else wd.clone(),
+                    "x": x if s == 0 else x.clone(),
+                    "xq": torch.empty((M_TOKENS, x.shape[1] // 2), dtype=torch.uint8, device=device),
+                    "xd": torch.empty((M_TOKENS, x.shape[1] // 32), dtype=torch.float32,
+                                      device=device),
+                    "y": torch.empty((M_TOKENS, wq.shape[0]), dtype=torch.float32, device=device),
+                })
+            self.sets.append(projs)
+        torch.cuda.synchronize()
+
+    def step(self, s, stream, events=None):
+        """Enqueue one chain pass on `stream`; optionally bracket each kernel with events."""
+        h = self.h32
+        for i, p in enumerate(self.sets[s % len(self.sets)]):
+            if events is not None:
+                events[2 * i][0].record(stream)
+            h.h32_quantize_act_q4(p["x"], xq=p["xq"], xd=p["xd"], stream=stream)
+            if events is not None:
+                events[2 * i][1].record(stream)
+                events[2 * i + 1][0].record(stream)
+            h.q4_0_x_q4_gemm(p["wq"], p["wd"], p["xq"], p["xd"], y=p["y"], stream=stream)
+            if events is not None:
+                events[2 * i + 1][1].record(stream)
+
+
+def kernel_names():
+    names = []
+    for p in CHAIN:
+        names += [f"quantize_act_q4[{p.name}]", f"q4_0_x_q4_gemm[{p.name}]"]
+    return names
+
+
+def algorithmic(p):
+    """Per-launch algorithmic work of one projection (M = 512)."""
+    M, N, K = M_TOKENS, p.N, p.K
+    nb = K // 32
+    return {
+        "quant_bytes": M * K * 2 + M * K // 2 + M * nb * 4,       # bf16 in, nibbles + scales out
+        "gemm_alu_ops": 2 * M * N * nb,                            # d_w*d_x and one fma per block
+        "gemm_int_ops": 2 * M * N * K,                             # 2 MNK (multiply + add)
+        "gemm_bytes": N * K // 2 + N * nb * 2 + M * K // 2 + M * nb * 4 + M * N * 4,
+    }
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = init_dist(world, "nccl")
+    import hadamard_rotated_bit_gb300 as h32
+    from hadamard_rotated_bit_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(dist, device)
+    h32.lib()
+
+    chain = Chain(torch, h32, device)
+    stream = torch.cuda.Stream(device)
+    peaks, peak_src = load_peaks()
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            chain.step(i, stream)
+    stream.synchronize()
+    if h32.h32_device_status(stream) != 0:
+        raise RuntimeError("device status not OK after warm-up")
+
+    # timed region: device-resident inputs, per-kernel events on the launch stream
+    nk = 2 * len(CHAIN)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(nk)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(args.steps):
+            chain.step(i, stream, evs[i])
+        t1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(dist, device)
+    elapsed_ms = t0.elapsed_time(t1)
+    elapsed_ms = max_over_ranks(dist, elapsed_ms, device)
+    status = h32.h32_device_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    per_kernel = np.zeros(nk)
+    for i in range(args.steps):
+        for k in range(nk):
+            per_kernel[k] += evs[i][k][0].elapsed_time(evs[i][k][1])
+    per_kernel /= args.steps  # ms per launch
+
+    tokens = M_TOKENS * args.steps * world
+    value = tokens / (elapsed_ms / 1e3)
+    ms_per_step = elapsed_ms / args.steps
+
+    # end to end through host buffers: H2D of the step's activations, the
+    # chain, D2H of the step's outputs, all inside the timed region
+    e2e = time_e2e(torch, h32, chain, stream, args, dist, device, world)
+
+    # roofline of the dominant kernel
+    names = kernel_names()
+    dom = int(np.argmax(per_kernel))
+    p = CHAIN[dom // 2]
+    alg = algorithmic(p)
+    clock_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    if dom % 2 == 1:
+        alu_peak = SMS * FP32_LANES_PER_SM * clock_mhz * 1e6 / 1e12  # T lane-ops/s
+        achieved = alg["gemm_alu_ops"] / (per_kernel[dom] / 1e3) / 1e12
+        roofline = {"kernel": names[dom], "bound": "alu", "achieved": round(achieved, 3),
+                    "peak": round(alu_peak, 3), "unit": "Tops/s (fp32 lane ops)",
+                    "frac": round(achieved / alu_peak, 4), "traffic": profiled_traffic(),
+                    "peak_source": f"{SMS} SMs x {FP32_LANES_PER_SM} FP32 lanes x "
+                                   f"{clock_mhz:.0f} MHz ({peak_src} max SM clock)",
+                    "algorithmic_per_launch": alg["gemm_alu_ops"],
+                    "ms_per_launch": round(per_kernel[dom], 5)}
+    else:
+        achieved = alg["quant_bytes"] / (per_kernel[dom] / 1e3) / 1e9
+        roofline = {"kernel": names[dom], "bound": "hbm", "achieved": round(achieved, 1),
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None}
+
+    # secondary views of the same timed launches
+    int8_peak = 252 * 2 * SMS * clock_mhz * 1e6 / 1e12    # measured mma.sync s8 MAC/clk/SM
+    fp8_peak = 2.0 * float(peaks["bf16_tflops"])           # nominal fp8 : bf16 ratio 2
+    kernels = {}
+    for i, p in enumerate(CHAIN):
+        alg = algorithmic(p)
+        tq, tg = per_kernel[2 * i], per_kernel[2 * i + 1]
+        kernels[p.name] = {
+            "quant_ms": round(tq, 5),
+            "quant_GBps": round(alg["quant_bytes"] / (tq / 1e3) / 1e9, 1),
+            "quant_hbm_frac": round(alg["quant_bytes"] / (tq / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "gemm_ms": round(tg, 5),
+            "gemm_eff_TOPS": round(alg["gemm_int_ops"] / (tg / 1e3) / 1e12, 1),
+            "gemm_frac_of_int8_mma_peak": round(alg["gemm_int_ops"] / (tg / 1e3) / 1e12 / int8_peak, 3),
+            "gemm_frac_of_fp8_tensor_peak": round(alg["gemm_int_ops"] / (tg / 1e3) / 1e12 / fp8_peak, 4),
+            "gemm_alu_frac": round(alg["gemm_alu_ops"] / (tg / 1e3) / 1e12 /
+                                   (SMS * FP32_LANES_PER_SM * clock_mhz * 1e6 / 1e12), 4),
+        }
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int4 codes (exact products), fp32 epilogue", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens_per_step": M_TOKENS,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: two alternating input sets of 193 MB each"},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": nk * args.steps,
+        "clocks": clocks,
+        "kernels": kernels,
+        "peaks": {"int8_mma_sync_TOPS": round(int8_peak, 1), "fp8_tensor_TFLOPS": fp8_peak,
+                  "hbm_GBps": peaks["hbm_gbs"], "source": peak_src},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_tokens)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def time_e2e(torch, h32, chain, stream, args, dist, device, world):
+    projs = chain.sets[0]
+    host_x = [p["x"].cpu().pin_memory() for p in projs]
+    host_y = [torch.empty(p["y"].shape, dtype=torch.float32).pin_memory() for p in projs]
+    h2d = sum(t.numel() * t.element_size() for t in host_x)
+    d2h = sum(t.numel() * t.element_size() for t in host_y)
+    steps = max(3, min(args.steps, 50))
+
+    def one(s):
+        pset = chain.sets[s % len(chain.sets)]
+        for p, hx in zip(pset, host_x):
+            p["x"].copy_(hx, non_blocking=True)
+        chain.step(s, stream)
+        for p, hy in zip(pset, host_y):
+            hy.copy_(p["y"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for s in range(3):
+            one(s)
+    stream.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for s in range(steps):
+            one(s)
+        t1.record(stream)
+    stream.synchronize()
+    ms = max_over_ranks(dist, t0.elapsed_time(t1), device)
+    return {"value": round(M_TOKENS * steps * world / (ms / 1e3), 1), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+# --------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline / reference arm)
+# --------------------------------------------------------------------------
+def cpu_baseline(sample_tokens: int):
+    """Time the CPU oracle, as it stands, on a bounded sample of the same
+    workload: `sample_tokens` of the 512 tokens through the whole chain
+    (quantize + GEMM for all three projections).  The oracle's offline weight
+    quantization is done first and not timed."""
+    import oracle
+    oracle.build()
+    prepared = []
+    for p in CHAIN:
+        cid = wl.CFG_ATTN if p is wl.ATTN else wl.CFG_FFN
+        wq, wd = oracle.quantize_weights_q4_0(p.weights(0, cid))
+        x = p.activations(M_TOKENS, 0, cid)[:sample_tokens]
+        prepared.append((wq, wd, x, p.K))
+    t = time.perf_counter()
+    for wq, wd, x, K in prepared:
+        xq, xd = oracle.quantize_act_q4(x)
+        oracle.gemm(wq, wd, xq, xd, K)
+    dt = time.perf_counter() - t
+    return {"value": round(sample_tokens / dt, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"{sample_tokens} of the 512 tokens through the whole chain "
+                      f"(3 quantizations + 3 full GEMMs), single-threaded C oracle"}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return None
+    per_step = []
+    for _ in range(args.warmup):
+        cpu_baseline(args.ref_tokens)
+    for _ in range(args.steps):
+        per_step.append(cpu_baseline(args.ref_tokens))
+    secs = sum(r["seconds"] for r in per_step)
+    value = args.ref_tokens * len(per_step) / secs
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / len(per_step), 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int64 block sums, fp32 epilogue",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens_per_step": args.ref_tokens,
+                       "note": "each step is a bounded sample of the pp512 chain"},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": per_step[0]["sample"]},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["h32", "reference"], default="h32")
+    ap.add_argument("--cpu-tokens", type=int, default=2)
+    ap.add_argument("--ref-tokens", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

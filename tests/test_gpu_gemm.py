@@ -40,6 +40,18 @@ def rel_err(got, ref):
     return np.abs(got - ref) / np.maximum(np.abs(ref), floor)
 
 
+def f64_excess(got, r64, wd, xd_rows, S):
+    """Error against the fp64 result in units of its allowance,
+    max(1e-3 |y64|, (nb + 1) 2^-24 sum_b |d_w d_x S_b|): 1e-3 relative, or the
+    forward error bound of fp32 recursive summation for outputs that cancel.
+    wd: [P][nb] fp16 bits, xd_rows: [P][nb], S: [P][nb] -> values <= 1 pass."""
+    nb = S.shape[-1]
+    terms = np.abs(wd.view(np.float16).astype(np.float64) * xd_rows.astype(np.float64) * S)
+    allow = np.maximum(REL_F64 * np.abs(r64), (nb + 1) * 2.0 ** -24 * terms.sum(axis=-1))
+    allow = np.maximum(allow, 1e-300)
+    return np.abs(np.asarray(got, np.float64) - r64) / allow
+
+
 def operands(M, N, K, xbits, seed_tid, outlier_frac=0.01, outlier_scale=20.0, rotate=True):
     x = wl.act_normal_outliers(M, K, outlier_frac, outlier_scale, 0, wl.CFG_TEST, seed_tid)
     w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, seed_tid + 1)
@@ -70,7 +82,10 @@ def check_full(h32, wq, wd, xq, xd, K, xbits):
     assert np.array_equal(S.astype(np.int64), rS), "block sums differ"
     assert rel_err(y, r32).max() <= REL_F32
     assert np.array_equal(y.view(np.uint32), r32.view(np.uint32)), "fp32 outputs not bit-identical"
-    assert rel_err(y, r64).max() <= REL_F64
+    M, N, nb = rS.shape
+    ex = f64_excess(y, r64, np.broadcast_to(wd[None], (M, N, nb)),
+                    np.broadcast_to(xd[:, None, :], (M, N, nb)), rS)
+    assert ex.max() <= 1.0
 
 
 @pytest.mark.parametrize("xbits", [4, 8])
@@ -171,10 +186,10 @@ def sampled_check(h32, wq, wd, xq, xd, K, xbits, nsamp=3000, seed=0):
     r = np.random.default_rng(seed)
     mi = np.concatenate([r.integers(0, M, nsamp), [0, M - 1, M - 1, 0]])
     ni = np.concatenate([r.integers(0, N, nsamp), [0, N - 1, 0, N - 1]])
-    r32, r64, _ = oracle.gemm_sampled(wq, wd, xq, xd, K, mi, ni)
+    r32, r64, rS = oracle.gemm_sampled(wq, wd, xq, xd, K, mi, ni, want_block_sums=True)
     got = y[mi, ni]
     assert np.array_equal(got.view(np.uint32), r32.view(np.uint32))
-    assert rel_err(got, r64).max() <= REL_F64
+    assert f64_excess(got, r64, wd[ni], xd[mi], rS).max() <= 1.0
     assert np.isfinite(y).all()
 
 
@@ -300,7 +315,9 @@ def test_moe_config_sampled(h32):
         R = int(off[-1])
         ri = np.concatenate([r.integers(0, R, 3000), off[1:-1].astype(np.int64), [R - 1]])
         ni = r.integers(0, N, ri.size)
-        r32, r64, _ = oracle.gemm_experts_sampled(wq, wd, xq, xd, ridx, off, N, K, ri, ni)
+        r32, r64, rS = oracle.gemm_experts_sampled(wq, wd, xq, xd, ridx, off, N, K, ri, ni, True)
         got = y[ri, ni]
         assert np.array_equal(got.view(np.uint32), r32.view(np.uint32))
-        assert rel_err(got, r64).max() <= REL_F64
+        e = np.searchsorted(off, ri, side="right") - 1
+        xrow = ri if ridx is None else ridx[ri]
+        assert f64_excess(got, r64, wd[e, ni], xd[xrow], rS).max() <= 1.0

@@ -21,7 +21,12 @@ __all__ = [
     "h32_quantize_act_q4", "h32_quantize_act_q8", "h32_rotate_quantize_weights_q4_0",
     "q4_0_x_q4_gemm", "q4_0_x_q8_gemm", "q4_0_x_q4_gemm_experts",
     "h32_device_status", "h32_status_string", "h32_set_wait_limit", "h32_version",
+    "h32_last_cuda_error",
 ]
+
+
+def h32_last_cuda_error() -> str:
+    return lib().h32_last_cuda_error().decode()
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_PKG, "lib", "libh32.so")
@@ -45,6 +50,7 @@ _SIGS = {
     "h32_status_string": (ctypes.c_char_p, [_INT]),
     "h32_set_wait_limit": (None, [ctypes.c_uint64]),
     "h32_version": (_INT, []),
+    "h32_last_cuda_error": (ctypes.c_char_p, []),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -55,7 +61,10 @@ _lock = threading.Lock()
 class H32Error(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn}: {h32_status_string(status)} (status {status})")
+        msg = f"{fn}: {h32_status_string(status)} (status {status})"
+        if status == H32_ERR_CUDA:
+            msg += f": {lib().h32_last_cuda_error().decode()}"
+        super().__init__(msg)
 
 
 def lib() -> ctypes.CDLL:

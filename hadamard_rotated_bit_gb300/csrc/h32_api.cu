@@ -22,7 +22,17 @@ std::mutex g_dev_mutex;
 
 uint64_t wait_limit() { return g_wait_polls.load(std::memory_order_relaxed); }
 
-h32_status launch_status(cudaError_t e) { return e == cudaSuccess ? H32_OK : H32_ERR_CUDA; }
+namespace {
+thread_local const char *t_last_cuda_error = "no error";
+}
+
+h32_status launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return H32_OK;
+    t_last_cuda_error = cudaGetErrorString(e);
+    return H32_ERR_CUDA;
+}
+
+void note_error(const char *what) { t_last_cuda_error = what; }
 
 h32_status check_device(int *sm_count) {
     int dev = -1;
@@ -54,7 +64,8 @@ h32_status check_device(int *sm_count) {
 extern "C" h32_status h32_device_status(void *stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     H32_TRY(h32::check_device(nullptr));
-    if (cudaStreamSynchronize(s) != cudaSuccess) return H32_ERR_CUDA;
+    const cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return h32::launch_status(e);
     h32_status a = h32::quant_read_and_clear_status(s);
     h32_status b = h32::gemm_read_and_clear_status(s);
     if (a == H32_ERR_CUDA || b == H32_ERR_CUDA) return H32_ERR_CUDA;
@@ -81,3 +92,5 @@ extern "C" void h32_set_wait_limit(uint64_t polls) {
 }
 
 extern "C" int h32_version(void) { return 100; }
+
+extern "C" const char *h32_last_cuda_error(void) { return h32::t_last_cuda_error; }

@@ -28,7 +28,8 @@ constexpr uint64_t kDefaultWaitPolls = 1ull << 22;
 // host side -----------------------------------------------------------------
 uint64_t wait_limit();                    // current bound (never 0)
 h32_status check_device(int *sm_count);   // an sm_103 device is current
-h32_status launch_status(cudaError_t e);  // map a launch error
+h32_status launch_status(cudaError_t e);  // map a CUDA error (and remember its text)
+void note_error(const char *what);        // remember a non-CUDA failure text
 
 // per-translation-unit status readers (each .cu file owns its status word)
 h32_status quant_read_and_clear_status(cudaStream_t s);

@@ -47,7 +47,6 @@ namespace {
 
 __device__ uint32_t g_gemm_status;
 
-constexpr int kThreads = 448;             // 14 warps
 constexpr int kBM = 128;                  // weight rows per tile
 constexpr int kBNMax = 128;               // tokens per tile
 constexpr int kStageBlocks = 4;           // 32-blocks per pipeline stage
@@ -59,17 +58,19 @@ constexpr uint64_t kDrainPolls = 1ull << 22;
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpConv0 = 2, kNumConv = 4, kWarpEpi0 = 6;
 constexpr int kConvThreads = kNumConv * 32;  // 128
-constexpr int kEpiThreads = 8 * 32;          // 256
 
 constexpr int kNibBytes = kBM * 64;          // one stage of weight nibbles (8 KB)
-constexpr int kOpBytes = kBNMax * 128;       // one widened operand stage (16 KB)
+// one widened operand stage: 16 row groups of 8 K-chunks of 16-byte core-matrix rows
+constexpr int kOpBytes = (kBNMax / 8) * 1152;  // 18 KB
 constexpr int kScaleBytes = kStageBlocks * kBNMax * 4;  // 2 KB
 
-// the MMA's view of a widened operand tile: core matrix (row group g, K chunk c)
-// at g * 1024 + c * 128; K-direction stride 128 B, M/N-direction stride 1024 B
-constexpr uint32_t kLBO = 128, kSBO = 1024;
+// The MMA's view of a widened operand tile: core matrix (row group g, K chunk
+// c) at g * 1152 + c * 144.  The K-direction stride of 144 bytes (not 128)
+// staggers the chunks by four banks, so the converters' 16-byte stores of
+// eight rows x four blocks per warp phase hit 32 distinct banks.
+constexpr uint32_t kLBO = 144, kSBO = 1152;
 __device__ __forceinline__ uint32_t op_offset(int r, int chunk) {
-    return (r >> 3) * 1024 + chunk * 128 + (r & 7) * 16;
+    return (r >> 3) * kSBO + chunk * kLBO + (r & 7) * 16;
 }
 
 template <int XB>
@@ -77,6 +78,17 @@ struct Cfg {
     static constexpr int kBOps = (XB == 4) ? 1 : 2;      // B operands per stage (q8: hi, lo)
     static constexpr int kSBufs = (XB == 4) ? 4 : 2;     // blocks in flight in TMEM
     static constexpr int kSCols = (XB == 4) ? 128 : 256; // TMEM columns per block
+    // epilogue warps per TMEM lane quadrant (each takes an even share of the
+    // tile's 16-column chunks)
+    static constexpr int kEpiPerQuad = 2;
+    static constexpr int kEpiWarps = 4 * kEpiPerQuad;
+    static constexpr int kEpiThreads = kEpiWarps * 32;
+    static constexpr int kMaxChunks = (8 + kEpiPerQuad - 1) / kEpiPerQuad;  // 16-column chunks
+    static constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
+    // the register file (64K) is granted per 128-thread group of warps
+    static constexpr int kMaxRegs = (65536 / ((kThreads + 127) / 128 * 128)) & ~7;
+    // two TMEM loads in flight per wait when the registers allow it
+    static constexpr bool kPairLoads = kMaxChunks <= 3;
     // shared memory map (offsets from a 1024-aligned base)
     static constexpr int kOffNib = 0;
     static constexpr int kOffA = kOffNib + kNibStages * kNibBytes;
@@ -188,13 +200,209 @@ __device__ __forceinline__ void split_q8(uint32_t w, uint32_t &h, uint32_t &l) {
     h = ((t ^ 0x80808080u) & m) | ((0x88888888u - h8) & ~m);
 }
 
+// packed fp32 pairs (low half = first element); IEEE round-to-nearest-even per lane
+__device__ __forceinline__ uint64_t pair_of(uint32_t lo, uint32_t hi) {
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// 16 columns of one block into the accumulators: acc = fma(fp32(dw * dx), S, acc),
+// two columns per packed operation; dx and S come in as pairs already
+__device__ __forceinline__ void fold16(uint64_t *acc, float dw, const float *dx,
+                                       const uint32_t (&v)[16]) {
+    const uint32_t w = __float_as_uint(dw);
+    const uint64_t dw2 = pair_of(w, w);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const ulonglong2 d = *reinterpret_cast<const ulonglong2 *>(dx + 4 * q);
+        acc[2 * q] = fma_f32x2(mul_f32x2(dw2, d.x), pair_of(v[4 * q], v[4 * q + 1]), acc[2 * q]);
+        acc[2 * q + 1] =
+            fma_f32x2(mul_f32x2(dw2, d.y), pair_of(v[4 * q + 2], v[4 * q + 3]), acc[2 * q + 1]);
+    }
+}
+
+// the same when some d_w * d_x falls outside the normal range: round the
+// product of the unscaled scales itself, then apply the 2^18 exactly
+__device__ __forceinline__ void fold16_exact(uint64_t *acc, float dw, const float *dx,
+                                          const uint32_t (&v)[16]) {
+    const float dw0 = dw * 0x1p-18f;
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        const uint64_t pr = acc[i / 2];
+        const float s0 = __fmul_rn(__fmul_rn(dw0, dx[i]), 262144.0f);
+        const float s1 = __fmul_rn(__fmul_rn(dw0, dx[i + 1]), 262144.0f);
+        const float a0 = __fmaf_rn(s0, __uint_as_float(v[i]), __uint_as_float(static_cast<uint32_t>(pr)));
+        const float a1 =
+            __fmaf_rn(s1, __uint_as_float(v[i + 1]), __uint_as_float(static_cast<uint32_t>(pr >> 32)));
+        acc[i / 2] = pair_of(__float_as_uint(a0), __float_as_uint(a1));
+    }
+}
+
+// activation items and weight-scale items of one stage, held in registers
+// between their global loads and their use
 template <int XB>
-__global__ void __launch_bounds__(kThreads, 1)
+struct StageRegs {
+    uint4 q[4][XB == 4 ? 1 : 2];
+    float dx[4];
+    uint32_t wd[4];
+};
+
+template <int XB>
+__device__ __forceinline__ void load_stage(const GemmArgs &a, const Tile &ti, int st, int ct,
+                                           StageRegs<XB> &R) {
+    const int64_t xrow_bytes = (XB == 4) ? a.K / 2 : a.K;
+    const int nb = a.nb;
+    const int kb0 = st * kStageBlocks;
+    const int nblk = min(kStageBlocks, nb - kb0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = ct + k * kConvThreads;
+        const int m = i >> 2, j = i & 3;
+        bool valid = (m < ti.rows) && (j < nblk);
+        int64_t tok = 0;
+        if (valid) {
+            const int64_t r = ti.g0 + m;
+            tok = a.row_idx ? a.row_idx[r] : r;
+            if (tok < 0 || tok >= a.T) {
+                record(kStatusGuard);
+                valid = false;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < (XB == 4 ? 1 : 2); ++h) R.q[k][h] = make_uint4(0, 0, 0, 0);
+        R.dx[k] = 0.0f;
+        if (valid) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + tok * xrow_bytes +
+                                                               (kb0 + j) * (XB == 4 ? 16 : 32));
+#pragma unroll
+            for (int h = 0; h < (XB == 4 ? 1 : 2); ++h) R.q[k][h] = __ldg(src + h);
+            R.dx[k] = __ldg(a.xd + tok * nb + kb0 + j);
+        }
+    }
+    const int wrow0 = ti.e * a.N + ti.n0;
+    const int nvalid_w = min(kBM, a.N - ti.n0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = ct + k * kConvThreads;
+        const int r = i >> 2, j = i & 3;
+        R.wd[k] = (r < nvalid_w && j < nblk)
+                      ? static_cast<uint32_t>(__ldg(a.wd + static_cast<int64_t>(wrow0 + r) * nb +
+                                                    kb0 + j))
+                      : 0u;
+    }
+}
+
+// Widen one stage: activation items from registers, weight nibbles from the
+// TMA tile; stage the scales.  Returns false when a wait gave up.
+template <int XB>
+__device__ __forceinline__ bool convert_stage(const GemmArgs &a, const Tile &ti, int st, uint32_t ks,
+                                              int ct, int lane, int cw, const StageRegs<XB> &R,
+                                              uint8_t *s_nib, uint8_t *s_a, uint8_t *s_b,
+                                              float *s_dw, float *s_dx, uint64_t *bars,
+                                              volatile int *misc, uint64_t lim,
+                                              volatile int *abort_flag) {
+    constexpr int kBOps = Cfg<XB>::kBOps;
+    const int cs = ks % kConvStages, ns = ks % kNibStages;
+    const int kb0 = st * kStageBlocks;
+    const int nblk = min(kStageBlocks, a.nb - kb0);
+    if (!warp_wait(&bars[kBarConvEmpty + cs], ((ks / kConvStages) & 1) ^ 1, lim, abort_flag)) {
+        set_abort(misc);
+        return false;
+    }
+    uint8_t *bdst = s_b + cs * kBOps * kOpBytes;
+    float *dx_dst = s_dx + cs * (kStageBlocks * kBNMax);
+    bool slow = false;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = ct + k * kConvThreads;
+        const int m = i >> 2, j = i & 3;
+        if (m < ti.ncols) {
+            if constexpr (XB == 4) {
+                const uint4 q = R.q[k][0];
+                uint32_t lo[4], hi[4];
+                widen8(q.x, lo[0], hi[0]);
+                widen8(q.y, lo[1], hi[1]);
+                widen8(q.z, lo[2], hi[2]);
+                widen8(q.w, lo[3], hi[3]);
+                *reinterpret_cast<uint4 *>(bdst + op_offset(m, 2 * j)) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                *reinterpret_cast<uint4 *>(bdst + op_offset(m, 2 * j + 1)) =
+                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            } else {
+                const uint4 q0 = R.q[k][0], q1 = R.q[k][1];
+                const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                uint32_t h[8], l[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) split_q8(w8[u], h[u], l[u]);
+                // elements 0..15 -> chunk 2j, 16..31 -> chunk 2j + 1
+                *reinterpret_cast<uint4 *>(bdst + op_offset(m, 2 * j)) =
+                    make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4 *>(bdst + op_offset(m, 2 * j + 1)) =
+                    make_uint4(h[4], h[5], h[6], h[7]);
+                *reinterpret_cast<uint4 *>(bdst + kOpBytes + op_offset(m, 2 * j)) =
+                    make_uint4(l[0], l[1], l[2], l[3]);
+                *reinterpret_cast<uint4 *>(bdst + kOpBytes + op_offset(m, 2 * j + 1)) =
+                    make_uint4(l[4], l[5], l[6], l[7]);
+            }
+            const float dx = R.dx[k];
+            const float adx = fabsf(dx);
+            if (dx != 0.0f && !(adx >= 0x1p-100f && adx <= 0x1p90f)) slow = true;
+            dx_dst[j * kBNMax + m] = dx;
+        }
+    }
+    // weights (TMA tile): item -> row r = i / 4, block j = i % 4
+    if (!warp_wait(&bars[kBarNibFull + ns], (ks / kNibStages) & 1, lim, abort_flag)) {
+        set_abort(misc);
+        return false;
+    }
+    uint8_t *adst = s_a + cs * kOpBytes;
+    float *dw_dst = s_dw + cs * (kStageBlocks * kBNMax);
+    const uint8_t *nib = s_nib + ns * kNibBytes;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = ct + k * kConvThreads;
+        const int r = i >> 2, j = i & 3;
+        const uint4 q = *reinterpret_cast<const uint4 *>(nib + r * 64 + j * 16);
+        // Q4_0 code c means c - 8: flipping the top bit of each nibble gives
+        // that value in two's complement
+        uint32_t lo[4], hi[4];
+        widen8(q.x ^ 0x88888888u, lo[0], hi[0]);
+        widen8(q.y ^ 0x88888888u, lo[1], hi[1]);
+        widen8(q.z ^ 0x88888888u, lo[2], hi[2]);
+        widen8(q.w ^ 0x88888888u, lo[3], hi[3]);
+        *reinterpret_cast<uint4 *>(adst + op_offset(r, 2 * j)) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4 *>(adst + op_offset(r, 2 * j + 1)) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(R.wd[k])));
+        // fold in the 2^18 of the MMA's operand encoding (exact)
+        dw_dst[j * kBNMax + r] = dw * 262144.0f;
+    }
+    mbar_arrive(&bars[kBarNibEmpty + ns]);
+    const unsigned any_slow = __any_sync(0xFFFFFFFFu, slow);
+    if (lane == 0) misc[kMiscSlow + cs * kNumConv + cw] = any_slow ? 1 : 0;
+    fence_proxy_async_smem();
+    mbar_arrive(&bars[kBarConvFull + cs]);
+    return true;
+}
+
+template <int XB, bool kSums>
+__global__ void __launch_bounds__(Cfg<XB>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a) {
     using C = Cfg<XB>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // align by offsetting the __shared__ pointer itself (a round trip through
+    // an integer would turn every shared access into a generic one)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *s_nib = smem + C::kOffNib;
     uint8_t *s_a = smem + C::kOffA;
     uint8_t *s_b = smem + C::kOffB;
@@ -221,11 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kConvStages; ++i) {
             mbar_init(&bars[kBarConvFull + i], kConvThreads);
-            mbar_init(&bars[kBarConvEmpty + i], 1 + kEpiThreads);
+            mbar_init(&bars[kBarConvEmpty + i], 1 + C::kEpiThreads);
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&bars[kBarSFull + i], 1);
-            mbar_init(&bars[kBarSEmpty + i], kEpiThreads);
+            mbar_init(&bars[kBarSEmpty + i], C::kEpiThreads);
         }
         mbar_init(&bars[kBarDrain], 1);
         misc[kMiscAbort] = 0;
@@ -238,11 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_off[1] = static_cast<int>(a.R);
         }
     } else {
-        for (int i = tid; i <= E; i += kThreads) s_off[i] = a.expert_off[i];
+        for (int i = tid; i <= E; i += C::kThreads) s_off[i] = a.expert_off[i];
     }
     __syncthreads();
     if (!dense) {
-        for (int i = tid; i <= E; i += kThreads) {
+        for (int i = tid; i <= E; i += C::kThreads) {
             const int v = s_off[i];
             bool bad = (i == 0 && v != 0) || (i == E && static_cast<int64_t>(v) != a.R) ||
                        (i < E && s_off[i + 1] < v);
@@ -356,16 +564,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t ad = smem_desc_noswizzle(a_base + j * 256, kLBO, kSBO);
+                        const uint64_t ad = smem_desc_noswizzle(a_base + j * 2 * kLBO, kLBO, kSBO);
                         const uint32_t d = tmem + buf * C::kSCols;
                         if constexpr (XB == 4) {
-                            mma_f8f6f4(d, ad, smem_desc_noswizzle(b_base + j * 256, kLBO, kSBO),
+                            mma_f8f6f4(d, ad,
+                                       smem_desc_noswizzle(b_base + j * 2 * kLBO, kLBO, kSBO),
                                        idesc, 0);
                         } else {
-                            mma_f8f6f4(d, ad, smem_desc_noswizzle(b_base + j * 256, kLBO, kSBO),
+                            mma_f8f6f4(d, ad,
+                                       smem_desc_noswizzle(b_base + j * 2 * kLBO, kLBO, kSBO),
                                        idesc, 0);
                             mma_f8f6f4(d + 128, ad,
-                                       smem_desc_noswizzle(b_base + kOpBytes + j * 256, kLBO, kSBO),
+                                       smem_desc_noswizzle(b_base + kOpBytes + j * 2 * kLBO, kLBO,
+                                                           kSBO),
                                        idesc, 0);
                         }
                         mma_commit(&bars[kBarSFull + buf]);
@@ -380,145 +591,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < kWarpEpi0) {
         // ------------------------------------------------------ converters
+        // Each thread owns four activation items (token m, block j) and four
+        // weight items (row r, block j) per stage; the global loads of the
+        // next stage are issued before the current stage is widened, so their
+        // latency hides behind the widening work.
         const int ct = tid - kWarpConv0 * 32;  // 0..127
         const int cw = warp - kWarpConv0;
-        const int64_t xrow_bytes = (XB == 4) ? a.K / 2 : a.K;
         uint32_t ks = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile ti = decode_tile(t, E, s_off, s_tpre, a.bn);
-            const int wrow0 = ti.e * a.N + ti.n0;
-            const int nvalid_w = min(kBM, a.N - ti.n0);
-            for (int st = 0; st < nst; ++st, ++ks) {
-                const int cs = ks % kConvStages, ns = ks % kNibStages;
-                const int kb0 = st * kStageBlocks;
-                const int nblk = min(kStageBlocks, nb - kb0);
-                if (!warp_wait(&bars[kBarConvEmpty + cs], ((ks / kConvStages) & 1) ^ 1, lim,
-                               abort_flag)) {
-                    set_abort(misc);
-                    ok = false;
-                    break;
-                }
-                uint8_t *bdst = s_b + cs * C::kBOps * kOpBytes;
-                float *dx_dst = s_dx + cs * (kStageBlocks * kBNMax);
-                bool slow = false;
-                // activations: item i -> token m = i / 4, block j = i % 4
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int i = ct + k * kConvThreads;
-                    const int m = i >> 2, j = i & 3;
-                    if (m < ti.ncols) {
-                        bool valid = (m < ti.rows) && (j < nblk);
-                        int64_t tok = 0;
-                        if (valid) {
-                            const int64_t r = ti.g0 + m;
-                            tok = a.row_idx ? a.row_idx[r] : r;
-                            if (tok < 0 || tok >= a.T) {
-                                record(kStatusGuard);
-                                valid = false;
-                            }
-                        }
-                        float dx = 0.0f;
-                        if constexpr (XB == 4) {
-                            uint4 q = make_uint4(0, 0, 0, 0);
-                            if (valid) {
-                                q = __ldg(reinterpret_cast<const uint4 *>(
-                                    a.xq + tok * xrow_bytes + (kb0 + j) * 16));
-                                dx = __ldg(a.xd + tok * nb + kb0 + j);
-                            }
-                            uint32_t lo[4], hi[4];
-                            widen8(q.x, lo[0], hi[0]);
-                            widen8(q.y, lo[1], hi[1]);
-                            widen8(q.z, lo[2], hi[2]);
-                            widen8(q.w, lo[3], hi[3]);
-                            *reinterpret_cast<uint4 *>(bdst + op_offset(m, 2 * j)) =
-                                make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                            *reinterpret_cast<uint4 *>(bdst + op_offset(m, 2 * j + 1)) =
-                                make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        } else {
-                            uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
-                            if (valid) {
-                                const uint4 *src = reinterpret_cast<const uint4 *>(
-                                    a.xq + tok * xrow_bytes + (kb0 + j) * 32);
-                                q0 = __ldg(src);
-                                q1 = __ldg(src + 1);
-                                dx = __ldg(a.xd + tok * nb + kb0 + j);
-                            }
-                            uint32_t h[8], l[8];
-                            const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) split_q8(w8[u], h[u], l[u]);
-                            // elements 0..15 -> chunk 2j, 16..31 -> chunk 2j + 1
-                            *reinterpret_cast<uint4 *>(bdst + op_offset(m, 2 * j)) =
-                                make_uint4(h[0], h[1], h[2], h[3]);
-                            *reinterpret_cast<uint4 *>(bdst + op_offset(m, 2 * j + 1)) =
-                                make_uint4(h[4], h[5], h[6], h[7]);
-                            *reinterpret_cast<uint4 *>(bdst + kOpBytes + op_offset(m, 2 * j)) =
-                                make_uint4(l[0], l[1], l[2], l[3]);
-                            *reinterpret_cast<uint4 *>(bdst + kOpBytes + op_offset(m, 2 * j + 1)) =
-                                make_uint4(l[4], l[5], l[6], l[7]);
-                        }
-                        const float adx = fabsf(dx);
-                        if (dx != 0.0f && !(adx >= 0x1p-100f && adx <= 0x1p90f)) slow = true;
-                        dx_dst[j * kBNMax + m] = dx;
-                    }
-                }
-                // weights (TMA tile): item i -> row r = i / 4, block j = i % 4
-                if (!warp_wait(&bars[kBarNibFull + ns], (ks / kNibStages) & 1, lim, abort_flag)) {
-                    set_abort(misc);
-                    ok = false;
-                    break;
-                }
-                uint8_t *adst = s_a + cs * kOpBytes;
-                float *dw_dst = s_dw + cs * (kStageBlocks * kBNMax);
-                const uint8_t *nib = s_nib + ns * kNibBytes;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int i = ct + k * kConvThreads;
-                    const int r = i >> 2, j = i & 3;
-                    const uint4 q = *reinterpret_cast<const uint4 *>(nib + r * 64 + j * 16);
-                    // Q4_0 code c means c - 8: flipping the top bit of each
-                    // nibble gives that value in two's complement
-                    uint32_t lo[4], hi[4];
-                    widen8(q.x ^ 0x88888888u, lo[0], hi[0]);
-                    widen8(q.y ^ 0x88888888u, lo[1], hi[1]);
-                    widen8(q.z ^ 0x88888888u, lo[2], hi[2]);
-                    widen8(q.w ^ 0x88888888u, lo[3], hi[3]);
-                    *reinterpret_cast<uint4 *>(adst + op_offset(r, 2 * j)) =
-                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    *reinterpret_cast<uint4 *>(adst + op_offset(r, 2 * j + 1)) =
-                        make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    float dw = 0.0f;
-                    if (r < nvalid_w && j < nblk)
-                        dw = __half2float(__ushort_as_half(
-                            __ldg(a.wd + static_cast<int64_t>(wrow0 + r) * nb + kb0 + j)));
-                    // fold in the 2^18 of the MMA's operand encoding (exact)
-                    dw_dst[j * kBNMax + r] = dw * 262144.0f;
-                }
-                mbar_arrive(&bars[kBarNibEmpty + ns]);
-                const unsigned any_slow = __any_sync(0xFFFFFFFFu, slow);
-                if (lane == 0) misc[kMiscSlow + cs * kNumConv + cw] = any_slow ? 1 : 0;
-                fence_proxy_async_smem();
-                mbar_arrive(&bars[kBarConvFull + cs]);
+        int t = blockIdx.x, st = 0;
+        Tile ti = decode_tile(t, E, s_off, s_tpre, a.bn);
+        StageRegs<XB> R0, R1;
+        load_stage<XB>(a, ti, st, ct, R0);
+        auto step = [&](StageRegs<XB> &cur, StageRegs<XB> &nxt) {
+            // where the next stage is
+            int t2 = t, st2 = st + 1;
+            Tile ti2 = ti;
+            if (st2 == nst) {
+                st2 = 0;
+                t2 += gridDim.x;
+                if (t2 < total) ti2 = decode_tile(t2, E, s_off, s_tpre, a.bn);
             }
+            if (t2 < total) load_stage<XB>(a, ti2, st2, ct, nxt);
+            ok = convert_stage<XB>(a, ti, st, ks, ct, lane, cw, cur, s_nib, s_a, s_b, s_dw, s_dx,
+                                   bars, misc, lim, abort_flag);
+            ++ks;
+            t = t2;
+            st = st2;
+            ti = ti2;
+        };
+        while (t < total && ok) {
+            step(R0, R1);
+            if (t >= total || !ok) break;
+            step(R1, R0);
         }
     } else {
         // -------------------------------------------------------- epilogue
         const int quad = warp & 3;                  // TMEM lanes 32*quad .. 32*quad+31
-        const int half = (warp - kWarpEpi0) >> 2;   // which share of the columns
+        const int part = (warp - kWarpEpi0) >> 2;   // which share of the columns
         const int row = quad * 32 + lane;           // weight row within the tile
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         uint32_t ks = 0, kb = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile ti = decode_tile(t, E, s_off, s_tpre, a.bn);
+            // the tile's 16-column chunks, split as evenly as possible
             const int n16 = ti.ncols >> 4;
-            const int first = (n16 + 1) >> 1;
-            const int c0 = half ? first * 16 : 0;
-            const int nch = half ? n16 - first : first;  // 16-column chunks, <= 4
-            float acc[64];
+            const int base = n16 / C::kEpiPerQuad, rem = n16 % C::kEpiPerQuad;
+            const int nch = base + (part < rem ? 1 : 0);  // <= kMaxChunks
+            const int c0 = 16 * (part * base + min(part, rem));
+            uint64_t acc[8 * C::kMaxChunks];              // column pairs (fp32 x 2)
 #pragma unroll
-            for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < 8 * C::kMaxChunks; ++i) acc[i] = 0ull;
             for (int st = 0; st < nst && ok; ++st, ++ks) {
                 const int cs = ks % kConvStages;
                 const int kb0 = st * kStageBlocks;
@@ -546,58 +670,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float *dxj = dxs + j * kBNMax + c0;
                     const uint32_t tcol = tmem + lane_addr + buf * C::kSCols + c0;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < C::kMaxChunks; ++c) {
                         if (c < nch) {
                             uint32_t v[16];
-                            float T[16];
                             tmem_ld_x16(tcol + c * 16, v);
-                            if constexpr (XB == 4) {
-                                tmem_ld_wait();
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) T[i] = __uint_as_float(v[i]);
-                            } else {
+                            if constexpr (XB == 8) {
                                 uint32_t u[16];
                                 tmem_ld_x16(tcol + 128 + c * 16, u);
                                 tmem_ld_wait();
                                 // S = 16 S_h + S_l, exact in fp32
 #pragma unroll
                                 for (int i = 0; i < 16; ++i)
-                                    T[i] = __fmaf_rn(16.0f, __uint_as_float(v[i]),
-                                                     __uint_as_float(u[i]));
-                            }
-                            if (!slow) {
-#pragma unroll
-                                for (int i = 0; i < 16; i += 4) {
-                                    const float4 d4 =
-                                        *reinterpret_cast<const float4 *>(dxj + c * 16 + i);
-                                    acc[c * 16 + i + 0] = __fmaf_rn(__fmul_rn(dw, d4.x), T[i + 0],
-                                                                    acc[c * 16 + i + 0]);
-                                    acc[c * 16 + i + 1] = __fmaf_rn(__fmul_rn(dw, d4.y), T[i + 1],
-                                                                    acc[c * 16 + i + 1]);
-                                    acc[c * 16 + i + 2] = __fmaf_rn(__fmul_rn(dw, d4.z), T[i + 2],
-                                                                    acc[c * 16 + i + 2]);
-                                    acc[c * 16 + i + 3] = __fmaf_rn(__fmul_rn(dw, d4.w), T[i + 3],
-                                                                    acc[c * 16 + i + 3]);
-                                }
+                                    v[i] = __float_as_uint(__fmaf_rn(16.0f, __uint_as_float(v[i]),
+                                                                     __uint_as_float(u[i])));
                             } else {
-                                // a scale product outside the normal range: round
-                                // d_w * d_x itself, then apply the 2^18 exactly
-                                const float dw0 = dw * 0x1p-18f;
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    const float s = __fmul_rn(__fmul_rn(dw0, dxj[c * 16 + i]),
-                                                              262144.0f);
-                                    acc[c * 16 + i] = __fmaf_rn(s, T[i], acc[c * 16 + i]);
-                                }
+                                tmem_ld_wait();
                             }
-                            if (a.bsum) {
+                            if (!slow) fold16(acc + 8 * c, dw, dxj + 16 * c, v);
+                            else fold16_exact(acc + 8 * c, dw, dxj + 16 * c, v);
+                            if constexpr (kSums) {
                                 const int64_t n = ti.n0 + row;
 #pragma unroll
                                 for (int i = 0; i < 16; ++i) {
                                     const int col = c0 + c * 16 + i;
                                     if (col < ti.rows && n < a.N)
                                         a.bsum[((ti.g0 + col) * static_cast<int64_t>(a.N) + n) * nb +
-                                               kb0 + j] = __float2int_rn(T[i] * 262144.0f);
+                                               kb0 + j] =
+                                            __float2int_rn(__uint_as_float(v[i]) * 262144.0f);
                                 }
                             }
                         }
@@ -613,12 +712,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t n = ti.n0 + row;
             if (n < a.N) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < C::kMaxChunks; ++c) {
                     if (c < nch) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int col = c0 + c * 16 + i;
-                            if (col < ti.rows) a.y[(ti.g0 + col) * a.ldy + n] = acc[c * 16 + i];
+                        for (int i = 0; i < 8; ++i) {
+                            const int col = c0 + c * 16 + 2 * i;
+                            const uint64_t pr = acc[8 * c + i];
+                            if (col < ti.rows)
+                                a.y[(ti.g0 + col) * a.ldy + n] =
+                                    __uint_as_float(static_cast<uint32_t>(pr));
+                            if (col + 1 < ti.rows)
+                                a.y[(ti.g0 + col + 1) * a.ldy + n] =
+                                    __uint_as_float(static_cast<uint32_t>(pr >> 32));
                         }
                     }
                 }
@@ -656,15 +761,22 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 128 rows x 64 bytes boxes over the weight nibbles viewed as [rows][K/2] bytes
 h32_status make_weight_map(CUtensorMap *map, const uint8_t *wq, int64_t rows, int64_t K) {
     auto enc = tensor_map_encoder();
-    if (!enc) return H32_ERR_CUDA;
+    if (!enc) {
+        note_error("cuTensorMapEncodeTiled is not available from the driver");
+        return H32_ERR_CUDA;
+    }
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
     const cuuint32_t box[2] = {64, kBM};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(wq), dims, strides,
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(wq), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? H32_OK : H32_ERR_CUDA;
+    if (r != CUDA_SUCCESS) {
+        note_error("cuTensorMapEncodeTiled rejected the weight tensor map");
+        return H32_ERR_CUDA;
+    }
+    return H32_OK;
 }
 
 // Tokens per tile for a dense product: simulate the static round-robin
@@ -697,14 +809,22 @@ int choose_bn(int64_t M, int64_t N, int sms) {
     return best;
 }
 
+template <int XB, bool kSums>
+h32_status launch_variant(const CUtensorMap &map, const GemmArgs &a, int grid, cudaStream_t s) {
+    using C = Cfg<XB>;
+    const cudaError_t e = cudaFuncSetAttribute(
+        gemm_kernel<XB, kSums>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return launch_status(e);
+    gemm_kernel<XB, kSums><<<grid, C::kThreads, C::kSmem, s>>>(map, a);
+    return launch_status(cudaGetLastError());
+}
+
+// the block-sum debug output is a separate compiled variant, so the product
+// path carries no per-element check for it
 template <int XB>
 h32_status launch(const CUtensorMap &map, const GemmArgs &a, int grid, cudaStream_t s) {
-    using C = Cfg<XB>;
-    if (cudaFuncSetAttribute(gemm_kernel<XB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmem) != cudaSuccess)
-        return H32_ERR_CUDA;
-    gemm_kernel<XB><<<grid, kThreads, C::kSmem, s>>>(map, a);
-    return launch_status(cudaGetLastError());
+    return a.bsum ? launch_variant<XB, true>(map, a, grid, s)
+                  : launch_variant<XB, false>(map, a, grid, s);
 }
 
 template <int XB>

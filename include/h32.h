@@ -163,6 +163,10 @@ const char *h32_status_string(h32_status status);
  */
 void h32_set_wait_limit(uint64_t polls);
 
+/* Text of the most recent CUDA failure seen by the library on the calling
+ * thread (after an H32_ERR_CUDA status); static storage, never NULL. */
+const char *h32_last_cuda_error(void);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int h32_version(void);
 

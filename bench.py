@@ -397,11 +397,9 @@ def time_e2e(torch, h32, chain, stream, args, dist, device, world):
 # --------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline / reference arm)
 # --------------------------------------------------------------------------
-def cpu_baseline(sample_tokens: int):
-    """Time the CPU oracle, as it stands, on a bounded sample of the same
-    workload: `sample_tokens` of the 512 tokens through the whole chain
-    (quantize + GEMM for all three projections).  The oracle's offline weight
-    quantization is done first and not timed."""
+def oracle_prepare(sample_tokens: int):
+    """The oracle's offline step (weights rotated + quantized) and the sampled
+    activations; not timed."""
     import oracle
     oracle.build()
     prepared = []
@@ -410,11 +408,24 @@ def cpu_baseline(sample_tokens: int):
         wq, wd = oracle.quantize_weights_q4_0(p.weights(0, cid))
         x = p.activations(M_TOKENS, 0, cid)[:sample_tokens]
         prepared.append((wq, wd, x, p.K))
+    return prepared
+
+
+def oracle_step(prepared) -> float:
+    """One timed pass of the oracle over the sample: quantize + full GEMM per projection."""
+    import oracle
     t = time.perf_counter()
     for wq, wd, x, K in prepared:
         xq, xd = oracle.quantize_act_q4(x)
         oracle.gemm(wq, wd, xq, xd, K)
-    dt = time.perf_counter() - t
+    return time.perf_counter() - t
+
+
+def cpu_baseline(sample_tokens: int):
+    """Time the CPU oracle, as it stands, on a bounded sample of the same
+    workload: `sample_tokens` of the 512 tokens through the whole chain
+    (quantize + GEMM for all three projections), single threaded."""
+    dt = oracle_step(oracle_prepare(sample_tokens))
     return {"value": round(sample_tokens / dt, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "seconds": round(dt, 2),
             "sample": f"{sample_tokens} of the 512 tokens through the whole chain "
@@ -422,27 +433,61 @@ def cpu_baseline(sample_tokens: int):
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle on the host cores, each step a bounded
+    sample (`--ref-tokens` tokens) of the pp512 chain."""
     rank, world, local = dist_env()
     if rank != 0:
         return None
-    per_step = []
+    prepared = oracle_prepare(args.ref_tokens)
     for _ in range(args.warmup):
-        cpu_baseline(args.ref_tokens)
-    for _ in range(args.steps):
-        per_step.append(cpu_baseline(args.ref_tokens))
-    secs = sum(r["seconds"] for r in per_step)
-    value = args.ref_tokens * len(per_step) / secs
+        oracle_step(prepared)
+    secs = sum(oracle_step(prepared) for _ in range(args.steps))
+    value = args.ref_tokens * args.steps / secs
+    sample = (f"{args.ref_tokens} of the 512 tokens per step through the whole chain "
+              f"(3 quantizations + 3 full GEMMs), single-threaded C oracle")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 * secs / len(per_step), 2), "higher_is_better": True,
+            "ms_per_step": round(1e3 * secs / args.steps, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int64 block sums, fp32 epilogue",
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "tokens_per_step": args.ref_tokens,
                        "note": "each step is a bounded sample of the pp512 chain"},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": per_step[0]["sample"]},
+                             "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+def run_only_gemm(args):
+    """A small case for profilers: one projection's GEMM alone (resident
+    inputs, `warmup + steps` launches), timed with CUDA events."""
+    import torch
+    import hadamard_rotated_bit_gb300 as h32
+    from hadamard_rotated_bit_gb300 import _build
+    _build.build()
+    p = {q.name: q for q in CHAIN}[args.only_gemm]
+    cid = wl.CFG_ATTN if p is wl.ATTN else wl.CFG_FFN
+    dev = torch.device("cuda", 0)
+    wq, wd = h32.h32_rotate_quantize_weights_q4_0(torch.from_numpy(p.weights(0, cid)).to(dev))
+    x = torch.from_numpy(p.activations(M_TOKENS, 0, cid).view(np.int16)).view(torch.bfloat16).to(dev)
+    xq, xd = h32.h32_quantize_act_q4(x)
+    y = torch.empty((M_TOKENS, p.N), dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        h32.q4_0_x_q4_gemm(wq, wd, xq, xd, y=y)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record()
+    for _ in range(args.steps):
+        h32.q4_0_x_q4_gemm(wq, wd, xq, xd, y=y)
+    t1.record()
+    torch.cuda.synchronize()
+    if h32.h32_device_status() != 0:
+        raise RuntimeError("device status not OK")
+    ms = t0.elapsed_time(t1) / args.steps
+    alg = algorithmic(p)
+    return {"only_gemm": p.name, "ms_per_launch": round(ms, 5),
+            "eff_TOPS": round(alg["gemm_int_ops"] / (ms / 1e3) / 1e12, 1),
+            "steps": args.steps, "warmup": args.warmup}
 
 
 def main(argv=None):
@@ -451,13 +496,17 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["h32", "reference"], default="h32")
-    ap.add_argument("--cpu-tokens", type=int, default=2)
+    ap.add_argument("--cpu-tokens", type=int, default=24)
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-gemm", choices=[p.name for p in CHAIN], default=None,
+                    help="time one projection's GEMM alone (a small case for profilers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.only_gemm:
+        line = run_only_gemm(args)
+    elif args.impl == "reference":
         line = run_reference(args)
     else:
         line = run_gpu(args)

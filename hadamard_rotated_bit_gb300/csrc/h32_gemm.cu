@@ -56,6 +56,17 @@ constexpr int kMaxExperts = 1024;
 constexpr int kTmemCols = 512;
 constexpr uint64_t kDrainPolls = 1ull << 22;
 
+// tuning constants (measured on GB300; see the design notes)
+#ifndef H32_Q4_GROUP
+#define H32_Q4_GROUP 1
+#endif
+#ifndef H32_Q4_EPI_PER_QUAD
+#define H32_Q4_EPI_PER_QUAD 2
+#endif
+#ifndef H32_PIPE_TMEM_LOADS
+#define H32_PIPE_TMEM_LOADS 0
+#endif
+
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpConv0 = 2, kNumConv = 4, kWarpEpi0 = 6;
 constexpr int kConvThreads = kNumConv * 32;  // 128
 
@@ -76,11 +87,15 @@ __device__ __forceinline__ uint32_t op_offset(int r, int chunk) {
 template <int XB>
 struct Cfg {
     static constexpr int kBOps = (XB == 4) ? 1 : 2;      // B operands per stage (q8: hi, lo)
-    static constexpr int kSBufs = (XB == 4) ? 4 : 2;     // blocks in flight in TMEM
     static constexpr int kSCols = (XB == 4) ? 128 : 256; // TMEM columns per block
+    // blocks handed from the MMA to the epilogue per synchronization, and the
+    // number of such groups in flight in TMEM (512 columns in all)
+    static constexpr int kGroup = (XB == 4) ? H32_Q4_GROUP : 1;
+    static constexpr int kGroupBufs = kTmemCols / (kGroup * kSCols);
+    static constexpr bool kPipeLoads = H32_PIPE_TMEM_LOADS;
     // epilogue warps per TMEM lane quadrant (each takes an even share of the
     // tile's 16-column chunks)
-    static constexpr int kEpiPerQuad = 2;
+    static constexpr int kEpiPerQuad = (XB == 4) ? H32_Q4_EPI_PER_QUAD : 2;
     static constexpr int kEpiWarps = 4 * kEpiPerQuad;
     static constexpr int kEpiThreads = kEpiWarps * 32;
     static constexpr int kMaxChunks = (8 + kEpiPerQuad - 1) / kEpiPerQuad;  // 16-column chunks
@@ -247,6 +262,19 @@ __device__ __forceinline__ void fold16_exact(uint64_t *acc, float dw, const floa
     }
 }
 
+// the exact block sums of 16 columns (debug output)
+__device__ __forceinline__ void store_sums(const GemmArgs &a, const Tile &ti, int row, int col0,
+                                           int b, const uint32_t (&v)[16]) {
+    const int64_t n = ti.n0 + row;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int col = col0 + i;
+        if (col < ti.rows && n < a.N)
+            a.bsum[((ti.g0 + col) * static_cast<int64_t>(a.N) + n) * a.nb + b] =
+                __float2int_rn(__uint_as_float(v[i]) * 262144.0f);
+    }
+}
+
 // activation items and weight-scale items of one stage, held in registers
 // between their global loads and their use
 template <int XB>
@@ -255,6 +283,29 @@ struct StageRegs {
     float dx[4];
     uint32_t wd[4];
 };
+
+// Predicated global loads into registers the caller zeroed: a load that is
+// switched off leaves the zero, and no instruction consumes the loaded value
+// until it is used, so the loads of the next stage stay in flight.
+__device__ __forceinline__ void ldg_pred(uint4 &v, const void *p, bool on) {
+    asm volatile(
+        "{\n.reg .pred q;\nsetp.ne.b32 q, %5, 0;\n"
+        "@q ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n}\n"
+        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+        : "l"(p), "r"(static_cast<int>(on)));
+}
+__device__ __forceinline__ void ldg_pred(float &v, const float *p, bool on) {
+    asm volatile(
+        "{\n.reg .pred q;\nsetp.ne.b32 q, %2, 0;\n@q ld.global.nc.f32 %0, [%1];\n}\n"
+        : "+f"(v)
+        : "l"(p), "r"(static_cast<int>(on)));
+}
+__device__ __forceinline__ void ldg_pred_u16(uint32_t &v, const uint16_t *p, bool on) {
+    asm volatile(
+        "{\n.reg .pred q;\nsetp.ne.b32 q, %2, 0;\n@q ld.global.nc.u16 %0, [%1];\n}\n"
+        : "+r"(v)
+        : "l"(p), "r"(static_cast<int>(on)));
+}
 
 template <int XB>
 __device__ __forceinline__ void load_stage(const GemmArgs &a, const Tile &ti, int st, int ct,
@@ -280,13 +331,10 @@ __device__ __forceinline__ void load_stage(const GemmArgs &a, const Tile &ti, in
 #pragma unroll
         for (int h = 0; h < (XB == 4 ? 1 : 2); ++h) R.q[k][h] = make_uint4(0, 0, 0, 0);
         R.dx[k] = 0.0f;
-        if (valid) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + tok * xrow_bytes +
-                                                               (kb0 + j) * (XB == 4 ? 16 : 32));
+        const uint8_t *src = a.xq + tok * xrow_bytes + (kb0 + j) * (XB == 4 ? 16 : 32);
 #pragma unroll
-            for (int h = 0; h < (XB == 4 ? 1 : 2); ++h) R.q[k][h] = __ldg(src + h);
-            R.dx[k] = __ldg(a.xd + tok * nb + kb0 + j);
-        }
+        for (int h = 0; h < (XB == 4 ? 1 : 2); ++h) ldg_pred(R.q[k][h], src + 16 * h, valid);
+        ldg_pred(R.dx[k], a.xd + tok * nb + kb0 + j, valid);
     }
     const int wrow0 = ti.e * a.N + ti.n0;
     const int nvalid_w = min(kBM, a.N - ti.n0);
@@ -294,10 +342,9 @@ __device__ __forceinline__ void load_stage(const GemmArgs &a, const Tile &ti, in
     for (int k = 0; k < 4; ++k) {
         const int i = ct + k * kConvThreads;
         const int r = i >> 2, j = i & 3;
-        R.wd[k] = (r < nvalid_w && j < nblk)
-                      ? static_cast<uint32_t>(__ldg(a.wd + static_cast<int64_t>(wrow0 + r) * nb +
-                                                    kb0 + j))
-                      : 0u;
+        R.wd[k] = 0u;
+        ldg_pred_u16(R.wd[k], a.wd + static_cast<int64_t>(wrow0 + r) * nb + kb0 + j,
+                     r < nvalid_w && j < nblk);
     }
 }
 
@@ -387,11 +434,16 @@ __device__ __forceinline__ bool convert_stage(const GemmArgs &a, const Tile &ti,
         // fold in the 2^18 of the MMA's operand encoding (exact)
         dw_dst[j * kBNMax + r] = dw * 262144.0f;
     }
-    mbar_arrive(&bars[kBarNibEmpty + ns]);
+    // one arrival per warp: every lane's shared-memory reads and writes of
+    // this stage are ordered before it by __syncwarp
     const unsigned any_slow = __any_sync(0xFFFFFFFFu, slow);
-    if (lane == 0) misc[kMiscSlow + cs * kNumConv + cw] = any_slow ? 1 : 0;
-    fence_proxy_async_smem();
-    mbar_arrive(&bars[kBarConvFull + cs]);
+    fence_proxy_async_smem();  // this thread's operand writes -> tensor-core reads
+    __syncwarp();
+    if (lane == 0) {
+        misc[kMiscSlow + cs * kNumConv + cw] = any_slow ? 1 : 0;
+        mbar_arrive(&bars[kBarNibEmpty + ns]);
+        mbar_arrive(&bars[kBarConvFull + cs]);
+    }
     return true;
 }
 
@@ -425,15 +477,15 @@ __global__ void __launch_bounds__(Cfg<XB>::kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < kNibStages; ++i) {
             mbar_init(&bars[kBarNibFull + i], 1);
-            mbar_init(&bars[kBarNibEmpty + i], kConvThreads);
+            mbar_init(&bars[kBarNibEmpty + i], kNumConv);
         }
         for (int i = 0; i < kConvStages; ++i) {
-            mbar_init(&bars[kBarConvFull + i], kConvThreads);
-            mbar_init(&bars[kBarConvEmpty + i], 1 + C::kEpiThreads);
+            mbar_init(&bars[kBarConvFull + i], kNumConv);
+            mbar_init(&bars[kBarConvEmpty + i], 1 + C::kEpiWarps);
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&bars[kBarSFull + i], 1);
-            mbar_init(&bars[kBarSEmpty + i], C::kEpiThreads);
+            mbar_init(&bars[kBarSEmpty + i], C::kEpiWarps);
         }
         mbar_init(&bars[kBarDrain], 1);
         misc[kMiscAbort] = 0;
@@ -538,7 +590,7 @@ __global__ void __launch_bounds__(Cfg<XB>::kThreads, 1)
         }
     } else if (warp == kWarpMma) {
         if (lane == 0) {
-            uint32_t ks = 0, kb = 0;
+            uint32_t ks = 0, kg = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const Tile ti = decode_tile(t, E, s_off, s_tpre, a.bn);
@@ -553,33 +605,34 @@ __global__ void __launch_bounds__(Cfg<XB>::kThreads, 1)
                     }
                     tc_fence_after();
                     const int nblk = min(kStageBlocks, nb - st * kStageBlocks);
-                    const uint32_t a_base = smem_u32(s_a + cs * kOpBytes);
-                    const uint32_t b_base = smem_u32(s_b + cs * C::kBOps * kOpBytes);
-                    for (int j = 0; j < nblk; ++j, ++kb) {
-                        const int buf = kb % C::kSBufs;
-                        if (!mbar_wait_bounded(&bars[kBarSEmpty + buf], ((kb / C::kSBufs) & 1) ^ 1,
-                                               lim, abort_flag)) {
+                    const uint64_t a_desc0 =
+                        smem_desc_noswizzle(smem_u32(s_a + cs * kOpBytes), kLBO, kSBO);
+                    const uint64_t b_desc0 =
+                        smem_desc_noswizzle(smem_u32(s_b + cs * C::kBOps * kOpBytes), kLBO, kSBO);
+                    for (int j0 = 0; j0 < nblk; j0 += C::kGroup, ++kg) {
+                        const int gb = kg % C::kGroupBufs;
+                        if (!mbar_wait_bounded(&bars[kBarSEmpty + gb], ((kg / C::kGroupBufs) & 1) ^ 1, lim,
+                                               abort_flag)) {
                             set_abort(misc);
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t ad = smem_desc_noswizzle(a_base + j * 2 * kLBO, kLBO, kSBO);
-                        const uint32_t d = tmem + buf * C::kSCols;
-                        if constexpr (XB == 4) {
-                            mma_f8f6f4(d, ad,
-                                       smem_desc_noswizzle(b_base + j * 2 * kLBO, kLBO, kSBO),
-                                       idesc, 0);
-                        } else {
-                            mma_f8f6f4(d, ad,
-                                       smem_desc_noswizzle(b_base + j * 2 * kLBO, kLBO, kSBO),
-                                       idesc, 0);
-                            mma_f8f6f4(d + 128, ad,
-                                       smem_desc_noswizzle(b_base + kOpBytes + j * 2 * kLBO, kLBO,
-                                                           kSBO),
-                                       idesc, 0);
+#pragma unroll
+                        for (int i = 0; i < C::kGroup; ++i) {
+                            const int j = j0 + i;
+                            if (j < nblk) {
+                                // block j's operands start 2 * j K-chunks into the tile
+                                // (descriptor addresses are in 16-byte units)
+                                const uint64_t koff = (2 * j * kLBO) >> 4;
+                                const uint32_t d = tmem + (gb * C::kGroup + i) * C::kSCols;
+                                mma_f8f6f4(d, a_desc0 + koff, b_desc0 + koff, idesc, 0);
+                                if constexpr (XB == 8)
+                                    mma_f8f6f4(d + 128, a_desc0 + koff,
+                                               b_desc0 + koff + (kOpBytes >> 4), idesc, 0);
+                            }
                         }
-                        mma_commit(&bars[kBarSFull + buf]);
+                        mma_commit(&bars[kBarSFull + gb]);
                     }
                     if (!ok) break;
                     mma_commit(&bars[kBarConvEmpty + cs]);
@@ -631,7 +684,7 @@ __global__ void __launch_bounds__(Cfg<XB>::kThreads, 1)
         const int part = (warp - kWarpEpi0) >> 2;   // which share of the columns
         const int row = quad * 32 + lane;           // weight row within the tile
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-        uint32_t ks = 0, kb = 0;
+        uint32_t ks = 0, kg = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile ti = decode_tile(t, E, s_off, s_tpre, a.bn);
@@ -658,54 +711,81 @@ __global__ void __launch_bounds__(Cfg<XB>::kThreads, 1)
                                   misc[kMiscSlow + cs * kNumConv + 3];
                 const float *dxs = s_dx + cs * (kStageBlocks * kBNMax);
                 const float *dws = s_dw + cs * (kStageBlocks * kBNMax);
-                for (int j = 0; j < nblk; ++j, ++kb) {
-                    const int buf = kb % C::kSBufs;
-                    if (!warp_wait(&bars[kBarSFull + buf], (kb / C::kSBufs) & 1, lim, abort_flag)) {
+                for (int j0 = 0; j0 < nblk; j0 += C::kGroup, ++kg) {
+                    const int gb = kg % C::kGroupBufs;
+                    if (!warp_wait(&bars[kBarSFull + gb], (kg / C::kGroupBufs) & 1, lim, abort_flag)) {
                         set_abort(misc);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const float dw = dws[j * kBNMax + row];
-                    const float *dxj = dxs + j * kBNMax + c0;
-                    const uint32_t tcol = tmem + lane_addr + buf * C::kSCols + c0;
 #pragma unroll
-                    for (int c = 0; c < C::kMaxChunks; ++c) {
-                        if (c < nch) {
-                            uint32_t v[16];
-                            tmem_ld_x16(tcol + c * 16, v);
-                            if constexpr (XB == 8) {
-                                uint32_t u[16];
-                                tmem_ld_x16(tcol + 128 + c * 16, u);
-                                tmem_ld_wait();
-                                // S = 16 S_h + S_l, exact in fp32
+                    for (int i = 0; i < C::kGroup; ++i) {
+                        const int j = j0 + i;
+                        if (j >= nblk) break;
+                        const float dw = dws[j * kBNMax + row];
+                        const float *dxj = dxs + j * kBNMax + c0;
+                        const uint32_t tcol =
+                            tmem + lane_addr + (gb * C::kGroup + i) * C::kSCols + c0;
+                        if constexpr (XB == 4 && C::kPipeLoads) {
+                            // software pipeline: the load of chunk c + 1 is in flight
+                            // while chunk c is folded
+                            uint32_t v0[16], v1[16];
+                            if (nch > 0) tmem_ld_x16(tcol, v0);
 #pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    v[i] = __float_as_uint(__fmaf_rn(16.0f, __uint_as_float(v[i]),
-                                                                     __uint_as_float(u[i])));
-                            } else {
-                                tmem_ld_wait();
+                            for (int c = 0; c < C::kMaxChunks; ++c) {
+                                if (c < nch) {
+                                    tmem_ld_wait();
+                                    uint32_t(&cur)[16] = (c & 1) ? v1 : v0;
+                                    uint32_t(&nxt)[16] = (c & 1) ? v0 : v1;
+                                    if (c + 1 < nch) tmem_ld_x16(tcol + (c + 1) * 16, nxt);
+                                    if (!slow) fold16(acc + 8 * c, dw, dxj + 16 * c, cur);
+                                    else fold16_exact(acc + 8 * c, dw, dxj + 16 * c, cur);
+                                    if constexpr (kSums)
+                                        store_sums(a, ti, row, c0 + c * 16, st * kStageBlocks + j, cur);
+                                }
                             }
-                            if (!slow) fold16(acc + 8 * c, dw, dxj + 16 * c, v);
-                            else fold16_exact(acc + 8 * c, dw, dxj + 16 * c, v);
-                            if constexpr (kSums) {
-                                const int64_t n = ti.n0 + row;
+                        } else if constexpr (XB == 4) {
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    const int col = c0 + c * 16 + i;
-                                    if (col < ti.rows && n < a.N)
-                                        a.bsum[((ti.g0 + col) * static_cast<int64_t>(a.N) + n) * nb +
-                                               kb0 + j] =
-                                            __float2int_rn(__uint_as_float(v[i]) * 262144.0f);
+                            for (int c = 0; c < C::kMaxChunks; ++c) {
+                                if (c < nch) {
+                                    uint32_t v[16];
+                                    tmem_ld_x16(tcol + c * 16, v);
+                                    tmem_ld_wait();
+                                    if (!slow) fold16(acc + 8 * c, dw, dxj + 16 * c, v);
+                                    else fold16_exact(acc + 8 * c, dw, dxj + 16 * c, v);
+                                    if constexpr (kSums)
+                                        store_sums(a, ti, row, c0 + c * 16, st * kStageBlocks + j, v);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < C::kMaxChunks; ++c) {
+                                if (c < nch) {
+                                    uint32_t v[16], u[16];
+                                    tmem_ld_x16(tcol + c * 16, v);
+                                    tmem_ld_x16(tcol + 128 + c * 16, u);
+                                    tmem_ld_wait();
+                                    // S = 16 S_h + S_l, exact in fp32
+#pragma unroll
+                                    for (int q = 0; q < 16; ++q)
+                                        v[q] = __float_as_uint(__fmaf_rn(
+                                            16.0f, __uint_as_float(v[q]), __uint_as_float(u[q])));
+                                    if (!slow) fold16(acc + 8 * c, dw, dxj + 16 * c, v);
+                                    else fold16_exact(acc + 8 * c, dw, dxj + 16 * c, v);
+                                    if constexpr (kSums)
+                                        store_sums(a, ti, row, c0 + c * 16, st * kStageBlocks + j, v);
                                 }
                             }
                         }
                     }
                     tc_fence_before();
-                    mbar_arrive(&bars[kBarSEmpty + buf]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[kBarSEmpty + gb]);
                 }
                 if (!ok) break;
-                mbar_arrive(&bars[kBarConvEmpty + cs]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kBarConvEmpty + cs]);
             }
             if (!ok) break;
             // store: lanes hold 32 consecutive weight rows of one token column

@@ -490,6 +490,160 @@ def run_only_gemm(args):
             "steps": args.steps, "warmup": args.warmup}
 
 
+# --------------------------------------------------------------------------
+# --suite: the other configurations of the path (one JSON line each)
+# --------------------------------------------------------------------------
+def _events_time(torch, fn, steps, warmup, stream):
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / steps  # ms per call
+
+
+def suite_chain_routes(torch, h32, dev, stream, steps, warmup):
+    """The pp512 chain on the exact 8-bit route and on the unrotated 4-bit route."""
+    out = []
+    for route in ("q8_rotated", "q4_unrotated"):
+        rot = route != "q4_unrotated"
+        bufs = []
+        for p in CHAIN:
+            cid = wl.CFG_ATTN if p is wl.ATTN else wl.CFG_FFN
+            wq, wd = h32.h32_rotate_quantize_weights_q4_0(
+                torch.from_numpy(p.weights(0, cid)).to(dev), rotate=rot)
+            x = torch.from_numpy(p.activations(M_TOKENS, 0, cid).view(np.int16)).view(
+                torch.bfloat16).to(dev)
+            bufs.append((wq, wd, x, torch.empty((M_TOKENS, p.N), device=dev)))
+
+        def step():
+            for wq, wd, x, y in bufs:
+                if route.startswith("q8"):
+                    xq, xd = h32.h32_quantize_act_q8(x, rotate=rot, stream=stream)
+                    h32.q4_0_x_q8_gemm(wq, wd, xq, xd, y=y, stream=stream)
+                else:
+                    xq, xd = h32.h32_quantize_act_q4(x, rotate=rot, stream=stream)
+                    h32.q4_0_x_q4_gemm(wq, wd, xq, xd, y=y, stream=stream)
+        ms = _events_time(torch, step, steps, warmup, stream)
+        out.append({"suite": f"pp512_chain_{route}", "value": round(M_TOKENS / (ms / 1e3), 1),
+                    "unit": UNIT, "ms_per_step": round(ms, 4)})
+        del bufs
+    return out
+
+
+def suite_moe(torch, h32, dev, stream, steps, warmup):
+    """One 1024-token MoE micro-batch: quantize, expert gate/up GEMM, quantize the
+    down input, expert down GEMM (routing, SwiGLU and combine are outside the path)."""
+    cfg = wl.MOE
+    row_idx, off, _ = wl.moe_routing(cfg)
+    x_gu, x_dn = wl.moe_inputs(cfg)
+    w_gu, w_dn = wl.moe_weights(cfg)
+    R = int(off[-1])
+
+    def prep(w):
+        E, N, K = w.shape
+        wq, wd = h32.h32_rotate_quantize_weights_q4_0(torch.from_numpy(w.reshape(E * N, K)).to(dev))
+        return wq.view(E, N, K // 2), wd.view(E, N, K // 32)
+    wq_gu, wd_gu = prep(w_gu)
+    wq_dn, wd_dn = prep(w_dn)
+    xg = torch.from_numpy(x_gu.view(np.int16)).view(torch.bfloat16).to(dev)
+    xn = torch.from_numpy(x_dn.view(np.int16)).view(torch.bfloat16).to(dev)
+    ridx = torch.from_numpy(row_idx).to(dev)
+    offs = torch.from_numpy(off).to(dev)
+    y_gu = torch.empty((R, wq_gu.shape[1]), device=dev)
+    y_dn = torch.empty((R, wq_dn.shape[1]), device=dev)
+    times = {}
+
+    def step():
+        xq, xd = h32.h32_quantize_act_q4(xg, stream=stream)
+        h32.q4_0_x_q4_gemm_experts(wq_gu, wd_gu, xq, xd, ridx, offs, R, y=y_gu, stream=stream)
+        xq2, xd2 = h32.h32_quantize_act_q4(xn, stream=stream)
+        h32.q4_0_x_q4_gemm_experts(wq_dn, wd_dn, xq2, xd2, None, offs, R, y=y_dn, stream=stream)
+    ms = _events_time(torch, step, steps, warmup, stream)
+    xq, xd = h32.h32_quantize_act_q4(xg, stream=stream)
+    times["gate_up_ms"] = _events_time(torch, lambda: h32.q4_0_x_q4_gemm_experts(
+        wq_gu, wd_gu, xq, xd, ridx, offs, R, y=y_gu, stream=stream), steps, warmup, stream)
+    xq2, xd2 = h32.h32_quantize_act_q4(xn, stream=stream)
+    times["down_ms"] = _events_time(torch, lambda: h32.q4_0_x_q4_gemm_experts(
+        wq_dn, wd_dn, xq2, xd2, None, offs, R, y=y_dn, stream=stream), steps, warmup, stream)
+    ops = 2 * R * (wq_gu.shape[1] * cfg.hidden + wq_dn.shape[1] * cfg.ffn)
+    return [{"suite": "moe_1024_tokens_top8_128_experts", "value": round(cfg.T / (ms / 1e3), 1),
+             "unit": UNIT, "ms_per_step": round(ms, 4),
+             "gemm_ms": {k: round(v, 4) for k, v in times.items()},
+             "gemm_eff_TOPS": round(ops / ((times["gate_up_ms"] + times["down_ms"]) / 1e3) / 1e12, 1)}]
+
+
+def suite_long(torch, h32, dev, stream, steps, warmup):
+    """The chain on long prompts, in 1024-token micro-batches."""
+    out = []
+    projs = [wl.LONG_ATTN, wl.LONG_GATE_UP, wl.LONG_DOWN]
+    weights = []
+    for p in projs:
+        wq, wd = h32.h32_rotate_quantize_weights_q4_0(
+            torch.from_numpy(p.weights(0, wl.CFG_LONG)).to(dev))
+        weights.append((wq, wd))
+    mb = 1024
+    for M in wl.LONG_MS:
+        xs = [torch.from_numpy(p.activations(M, 0, wl.CFG_LONG).view(np.int16)).view(
+            torch.bfloat16).to(dev) for p in projs]
+        ys = [torch.empty((mb, p.N), device=dev) for p in projs]
+
+        def step():
+            for s0 in range(0, M, mb):
+                for (wq, wd), x, y in zip(weights, xs, ys):
+                    xq, xd = h32.h32_quantize_act_q4(x[s0:s0 + mb], stream=stream)
+                    h32.q4_0_x_q4_gemm(wq, wd, xq, xd, y=y[:min(mb, M - s0)], stream=stream)
+        ms = _events_time(torch, step, max(1, steps // max(1, M // 1024)), max(1, warmup // 4),
+                          stream)
+        out.append({"suite": f"long_prompt_{M}_tokens_1024_microbatches",
+                    "value": round(M / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 3)})
+        del xs, ys
+    return out
+
+
+def suite_quant_stream(torch, h32, dev, stream, steps, warmup, peaks):
+    """The rotate+quantize kernel streaming a large activation matrix (16384 x 17408 bf16)."""
+    M, K = 16384, 17408
+    g = torch.Generator(device=dev).manual_seed(0)
+    x = torch.randn((M, K), device=dev, generator=g).to(torch.bfloat16)
+    out = []
+    for bits in (4, 8):
+        xq = torch.empty((M, K // 2 if bits == 4 else K), dtype=torch.uint8, device=dev)
+        xd = torch.empty((M, K // 32), dtype=torch.float32, device=dev)
+        fn = h32.h32_quantize_act_q4 if bits == 4 else h32.h32_quantize_act_q8
+        ms = _events_time(torch, lambda: fn(x, xq=xq, xd=xd, stream=stream), steps, warmup, stream)
+        nbytes = M * K * 2 + xq.numel() + xd.numel() * 4
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out.append({"suite": f"quantize_q{bits}_stream_16384x17408_bf16", "value": round(gbs, 1),
+                    "unit": "GB/s", "ms_per_call": round(ms, 4),
+                    "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_call": nbytes})
+    return out
+
+
+def run_suite(args):
+    import torch
+    import hadamard_rotated_bit_gb300 as h32
+    from hadamard_rotated_bit_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    peaks, _ = load_peaks()
+    steps, warmup = args.steps, args.warmup
+    lines = []
+    lines += suite_quant_stream(torch, h32, dev, stream, steps, warmup, peaks)
+    lines += suite_chain_routes(torch, h32, dev, stream, steps, warmup)
+    lines += suite_moe(torch, h32, dev, stream, steps, warmup)
+    lines += suite_long(torch, h32, dev, stream, steps, warmup)
+    if h32.h32_device_status(stream) != 0:
+        raise RuntimeError("device status not OK after the suite")
+    return lines
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -499,11 +653,18 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=24)
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suite", action="store_true",
+                    help="measure the other configurations (8-bit and unrotated routes, MoE, "
+                         "long prompts, streaming quantizer), one JSON line each")
     ap.add_argument("--only-gemm", choices=[p.name for p in CHAIN], default=None,
                     help="time one projection's GEMM alone (a small case for profilers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.suite:
+        for ln in run_suite(args):
+            print(json.dumps(ln), flush=True)
+        return
     if args.only_gemm:
         line = run_only_gemm(args)
     elif args.impl == "reference":

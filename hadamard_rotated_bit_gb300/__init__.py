@@ -21,7 +21,8 @@ __all__ = [
     "h32_quantize_act_q4", "h32_quantize_act_q8", "h32_rotate_quantize_weights_q4_0",
     "q4_0_x_q4_gemm", "q4_0_x_q8_gemm", "q4_0_x_q4_gemm_experts",
     "h32_device_status", "h32_status_string", "h32_set_wait_limit", "h32_version",
-    "h32_last_cuda_error",
+    "h32_last_cuda_error", "h32_quantize_act_q4_tc", "h32_prepack_weights_q4_0_tc",
+    "q4_0_x_q4_gemm_tc",
 ]
 
 
@@ -51,6 +52,9 @@ _SIGS = {
     "h32_set_wait_limit": (None, [ctypes.c_uint64]),
     "h32_version": (_INT, []),
     "h32_last_cuda_error": (ctypes.c_char_p, []),
+    "h32_quantize_act_q4_tc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _I64, _INT, _P]),
+    "h32_prepack_weights_q4_0_tc": (_INT, [_P, _P, _I64, _I64, _P, _P, _I64, _P]),
+    "q4_0_x_q4_gemm_tc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -251,3 +255,70 @@ def q4_0_x_q4_gemm_experts(wq, wd, xq, xd, row_idx, expert_off, R, y=None, block
 def h32_device_status(stream=None) -> int:
     """Synchronize the stream and return (and clear) the library's device status."""
     return int(lib().h32_device_status(_stream(stream)))
+
+
+# --------------------------------------------------------------------------
+# tensor-core form (one byte per code: the e4m3 encoding of code * 2^-9)
+# --------------------------------------------------------------------------
+def _round4(n: int) -> int:
+    return (n + 3) // 4 * 4
+
+
+def h32_quantize_act_q4_tc(x, rotate=True, xw=None, xdt=None, stream=None):
+    """x [M][K] bf16/fp32 -> (xw [M][K] uint8 tc-form codes, xdt [K/32][ldxd] fp32 scales,
+    block-major, ldxd = M rounded up to a multiple of 4)."""
+    torch = _torch()
+    _cuda(x, "x")
+    if x.dtype == torch.bfloat16:
+        dt = H32_IN_BF16
+    elif x.dtype == torch.float32:
+        dt = H32_IN_F32
+    else:
+        raise ValueError("x must be bf16 or fp32")
+    ldx = _rows(x, "x")
+    M, K = x.shape
+    if xw is None:
+        xw = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if xdt is None:
+        xdt = torch.zeros((K // 32, _round4(M)), dtype=torch.float32, device=x.device)
+    st = lib().h32_quantize_act_q4_tc(_ptr(x), dt, M, K, ldx, _ptr(xw), _ptr(xdt), xdt.shape[1],
+                                      int(bool(rotate)), _stream(stream))
+    _check("h32_quantize_act_q4_tc", st)
+    return xw, xdt
+
+
+def h32_prepack_weights_q4_0_tc(wq, wd, wp=None, wsc=None, stream=None):
+    """Q4_0 planes (wq [N][K/2], wd [N][K/32] fp16 bits) -> tc form
+    (wp [N][K] uint8, wsc [N][ldws] fp32 = d * 2^18, ldws = K/32 rounded up to 4)."""
+    torch = _torch()
+    _cuda(wq, "wq")
+    _cuda(wd, "wd")
+    N, K = wq.shape[0], wq.shape[1] * 2
+    if wp is None:
+        wp = torch.empty((N, K), dtype=torch.uint8, device=wq.device)
+    if wsc is None:
+        wsc = torch.empty((N, _round4(K // 32)), dtype=torch.float32, device=wq.device)
+    st = lib().h32_prepack_weights_q4_0_tc(_ptr(wq), _ptr(wd), N, K, _ptr(wp), _ptr(wsc),
+                                           wsc.shape[1], _stream(stream))
+    _check("h32_prepack_weights_q4_0_tc", st)
+    return wp, wsc
+
+
+def q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=None, y=None, block_sums=None, stream=None):
+    """The W4A4 product on tc-form operands (bit-identical to q4_0_x_q4_gemm)."""
+    torch = _torch()
+    N, K = wp.shape
+    if M is None:
+        M = xw.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=wp.device)
+    ldy = _rows(y, "y")
+    S = None
+    if block_sums is True:
+        S = torch.empty((M, N, K // 32), dtype=torch.int32, device=wp.device)
+    elif block_sums is not None and block_sums is not False:
+        S = block_sums
+    st = lib().q4_0_x_q4_gemm_tc(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt),
+                                 xdt.shape[1], M, N, K, _ptr(y), ldy, _ptr(S), _stream(stream))
+    _check("q4_0_x_q4_gemm_tc", st)
+    return (y, S) if S is not None else y

@@ -66,12 +66,16 @@ extern "C" h32_status h32_device_status(void *stream) {
     H32_TRY(h32::check_device(nullptr));
     const cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return h32::launch_status(e);
-    h32_status a = h32::quant_read_and_clear_status(s);
-    h32_status b = h32::gemm_read_and_clear_status(s);
-    if (a == H32_ERR_CUDA || b == H32_ERR_CUDA) return H32_ERR_CUDA;
-    if (a == H32_ERR_TIMEOUT || b == H32_ERR_TIMEOUT) return H32_ERR_TIMEOUT;
-    if (a != H32_OK) return a;
-    return b;
+    const h32_status st[3] = {h32::quant_read_and_clear_status(s),
+                              h32::gemm_read_and_clear_status(s),
+                              h32::tc_read_and_clear_status(s)};
+    for (h32_status v : st)
+        if (v == H32_ERR_CUDA) return H32_ERR_CUDA;
+    for (h32_status v : st)
+        if (v == H32_ERR_TIMEOUT) return H32_ERR_TIMEOUT;
+    for (h32_status v : st)
+        if (v != H32_OK) return v;
+    return H32_OK;
 }
 
 extern "C" const char *h32_status_string(h32_status st) {

@@ -215,6 +215,116 @@ __global__ void __launch_bounds__(256) quant_w_kernel(const float *__restrict__ 
     }
 }
 
+// ----------------------------------------------------------------------------
+// tensor-core form: one byte per code, the e4m3 encoding of code * 2^-9
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t byte_sign_mask(uint32_t x) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(r) : "r"(x));
+    return r;
+}
+
+// four int8 codes in [-8, 8] -> four e4m3 bytes (sign | magnitude)
+__device__ __forceinline__ uint32_t tc_bytes(uint32_t c) {
+    const uint32_t m = byte_sign_mask(c);                       // 0xFF where negative
+    const uint32_t mag = (c ^ m) + (m & 0x01010101u);           // |c| per byte, no carries
+    return mag | (m & 0x80808080u);
+}
+
+// Rotate + quantize to 4-bit codes in tc form.  Threads walk the blocks in
+// block-major order (g = b * M + row) so that the transposed scale stores of a
+// warp are contiguous; each lane still reads a whole 64-byte (or 128-byte)
+// block row segment and writes a whole 32-byte code segment.
+template <bool kBf16, bool kRotate>
+__global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restrict__ x, uint32_t nblk,
+                                                          uint32_t M, uint32_t K, int64_t ldx,
+                                                          uint8_t *__restrict__ xw,
+                                                          float *__restrict__ xdt, int64_t ldxd) {
+    const uint32_t stride = gridDim.x * blockDim.x;
+    const uint32_t sb = stride / M, srow = stride % M;
+    uint32_t g = blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t b = g / M, row = g % M;
+    for (; g < nblk; g += stride) {
+        float v[32];
+        if constexpr (kBf16) {
+            load_block_bf16(reinterpret_cast<const uint16_t *>(x) + int64_t(row) * ldx + 32 * b, v);
+        } else {
+            load_block_f32(reinterpret_cast<const float *>(x) + int64_t(row) * ldx + 32 * b, v);
+        }
+        if constexpr (kRotate) rotate32(v);
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const float d = __fdiv_rn(amax, 7.0f);
+        const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+        uint32_t bits[32];
+        if (!(amax < INFINITY) || isinf(id)) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float t = __fmul_rn(v[i], id);
+                t = fminf(fmaxf(t, -8.0f), 7.0f);
+                bits[i] = __float_as_uint(__fadd_rn(t, kRoundMagic));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                bits[i] = __float_as_uint(__fadd_rn(__fmul_rn(v[i], id), kRoundMagic));
+        }
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            w[k] = tc_bytes(
+                pack_low_bytes(bits[4 * k], bits[4 * k + 1], bits[4 * k + 2], bits[4 * k + 3]));
+        uint4 *dst = reinterpret_cast<uint4 *>(xw + int64_t(row) * K + 32 * b);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        xdt[int64_t(b) * ldxd + row] = d;
+        b += sb;
+        row += srow;
+        if (row >= M) {
+            row -= M;
+            ++b;
+        }
+    }
+}
+
+// Q4_0 -> tc form: bytes of (q - 8) * 2^-9 in element order, scale d * 2^18 (exact)
+__global__ void __launch_bounds__(256) prepack_w_tc_kernel(const uint8_t *__restrict__ wq,
+                                                          const uint16_t *__restrict__ wd,
+                                                          uint32_t N, uint32_t nb, uint32_t ldws,
+                                                          uint8_t *__restrict__ wp,
+                                                          float *__restrict__ wsc) {
+    const uint32_t total = N * ldws;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < total; g += stride) {
+        const uint32_t n = g / ldws, b = g - n * ldws;
+        if (b >= nb) {
+            wsc[g] = 0.0f;
+            continue;
+        }
+        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(wq + (int64_t(n) * nb + b) * 16));
+        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            // flipping the top bit of a Q4_0 code gives q - 8 in two's complement;
+            // nibbles -> sign-extended bytes -> tc bytes
+            const uint32_t t = qw[k] ^ 0x88888888u;
+            const uint32_t l = t & 0x0F0F0F0Fu, h = (t >> 4) & 0x0F0F0F0Fu;
+            // sign-extend each 4-bit value to a byte: (v ^ 8) - 8 per byte, done as
+            // v | (0xF0 where bit 3 set)
+            const uint32_t ls = l | (byte_sign_mask(l << 4) & 0xF0F0F0F0u);
+            const uint32_t hs = h | (byte_sign_mask(h << 4) & 0xF0F0F0F0u);
+            lo[k] = tc_bytes(ls);
+            hi[k] = tc_bytes(hs);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(wp + int64_t(n) * nb * 32 + int64_t(b) * 32);
+        dst[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        dst[1] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        wsc[g] = __half2float(__ushort_as_half(__ldg(wd + int64_t(n) * nb + b))) * 262144.0f;
+    }
+}
+
 int grid_for(uint32_t nblk, int sm_count) {
     const uint32_t want = (nblk + 255) / 256;
     const uint32_t cap = static_cast<uint32_t>(sm_count) * 8;
@@ -254,6 +364,10 @@ h32_status quantize_act(const void *x, h32_in_dtype dt, int64_t M, int64_t K, in
 
 h32_status quant_read_and_clear_status(cudaStream_t) { return H32_OK; }
 
+namespace {
+int grid_for_tc(uint32_t nblk, int sm_count) { return grid_for(nblk, sm_count); }
+}  // namespace
+
 }  // namespace h32
 
 extern "C" h32_status h32_quantize_act_q4(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
@@ -284,5 +398,56 @@ extern "C" h32_status h32_rotate_quantize_weights_q4_0(const float *w, int64_t N
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (rotate) quant_w_kernel<true><<<grid, 256, 0, s>>>(w, nblk, wq, wd);
     else quant_w_kernel<false><<<grid, 256, 0, s>>>(w, nblk, wq, wd);
+    return launch_status(cudaGetLastError());
+}
+
+extern "C" h32_status h32_quantize_act_q4_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
+                                             int64_t ldx, uint8_t *xw, float *xdt, int64_t ldxd,
+                                             int rotate, void *stream) {
+    using namespace h32;
+    if (M < 0 || K <= 0 || (K % 32) != 0 || ldx < K || ldxd < M || (ldxd % 4) != 0)
+        return H32_ERR_INVALID_ARG;
+    if (dt != H32_IN_F32 && dt != H32_IN_BF16) return H32_ERR_INVALID_ARG;
+    if (M == 0) return H32_OK;
+    if (!x || !xw || !xdt) return H32_ERR_INVALID_ARG;
+    const int64_t esize = (dt == H32_IN_BF16) ? 2 : 4;
+    if (!aligned16(x) || !aligned16(xw) || !aligned16(xdt) || ((ldx * esize) % 16) != 0)
+        return H32_ERR_ALIGNMENT;
+    if (M * (K / 32) > 0x7FFFFFFFll || M > 0x7FFFFFFFll || K > 0x7FFFFFFFll)
+        return H32_ERR_INVALID_ARG;
+    int sms = 0;
+    H32_TRY(check_device(&sms));
+    const uint32_t nblk = static_cast<uint32_t>(M * (K / 32));
+    const int grid = grid_for_tc(nblk, sms);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint32_t m32 = static_cast<uint32_t>(M), k32 = static_cast<uint32_t>(K);
+    if (dt == H32_IN_BF16) {
+        if (rotate) quant_act_tc_kernel<true, true><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, xw, xdt, ldxd);
+        else quant_act_tc_kernel<true, false><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, xw, xdt, ldxd);
+    } else {
+        if (rotate) quant_act_tc_kernel<false, true><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, xw, xdt, ldxd);
+        else quant_act_tc_kernel<false, false><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, xw, xdt, ldxd);
+    }
+    return launch_status(cudaGetLastError());
+}
+
+extern "C" h32_status h32_prepack_weights_q4_0_tc(const uint8_t *wq, const uint16_t *wd, int64_t N,
+                                                  int64_t K, uint8_t *wp, float *wsc, int64_t ldws,
+                                                  void *stream) {
+    using namespace h32;
+    if (N < 0 || K <= 0 || (K % 32) != 0 || ldws < K / 32 || (ldws % 4) != 0)
+        return H32_ERR_INVALID_ARG;
+    if (N == 0) return H32_OK;
+    if (!wq || !wd || !wp || !wsc) return H32_ERR_INVALID_ARG;
+    if (!aligned16(wq) || !aligned16(wd) || !aligned16(wp) || !aligned16(wsc))
+        return H32_ERR_ALIGNMENT;
+    if (N * ldws > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
+    int sms = 0;
+    H32_TRY(check_device(&sms));
+    const uint32_t total = static_cast<uint32_t>(N * ldws);
+    const int grid = grid_for(total, sms);
+    prepack_w_tc_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        wq, wd, static_cast<uint32_t>(N), static_cast<uint32_t>(K / 32),
+        static_cast<uint32_t>(ldws), wp, wsc);
     return launch_status(cudaGetLastError());
 }

@@ -144,6 +144,55 @@ h32_status q4_0_x_q4_gemm_experts(const uint8_t *wq, const uint16_t *wd, int32_t
                                   float *y, int64_t ldy, int32_t *block_sums, void *stream);
 
 /*
+ * ---------------------------------------------------------------------------
+ * Tensor-core form ("tc form").  GB300 has no integer tensor-core MMA; the
+ * exact 4-bit products run on the FP8 tensor cores, with every code v stored
+ * as one byte: the e4m3 encoding of v * 2^-9 (sign bit | |v|, so 0..7 are
+ * e4m3 subnormals and 8 the smallest normal).  The calls below produce and
+ * consume that form directly, so the GEMM needs no widening step: weights are
+ * repacked once, offline (lossless: the same codes and scales), and the
+ * activation quantizer writes the tc form.  Results are bit-identical to the
+ * Q4_0 entry points above.
+ * ---------------------------------------------------------------------------
+ */
+
+/*
+ * Rotate and quantize activations exactly as h32_quantize_act_q4, writing the
+ * codes in tc form and the scales block-major:
+ *   xw     [M][K] out: one byte per code, e4m3 of code * 2^-9, element order
+ *   xdt    [K/32][ldxd] out: fp32 scales, xdt[b][m] = d of row m, block b
+ *   ldxd   >= M, a multiple of 4 (entries m >= M are left untouched)
+ */
+h32_status h32_quantize_act_q4_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
+                                  int64_t ldx, uint8_t *xw, float *xdt, int64_t ldxd, int rotate,
+                                  void *stream);
+
+/*
+ * Repack Q4_0 weights (as written by h32_rotate_quantize_weights_q4_0) into
+ * tc form, once, offline:
+ *   wp     [N][K] out: one byte per weight, e4m3 of (q - 8) * 2^-9, element order
+ *   wsc    [N][ldws] out: fp32 d * 2^18 (exact), ldws >= K/32, a multiple of 4;
+ *          entries b >= K/32 are written as 0
+ */
+h32_status h32_prepack_weights_q4_0_tc(const uint8_t *wq, const uint16_t *wd, int64_t N,
+                                       int64_t K, uint8_t *wp, float *wsc, int64_t ldws,
+                                       void *stream);
+
+/*
+ * The W4A4 product of q4_0_x_q4_gemm on tc-form operands:
+ *   y[m][n] = sum over blocks b in order of acc = fma(fp32(d_w * d_x), S, acc)
+ * with d_w = wsc[n][b] * 2^-18, d_x = xdt[b][m], bit-identical to q4_0_x_q4_gemm.
+ *   wp, wsc, ldws   from h32_prepack_weights_q4_0_tc
+ *   xw, xdt, ldxd   from h32_quantize_act_q4_tc
+ *   y               [M][ldy] fp32 out;  block_sums nullable int32 [M][N][K/32]
+ * Requires K % 128 == 0 and N % 16 == 0.
+ */
+h32_status q4_0_x_q4_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws,
+                             const uint8_t *xw, const float *xdt, int64_t ldxd, int64_t M,
+                             int64_t N, int64_t K, float *y, int64_t ldy, int32_t *block_sums,
+                             void *stream);
+
+/*
  * Synchronize `stream`, then report and clear the device status word of every
  * kernel this library launched on the current device since the last call:
  * H32_OK, H32_ERR_TIMEOUT or H32_ERR_DEVICE_GUARD (or H32_ERR_CUDA when the

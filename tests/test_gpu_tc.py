@@ -1,0 +1,108 @@
+"""GPU parity of the tensor-core-form path against the CPU oracle.
+
+The tc form stores every 4-bit code v as the e4m3 byte of v * 2^-9 (the
+exact operand form of the FP8 tensor cores).  The bytes are decoded here with
+an independent e4m3 decoder; codes and scales must equal the oracle's, and the
+tc GEMM must equal the oracle's same-order fp32 result bit for bit ("509
+tokens a second of prompt: the Hadamard route ships", sections "Why prompts
+are a matrix-unit problem" and "The rotation")."""
+import numpy as np
+import pytest
+
+import oracle
+from hadamard_rotated_bit_gb300 import workloads as wl
+from tests._gpu import np_of, torch_bf16, torch_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def h32():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import hadamard_rotated_bit_gb300 as m
+    from hadamard_rotated_bit_gb300 import _build
+    _build.build()
+    return m
+
+
+def e4m3_value(b: np.ndarray) -> np.ndarray:
+    """IEEE-style e4m3 (bias 7, subnormals, no infinities) -> float64."""
+    b = b.astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = b & 7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * 2.0 ** (e - 7.0))
+    return sign * mag
+
+
+def test_prepack_matches_q4_0(h32):
+    w = wl.weights_normal(80, 384, 0.02, 0, wl.CFG_TEST, 200)
+    wq, wd = oracle.quantize_weights_q4_0(w)
+    wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(wq), torch_of(wd.view(np.int16)))
+    wp, wsc = np_of(wp), np_of(wsc)
+    codes = oracle.decode_w4(wq, 384).astype(np.float64)
+    assert np.array_equal(e4m3_value(wp) * 2.0 ** 9, codes)
+    nb = 384 // 32
+    assert wsc.shape == (80, 12)
+    assert np.array_equal(wsc.astype(np.float64), wd.view(np.float16).astype(np.float64) * 2.0 ** 18)
+    w2 = wl.weights_normal(16, 160, 0.02, 0, wl.CFG_TEST, 201)   # nb = 5, padded to 8
+    wq2, wd2 = oracle.quantize_weights_q4_0(w2)
+    wp2, wsc2 = h32.h32_prepack_weights_q4_0_tc(torch_of(wq2), torch_of(wd2.view(np.int16)))
+    wsc2 = np_of(wsc2)
+    assert wsc2.shape == (16, 8) and np.all(wsc2[:, 5:] == 0)
+
+
+@pytest.mark.parametrize("M,K", [(1, 128), (37, 256), (512, 5120)])
+def test_quantize_tc_matches_oracle(h32, M, K):
+    x = wl.f32_to_bf16_bits(wl.act_normal_outliers(M, K, 0.005, 30.0, 0, wl.CFG_TEST, 210 + M))
+    xw, xdt = h32.h32_quantize_act_q4_tc(torch_bf16(x))
+    xw, xdt = np_of(xw), np_of(xdt)
+    rq, rd = oracle.quantize_act_q4(x)
+    codes = oracle.decode_act4(rq, K).astype(np.float64)
+    assert np.array_equal(e4m3_value(xw) * 2.0 ** 9, codes)
+    assert np.array_equal(xdt[:, :M].T.view(np.uint32), rd.view(np.uint32))
+
+
+def _tc_operands(h32, x_bits, w):
+    wq, wd = oracle.quantize_weights_q4_0(w)
+    xq, xd = oracle.quantize_act_q4(x_bits)
+    wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(wq), torch_of(wd.view(np.int16)))
+    xw, xdt = h32.h32_quantize_act_q4_tc(torch_bf16(x_bits))
+    return (wq, wd, xq, xd), (wp, wsc, xw, xdt)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 16, 128), (17, 144, 256), (64, 256, 512), (129, 128, 384),
+                                   (300, 384, 1024)])
+def test_gemm_tc_bit_exact(h32, M, N, K):
+    import torch
+    x = wl.f32_to_bf16_bits(wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, 220 + M))
+    w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, 221 + N)
+    (wq, wd, xq, xd), (wp, wsc, xw, xdt) = _tc_operands(h32, x, w)
+    y, S = h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M, block_sums=True)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r32, r64, rS = oracle.gemm(wq, wd, xq, xd, K, want_block_sums=True)
+    assert np.array_equal(np_of(S).astype(np.int64), rS)
+    assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
+    y2 = h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M)
+    assert np.array_equal(np_of(y2).view(np.uint32), r32.view(np.uint32))
+
+
+@pytest.mark.parametrize("proj", ["attn", "ffn_gate_up", "ffn_down"])
+def test_gemm_tc_pp512_sampled(h32, proj):
+    import torch
+    p = {q.name: q for q in (wl.ATTN, wl.FFN_GATE_UP, wl.FFN_DOWN)}[proj]
+    cid = wl.CFG_ATTN if p is wl.ATTN else wl.CFG_FFN
+    x = p.activations(512, 0, cid)
+    w = p.weights(0, cid)
+    (wq, wd, xq, xd), (wp, wsc, xw, xdt) = _tc_operands(h32, x, w)
+    y = np_of(h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=512))
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r = np.random.default_rng(1)
+    mi = np.concatenate([r.integers(0, 512, 3000), [0, 511]])
+    ni = np.concatenate([r.integers(0, p.N, 3000), [p.N - 1, 0]])
+    r32, _, _ = oracle.gemm_sampled(wq, wd, xq, xd, p.K, mi, ni)
+    assert np.array_equal(y[mi, ni].view(np.uint32), r32.view(np.uint32))

@@ -258,7 +258,7 @@ def h32_device_status(stream=None) -> int:
 
 
 # --------------------------------------------------------------------------
-# tensor-core form (one byte per code: the e4m3 encoding of code * 2^-9)
+# tensor-core form (one byte per code: the e4m3 encoding of the integer code)
 # --------------------------------------------------------------------------
 def _round4(n: int) -> int:
     return (n + 3) // 4 * 4
@@ -289,7 +289,7 @@ def h32_quantize_act_q4_tc(x, rotate=True, xw=None, xdt=None, stream=None):
 
 def h32_prepack_weights_q4_0_tc(wq, wd, wp=None, wsc=None, stream=None):
     """Q4_0 planes (wq [N][K/2], wd [N][K/32] fp16 bits) -> tc form
-    (wp [N][K] uint8, wsc [N][ldws] fp32 = d * 2^18, ldws = K/32 rounded up to 4)."""
+    (wp [N][K] uint8, wsc [N][ldws] fp32 = d, ldws = K/32 rounded up to 4)."""
     torch = _torch()
     _cuda(wq, "wq")
     _cuda(wd, "wd")

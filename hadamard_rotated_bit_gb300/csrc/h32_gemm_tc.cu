@@ -7,8 +7,11 @@
 // accumulated in block order, acc = fma(fp32(d_w * d_x), S, acc), bit for bit.
 //
 // Here both operands arrive already in the byte form the FP8 tensor cores
-// consume (each code v as the e4m3 byte of v * 2^-9): the weights repacked
-// once offline, the activations written so by their quantizer.  The kernel is
+// consume (each code v as the e4m3 byte of the integer v, exact for |v| <= 8):
+// the weights repacked once offline, the activations written so by their
+// quantizer.  One K = 32 MMA yields the block sum S itself, exact in fp32 (an
+// integer of magnitude <= 2048), so the epilogue is the definition as written
+// for every finite scale, subnormal products included.  The kernel is
 // therefore a plain warp-specialised pipeline with no widening step:
 //   warp 0      TMA producer: per 128-element K stage, a 128-row weight tile
 //               and a token tile (128-byte rows, 128B-swizzled, consumed by
@@ -31,6 +34,11 @@
 
 #ifndef H32_TC_EPI_PER_QUAD
 #define H32_TC_EPI_PER_QUAD 2
+#endif
+// 1: issue every TMEM load of a block before one wait (one exposed latency per
+// block instead of one per 16-column chunk)
+#ifndef H32_TC_LD_ALL
+#define H32_TC_LD_ALL 0
 #endif
 
 namespace h32 {
@@ -283,12 +291,23 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
                         const float dw = dws[j];
                         const float *dxj = sb + j * a.bn + c0;
                         const uint32_t tcol = tmem + lane_addr + (gb * kGroup + i) * 128 + c0;
+#if H32_TC_LD_ALL
+                        uint32_t vv[C::kMaxChunks][16];
+#pragma unroll
+                        for (int c = 0; c < C::kMaxChunks; ++c)
+                            if (c < nch) tmem_ld_x16(tcol + c * 16, vv[c]);
+                        tmem_ld_wait();
+#endif
 #pragma unroll
                         for (int c = 0; c < C::kMaxChunks; ++c) {
                             if (c < nch) {
+#if H32_TC_LD_ALL
+                                uint32_t (&v)[16] = vv[c];
+#else
                                 uint32_t v[16];
                                 tmem_ld_x16(tcol + c * 16, v);
                                 tmem_ld_wait();
+#endif
                                 fold16(acc + 8 * c, dw, dxj + 16 * c, v);
                                 if constexpr (kSums) {
                                     const int n = ti.n0 + row;
@@ -302,7 +321,7 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
                                         for (int q = 0; q < 16; ++q)
                                             if (q < lim_q)
                                                 bp[q * step] =
-                                                    __float2int_rn(__uint_as_float(v[q]) * 262144.0f);
+                                                    __float2int_rn(__uint_as_float(v[q]));
                                     }
                                 }
                             }

@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(256) quant_w_kernel(const float *__restrict__ 
 }
 
 // ----------------------------------------------------------------------------
-// tensor-core form: one byte per code, the e4m3 encoding of code * 2^-9
+// tensor-core form: one byte per code, the e4m3 encoding of the integer code
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t byte_sign_mask(uint32_t x) {
     uint32_t r;
@@ -224,11 +224,24 @@ __device__ __forceinline__ uint32_t byte_sign_mask(uint32_t x) {
     return r;
 }
 
-// four int8 codes in [-8, 8] -> four e4m3 bytes (sign | magnitude)
+// four magnitudes 0..8 (one per byte) -> their e4m3 bytes.  e4m3 (bias 7,
+// 3 mantissa bits) holds every integer up to 16 exactly: 1 = 0x38, 2 = 0x40,
+// 3 = 0x44, 4 = 0x48, 5 = 0x4A, 6 = 0x4C, 7 = 0x4E, 8 = 0x50.  A byte permute
+// looks 0..7 up in an 8-byte table; the selector nibble 8 picks table byte 0
+// (0x00) in sign-replicate mode, which stays 0x00, and 8 is then or-ed in.
+__device__ __forceinline__ uint32_t e4m3_of_magnitudes(uint32_t mag) {
+    const uint32_t sel = (mag & 0xFu) | ((mag >> 4) & 0xF0u) | ((mag >> 8) & 0xF00u) |
+                         ((mag >> 12) & 0xF000u);
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(0x44403800u), "r"(0x4E4C4A48u), "r"(sel));
+    return r | (((mag >> 3) & 0x01010101u) * 0x50u);
+}
+
+// four int8 codes in [-8, 8] -> four e4m3 bytes (sign bit | e4m3 of |c|)
 __device__ __forceinline__ uint32_t tc_bytes(uint32_t c) {
     const uint32_t m = byte_sign_mask(c);                       // 0xFF where negative
     const uint32_t mag = (c ^ m) + (m & 0x01010101u);           // |c| per byte, no carries
-    return mag | (m & 0x80808080u);
+    return e4m3_of_magnitudes(mag) | (m & 0x80808080u);
 }
 
 // Rotate + quantize to 4-bit codes in tc form.  Threads walk the blocks in
@@ -288,7 +301,7 @@ __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restric
     }
 }
 
-// Q4_0 -> tc form: bytes of (q - 8) * 2^-9 in element order, scale d * 2^18 (exact)
+// Q4_0 -> tc form: e4m3 bytes of q - 8 in element order, scale d widened to fp32
 __global__ void __launch_bounds__(256) prepack_w_tc_kernel(const uint8_t *__restrict__ wq,
                                                           const uint16_t *__restrict__ wd,
                                                           uint32_t N, uint32_t nb, uint32_t ldws,
@@ -321,7 +334,7 @@ __global__ void __launch_bounds__(256) prepack_w_tc_kernel(const uint8_t *__rest
         uint4 *dst = reinterpret_cast<uint4 *>(wp + int64_t(n) * nb * 32 + int64_t(b) * 32);
         dst[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         dst[1] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        wsc[g] = __half2float(__ushort_as_half(__ldg(wd + int64_t(n) * nb + b))) * 262144.0f;
+        wsc[g] = __half2float(__ushort_as_half(__ldg(wd + int64_t(n) * nb + b)));
     }
 }
 

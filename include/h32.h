@@ -147,8 +147,9 @@ h32_status q4_0_x_q4_gemm_experts(const uint8_t *wq, const uint16_t *wd, int32_t
  * ---------------------------------------------------------------------------
  * Tensor-core form ("tc form").  GB300 has no integer tensor-core MMA; the
  * exact 4-bit products run on the FP8 tensor cores, with every code v stored
- * as one byte: the e4m3 encoding of v * 2^-9 (sign bit | |v|, so 0..7 are
- * e4m3 subnormals and 8 the smallest normal).  The calls below produce and
+ * as one byte: the e4m3 encoding of the integer v itself (every integer of
+ * magnitude 0..8 is exact in e4m3, so each 32-term block sum S comes out of
+ * the MMA exact, as an integer-valued fp32).  The calls below produce and
  * consume that form directly, so the GEMM needs no widening step: weights are
  * repacked once, offline (lossless: the same codes and scales), and the
  * activation quantizer writes the tc form.  Results are bit-identical to the
@@ -159,7 +160,7 @@ h32_status q4_0_x_q4_gemm_experts(const uint8_t *wq, const uint16_t *wd, int32_t
 /*
  * Rotate and quantize activations exactly as h32_quantize_act_q4, writing the
  * codes in tc form and the scales block-major:
- *   xw     [M][K] out: one byte per code, e4m3 of code * 2^-9, element order
+ *   xw     [M][K] out: one byte per code, the e4m3 encoding of the code, element order
  *   xdt    [K/32][ldxd] out: fp32 scales, xdt[b][m] = d of row m, block b
  *   ldxd   >= M, a multiple of 4 (entries m >= M are left untouched)
  */
@@ -170,8 +171,8 @@ h32_status h32_quantize_act_q4_tc(const void *x, h32_in_dtype dt, int64_t M, int
 /*
  * Repack Q4_0 weights (as written by h32_rotate_quantize_weights_q4_0) into
  * tc form, once, offline:
- *   wp     [N][K] out: one byte per weight, e4m3 of (q - 8) * 2^-9, element order
- *   wsc    [N][ldws] out: fp32 d * 2^18 (exact), ldws >= K/32, a multiple of 4;
+ *   wp     [N][K] out: one byte per weight, the e4m3 encoding of q - 8, element order
+ *   wsc    [N][ldws] out: fp32 d (exact widening of the fp16), ldws >= K/32, a multiple of 4;
  *          entries b >= K/32 are written as 0
  */
 h32_status h32_prepack_weights_q4_0_tc(const uint8_t *wq, const uint16_t *wd, int64_t N,
@@ -181,7 +182,8 @@ h32_status h32_prepack_weights_q4_0_tc(const uint8_t *wq, const uint16_t *wd, in
 /*
  * The W4A4 product of q4_0_x_q4_gemm on tc-form operands:
  *   y[m][n] = sum over blocks b in order of acc = fma(fp32(d_w * d_x), S, acc)
- * with d_w = wsc[n][b] * 2^-18, d_x = xdt[b][m], bit-identical to q4_0_x_q4_gemm.
+ * with d_w = wsc[n][b], d_x = xdt[b][m], bit-identical to q4_0_x_q4_gemm for
+ * every finite scale (subnormal products d_w * d_x included).
  *   wp, wsc, ldws   from h32_prepack_weights_q4_0_tc
  *   xw, xdt, ldxd   from h32_quantize_act_q4_tc
  *   y               [M][ldy] fp32 out;  block_sums nullable int32 [M][N][K/32]

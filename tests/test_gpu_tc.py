@@ -1,6 +1,6 @@
 """GPU parity of the tensor-core-form path against the CPU oracle.
 
-The tc form stores every 4-bit code v as the e4m3 byte of v * 2^-9 (the
+The tc form stores every 4-bit code v as the e4m3 byte of the integer v (the
 exact operand form of the FP8 tensor cores).  The bytes are decoded here with
 an independent e4m3 decoder; codes and scales must equal the oracle's, and the
 tc GEMM must equal the oracle's same-order fp32 result bit for bit ("509
@@ -43,10 +43,10 @@ def test_prepack_matches_q4_0(h32):
     wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(wq), torch_of(wd.view(np.int16)))
     wp, wsc = np_of(wp), np_of(wsc)
     codes = oracle.decode_w4(wq, 384).astype(np.float64)
-    assert np.array_equal(e4m3_value(wp) * 2.0 ** 9, codes)
+    assert np.array_equal(e4m3_value(wp), codes)
     nb = 384 // 32
     assert wsc.shape == (80, 12)
-    assert np.array_equal(wsc.astype(np.float64), wd.view(np.float16).astype(np.float64) * 2.0 ** 18)
+    assert np.array_equal(wsc.astype(np.float64), wd.view(np.float16).astype(np.float64))
     w2 = wl.weights_normal(16, 160, 0.02, 0, wl.CFG_TEST, 201)   # nb = 5, padded to 8
     wq2, wd2 = oracle.quantize_weights_q4_0(w2)
     wp2, wsc2 = h32.h32_prepack_weights_q4_0_tc(torch_of(wq2), torch_of(wd2.view(np.int16)))
@@ -61,15 +61,16 @@ def test_quantize_tc_matches_oracle(h32, M, K):
     xw, xdt = np_of(xw), np_of(xdt)
     rq, rd = oracle.quantize_act_q4(x)
     codes = oracle.decode_act4(rq, K).astype(np.float64)
-    assert np.array_equal(e4m3_value(xw) * 2.0 ** 9, codes)
+    assert np.array_equal(e4m3_value(xw), codes)
     assert np.array_equal(xdt[:, :M].T.view(np.uint32), rd.view(np.uint32))
 
 
-def _tc_operands(h32, x_bits, w):
+def _tc_operands(h32, x, w, bf16=True):
+    """x: bf16 bits (uint16) when bf16, else fp32."""
     wq, wd = oracle.quantize_weights_q4_0(w)
-    xq, xd = oracle.quantize_act_q4(x_bits)
+    xq, xd = oracle.quantize_act_q4(x)
     wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(wq), torch_of(wd.view(np.int16)))
-    xw, xdt = h32.h32_quantize_act_q4_tc(torch_bf16(x_bits))
+    xw, xdt = h32.h32_quantize_act_q4_tc(torch_bf16(x) if bf16 else torch_of(x))
     return (wq, wd, xq, xd), (wp, wsc, xw, xdt)
 
 
@@ -88,6 +89,71 @@ def test_gemm_tc_bit_exact(h32, M, N, K):
     assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
     y2 = h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M)
     assert np.array_equal(np_of(y2).view(np.uint32), r32.view(np.uint32))
+
+
+def test_gemm_tc_tiny_scales(h32):
+    """Rows of magnitude ~1e-33 put d_w * d_x below the normal fp32 range; the
+    tc GEMM takes no special path and must still equal the sequential fp32
+    definition bit for bit."""
+    import torch
+    M, N, K = 32, 64, 256
+    x = wl.act_normal_outliers(M, K, 0.0, 1.0, 0, wl.CFG_TEST, 230)
+    x[::4] *= np.float32(1e-33)
+    x[1::4] *= np.float32(1e30)
+    w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, 231)
+    (wq, wd, xq, xd), (wp, wsc, xw, xdt) = _tc_operands(h32, x, w, bf16=False)
+    y, S = h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M, block_sums=True)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r32, _, rS = oracle.gemm(wq, wd, xq, xd, K, want_block_sums=True)
+    assert np.array_equal(np_of(S).astype(np.int64), rS)
+    assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
+
+
+def test_gemm_tc_extreme_codes(h32):
+    """Weight value -8 against activation code -8 (S = 2048 per block, the
+    largest block sum), next to +7 and all-zero blocks; e4m3 bytes are built
+    here from their definition, independently of the quantizer."""
+    import torch
+    M, N, K = 40, 32, 256
+    xc = np.full((M, K), -8, np.int64)
+    xc[::3] = 7
+    xc[1::5] = 0
+    wc = np.zeros((N, K), np.int64)
+    wc[::2] = -8
+    wc[1::4] = 7
+
+    def e4m3_bytes(c):
+        lut = {0: 0x00, 1: 0x38, 2: 0x40, 3: 0x44, 4: 0x48, 5: 0x4A, 6: 0x4C, 7: 0x4E, 8: 0x50}
+        mag = np.vectorize(lut.get)(np.abs(c))
+        return (mag | np.where(c < 0, 0x80, 0)).astype(np.uint8)
+
+    assert np.array_equal(e4m3_value(e4m3_bytes(np.arange(-8, 9))), np.arange(-8, 9))
+    xd = np.full((M, K // 32), 0.5, np.float32)
+    xd[2::7] = 1e-30
+    wd = oracle.f32_to_f16(np.full((N, K // 32), 0.25, np.float32))
+    # the same operands in the oracle's nibble layout: element j < 16 of a
+    # block in the low nibble of byte j, element j + 16 in its high nibble
+    def pack(u):
+        u = u.reshape(u.shape[0], -1, 32)
+        return ((u[:, :, :16] & 15) | ((u[:, :, 16:] & 15) << 4)).reshape(u.shape[0], -1).astype(np.uint8)
+
+    wq = pack(wc + 8)
+    xq = pack(xc)
+    assert np.array_equal(oracle.decode_w4(wq, K), wc)
+    assert np.array_equal(oracle.decode_act4(xq, K), xc)
+    wsc = np.zeros((N, 8), np.float32)
+    wsc[:, :K // 32] = wd.view(np.float16).astype(np.float32)
+    xdt = np.zeros((K // 32, M), np.float32)
+    xdt[:, :] = xd.T
+    y, S = h32.q4_0_x_q4_gemm_tc(torch_of(e4m3_bytes(wc)), torch_of(wsc), torch_of(e4m3_bytes(xc)),
+                                 torch_of(xdt), M=M, block_sums=True)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r32, _, rS = oracle.gemm(wq, wd, xq, xd, K, want_block_sums=True)
+    assert np.abs(rS).max() == 2048
+    assert np.array_equal(np_of(S).astype(np.int64), rS)
+    assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
 
 
 @pytest.mark.parametrize("proj", ["attn", "ffn_gate_up", "ffn_down"])

@@ -40,9 +40,20 @@ M_TOKENS = 512
 WORKLOAD = ("pp512 GEMM chain, rotated 4-bit route: 512 tokens through attention "
             "5120->5120, FFN gate/up 5120->34816, FFN down 17408->5120 "
             "(quantize activations + W4A4 GEMM per projection)")
+# operand forms of the chain: "tc" = weights repacked once into tensor-core bytes,
+# activations quantized straight into that form; "q4_0" = Q4_0 weights and
+# nibble-packed activations consumed directly
+FORMS = ("tc", "q4_0")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_w4a4_pp512_ffn_gate_up.md")
-GEMM_SOURCE = os.path.join(ROOT, "hadamard_rotated_bit_gb300", "csrc", "h32_gemm.cu")
+_CSRC = os.path.join(ROOT, "hadamard_rotated_bit_gb300", "csrc")
+PROFILE_SUMMARY = {"tc": os.path.join(ROOT, "profiles", "gemm_tc_w4a4_pp512_ffn_gate_up.md"),
+                   "q4_0": os.path.join(ROOT, "profiles", "gemm_w4a4_pp512_ffn_gate_up.md")}
+# the sources a GEMM kernel is compiled from (the profile's traffic is only
+# reported while they are unchanged)
+GEMM_SOURCES = {"tc": [os.path.join(_CSRC, f) for f in ("h32_gemm_tc.cu", "h32_common.cuh",
+                                                        "h32_epilogue.cuh")],
+                "q4_0": [os.path.join(_CSRC, f) for f in ("h32_gemm.cu", "h32_common.cuh",
+                                                          "h32_epilogue.cuh")]}
 SMS = 152
 FP32_LANES_PER_SM = 128   # FP32 FMA/FMUL lanes per SM per clock
 
@@ -97,21 +108,24 @@ def load_peaks():
                 "sm_max_mhz": 2070.0}, "fallback"
 
 
-def source_sha(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_sha(paths) -> str:
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def profiled_traffic():
+def profiled_traffic(form):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel source (else None)."""
+    summary, if it was taken on the current kernel sources (else None)."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(PROFILE_SUMMARY[form]).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(source sha256/16:\s*([0-9a-f]+)\)",
                   text)
-    if not m or m.group(2) != source_sha(GEMM_SOURCE):
+    if not m or m.group(2) != source_sha(GEMM_SOURCES[form]):
         return None
     return float(m.group(1))
 
@@ -172,8 +186,8 @@ class ClockSampler:
 class Chain:
     """Resident inputs, outputs and intermediate buffers of the pp512 chain."""
 
-    def __init__(self, torch, h32, device, sets=2, seed=0):
-        self.torch, self.h32, self.device = torch, h32, device
+    def __init__(self, torch, h32, device, sets=2, seed=0, form="tc"):
+        self.torch, self.h32, self.device, self.form = torch, h32, device, form
         self.sets = []
         base = []
         for p in CHAIN:
@@ -181,54 +195,70 @@ class Chain:
             w = torch.from_numpy(p.weights(seed, cid)).to(device)
             wq, wd = h32.h32_rotate_quantize_weights_q4_0(w)
             del w
+            if form == "tc":   # the offline repack, once per weight matrix
+                wq, wd = h32.h32_prepack_weights_q4_0_tc(wq, wd)
             xb = p.activations(M_TOKENS, seed, cid)
             x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(device)
             base.append((wq, wd, x))
         for s in range(sets):
             projs = []
             for (wq, wd, x) in base:
-                projs.append({
-                    "wq": wq if s == 0 else wq.clone(), "wd": wd if s == 0 else wd.clone(),
-                    "x": x if s == 0 else x.clone(),
-                    "xq": torch.empty((M_TOKENS, x.shape[1] // 2), dtype=torch.uint8, device=device),
-                    "xd": torch.empty((M_TOKENS, x.shape[1] // 32), dtype=torch.float32,
-                                      device=device),
-                    "y": torch.empty((M_TOKENS, wq.shape[0]), dtype=torch.float32, device=device),
-                })
+                K = x.shape[1]
+                d = {"wq": wq if s == 0 else wq.clone(), "wd": wd if s == 0 else wd.clone(),
+                     "x": x if s == 0 else x.clone(),
+                     "y": torch.empty((M_TOKENS, wq.shape[0]), dtype=torch.float32, device=device)}
+                if form == "tc":
+                    d["xq"] = torch.empty((M_TOKENS, K), dtype=torch.uint8, device=device)
+                    d["xd"] = torch.zeros((K // 32, M_TOKENS), dtype=torch.float32, device=device)
+                else:
+                    d["xq"] = torch.empty((M_TOKENS, K // 2), dtype=torch.uint8, device=device)
+                    d["xd"] = torch.empty((M_TOKENS, K // 32), dtype=torch.float32, device=device)
+                projs.append(d)
             self.sets.append(projs)
         torch.cuda.synchronize()
 
     def step(self, s, stream, events=None):
         """Enqueue one chain pass on `stream`; optionally bracket each kernel with events."""
         h = self.h32
+        tc = self.form == "tc"
         for i, p in enumerate(self.sets[s % len(self.sets)]):
             if events is not None:
                 events[2 * i][0].record(stream)
-            h.h32_quantize_act_q4(p["x"], xq=p["xq"], xd=p["xd"], stream=stream)
+            if tc:
+                h.h32_quantize_act_q4_tc(p["x"], xw=p["xq"], xdt=p["xd"], stream=stream)
+            else:
+                h.h32_quantize_act_q4(p["x"], xq=p["xq"], xd=p["xd"], stream=stream)
             if events is not None:
                 events[2 * i][1].record(stream)
                 events[2 * i + 1][0].record(stream)
-            h.q4_0_x_q4_gemm(p["wq"], p["wd"], p["xq"], p["xd"], y=p["y"], stream=stream)
+            if tc:
+                h.q4_0_x_q4_gemm_tc(p["wq"], p["wd"], p["xq"], p["xd"], M=M_TOKENS, y=p["y"],
+                                    stream=stream)
+            else:
+                h.q4_0_x_q4_gemm(p["wq"], p["wd"], p["xq"], p["xd"], y=p["y"], stream=stream)
             if events is not None:
                 events[2 * i + 1][1].record(stream)
 
 
-def kernel_names():
+def kernel_names(form):
+    sfx = "_tc" if form == "tc" else ""
     names = []
     for p in CHAIN:
-        names += [f"quantize_act_q4[{p.name}]", f"q4_0_x_q4_gemm[{p.name}]"]
+        names += [f"h32_quantize_act_q4{sfx}[{p.name}]", f"q4_0_x_q4_gemm{sfx}[{p.name}]"]
     return names
 
 
-def algorithmic(p):
+def algorithmic(p, form="tc"):
     """Per-launch algorithmic work of one projection (M = 512)."""
     M, N, K = M_TOKENS, p.N, p.K
     nb = K // 32
+    code = 1 if form == "tc" else 0.5          # bytes per stored 4-bit code
+    wscale = 4 if form == "tc" else 2          # fp32 (tc) or fp16 (Q4_0) weight scales
     return {
-        "quant_bytes": M * K * 2 + M * K // 2 + M * nb * 4,       # bf16 in, nibbles + scales out
+        "quant_bytes": int(M * K * 2 + M * K * code + M * nb * 4),   # bf16 in, codes + scales out
         "gemm_alu_ops": 2 * M * N * nb,                            # d_w*d_x and one fma per block
         "gemm_int_ops": 2 * M * N * K,                             # 2 MNK (multiply + add)
-        "gemm_bytes": N * K // 2 + N * nb * 2 + M * K // 2 + M * nb * 4 + M * N * 4,
+        "gemm_bytes": int(N * K * code + N * nb * wscale + M * K * code + M * nb * 4 + M * N * 4),
     }
 
 
@@ -245,7 +275,7 @@ def run_gpu(args):
     barrier(dist, device)
     h32.lib()
 
-    chain = Chain(torch, h32, device)
+    chain = Chain(torch, h32, device, form=args.form)
     stream = torch.cuda.Stream(device)
     peaks, peak_src = load_peaks()
 
@@ -297,17 +327,17 @@ def run_gpu(args):
     e2e = time_e2e(torch, h32, chain, stream, args, dist, device, world)
 
     # roofline of the dominant kernel
-    names = kernel_names()
+    names = kernel_names(args.form)
     dom = int(np.argmax(per_kernel))
     p = CHAIN[dom // 2]
-    alg = algorithmic(p)
+    alg = algorithmic(p, args.form)
     clock_mhz = float(peaks.get("sm_max_mhz", 2070.0))
     if dom % 2 == 1:
         alu_peak = SMS * FP32_LANES_PER_SM * clock_mhz * 1e6 / 1e12  # T lane-ops/s
         achieved = alg["gemm_alu_ops"] / (per_kernel[dom] / 1e3) / 1e12
         roofline = {"kernel": names[dom], "bound": "alu", "achieved": round(achieved, 3),
                     "peak": round(alu_peak, 3), "unit": "Tops/s (fp32 lane ops)",
-                    "frac": round(achieved / alu_peak, 4), "traffic": profiled_traffic(),
+                    "frac": round(achieved / alu_peak, 4), "traffic": profiled_traffic(args.form),
                     "peak_source": f"{SMS} SMs x {FP32_LANES_PER_SM} FP32 lanes x "
                                    f"{clock_mhz:.0f} MHz ({peak_src} max SM clock)",
                     "algorithmic_per_launch": alg["gemm_alu_ops"],
@@ -323,7 +353,7 @@ def run_gpu(args):
     fp8_peak = 2.0 * float(peaks["bf16_tflops"])           # nominal fp8 : bf16 ratio 2
     kernels = {}
     for i, p in enumerate(CHAIN):
-        alg = algorithmic(p)
+        alg = algorithmic(p, args.form)
         tq, tg = per_kernel[2 * i], per_kernel[2 * i + 1]
         kernels[p.name] = {
             "quant_ms": round(tq, 5),
@@ -343,6 +373,7 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int4 codes (exact products), fp32 epilogue", "data": "synthetic",
         "config": {"workload": WORKLOAD, "tokens_per_step": M_TOKENS,
+                   "operand_form": args.form,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: two alternating input sets of 193 MB each"},
         "roofline": roofline,
@@ -470,22 +501,32 @@ def run_only_gemm(args):
     dev = torch.device("cuda", 0)
     wq, wd = h32.h32_rotate_quantize_weights_q4_0(torch.from_numpy(p.weights(0, cid)).to(dev))
     x = torch.from_numpy(p.activations(M_TOKENS, 0, cid).view(np.int16)).view(torch.bfloat16).to(dev)
-    xq, xd = h32.h32_quantize_act_q4(x)
     y = torch.empty((M_TOKENS, p.N), dtype=torch.float32, device=dev)
+    if args.form == "tc":
+        wq, wd = h32.h32_prepack_weights_q4_0_tc(wq, wd)
+        xq, xd = h32.h32_quantize_act_q4_tc(x)
+
+        def gemm():
+            h32.q4_0_x_q4_gemm_tc(wq, wd, xq, xd, M=M_TOKENS, y=y)
+    else:
+        xq, xd = h32.h32_quantize_act_q4(x)
+
+        def gemm():
+            h32.q4_0_x_q4_gemm(wq, wd, xq, xd, y=y)
     for _ in range(args.warmup):
-        h32.q4_0_x_q4_gemm(wq, wd, xq, xd, y=y)
+        gemm()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t0.record()
     for _ in range(args.steps):
-        h32.q4_0_x_q4_gemm(wq, wd, xq, xd, y=y)
+        gemm()
     t1.record()
     torch.cuda.synchronize()
     if h32.h32_device_status() != 0:
         raise RuntimeError("device status not OK")
     ms = t0.elapsed_time(t1) / args.steps
-    alg = algorithmic(p)
-    return {"only_gemm": p.name, "ms_per_launch": round(ms, 5),
+    alg = algorithmic(p, args.form)
+    return {"only_gemm": p.name, "form": args.form, "ms_per_launch": round(ms, 5),
             "eff_TOPS": round(alg["gemm_int_ops"] / (ms / 1e3) / 1e12, 1),
             "steps": args.steps, "warmup": args.warmup}
 
@@ -650,6 +691,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["h32", "reference"], default="h32")
+    ap.add_argument("--form", choices=list(FORMS), default="tc",
+                    help="operand form of the chain (default: tensor-core form)")
     ap.add_argument("--cpu-tokens", type=int, default=24)
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")

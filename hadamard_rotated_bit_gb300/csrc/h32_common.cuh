@@ -85,13 +85,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit` polls, or as soon as *abort is set by another role of the CTA.
 // Returns false when it gave up.
+// 1: back off with a short sleep once a wait has polled 64 times
+#ifndef H32_WAIT_SLEEP
+#define H32_WAIT_SLEEP 1
+#endif
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit,
                                                   volatile int *abort) {
     if (mbar_try_wait(bar, parity)) return true;
     for (uint64_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
+#if H32_WAIT_SLEEP
         if (i > 64) __nanosleep(64);
+#endif
     }
     return false;
 }

@@ -18,12 +18,27 @@
 //               tcgen05.mma straight from shared memory), the weight scales
 //               (128 rows x 4 blocks) and the token scales (4 blocks x tokens)
 //   warp 1      TMEM allocator and MMA issuer: one K=32 MMA per block into one
-//               of four TMEM buffers; a commit per two blocks
-//   warps 2..   epilogue: tcgen05.ld each block's S, fold the scales in with
-//               packed fp32 operations, store coalesced rows of y
-// The MMA and the epilogue hand off two blocks per synchronization (each
-// hand-off costs of the order of two hundred cycles on this chip, so it is
-// amortised over twice the work).  Every wait is bounded.
+//               of four 128-column TMEM slots; a commit per two blocks
+//   warps 2..   epilogue (16 warps, four per TMEM lane quarter, each a
+//               quarter of the tile's columns): tcgen05.ld each block's S, fold
+//               the scales in with packed fp32 operations, store rows of y
+// The MMA and the epilogue hand off two blocks per synchronization; measured
+// on GB300, one block per hand-off (four buffers) is slower, as every hand-off
+// puts all epilogue warps in step.  Every wait is bounded.
+
+// epilogue warps per TMEM lane quarter
+#ifndef H32_TC_EPI_PER_QUAD
+#define H32_TC_EPI_PER_QUAD 4
+#endif
+// 1: load a chunk of both blocks of a hand-off under one TMEM wait
+#ifndef H32_TC_DUAL
+#define H32_TC_DUAL 1
+#endif
+// poll without sleeping: the waits here are short and on the critical path
+#ifndef H32_WAIT_SLEEP
+#define H32_WAIT_SLEEP 0
+#endif
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -31,15 +46,6 @@
 
 #include "h32_common.cuh"
 #include "h32_epilogue.cuh"
-
-#ifndef H32_TC_EPI_PER_QUAD
-#define H32_TC_EPI_PER_QUAD 2
-#endif
-// 1: issue every TMEM load of a block before one wait (one exposed latency per
-// block instead of one per 16-column chunk)
-#ifndef H32_TC_LD_ALL
-#define H32_TC_LD_ALL 0
-#endif
 
 namespace h32 {
 namespace {
@@ -51,8 +57,12 @@ constexpr int kBNMax = 128;          // tokens per tile (MMA N)
 constexpr int kStages = 5;           // 128-element K stages in flight
 constexpr int kTileBytes = 16384;    // 128 rows x 128 bytes
 constexpr int kScaleBytes = 2048;    // 4 blocks x 128 fp32
-constexpr int kGroup = 2;            // blocks per MMA -> epilogue hand-off
-constexpr int kTmemCols = 512;       // 2 hand-off buffers x 2 blocks x 128 columns
+#ifndef H32_TC_GROUP
+#define H32_TC_GROUP 2
+#endif
+constexpr int kGroup = H32_TC_GROUP;       // blocks per MMA -> epilogue hand-off
+constexpr int kBufs = 4 / kGroup;          // hand-off buffers in TMEM (4 blocks of 128 columns)
+constexpr int kTmemCols = 512;       // kBufs hand-off buffers x kGroup blocks x 128 columns
 constexpr uint64_t kDrainPolls = 1ull << 22;
 
 template <int EPQ>
@@ -75,8 +85,8 @@ enum {
     kBarFull = 0,
     kBarEmpty = kBarFull + kStages,
     kBarSFull = kBarEmpty + kStages,
-    kBarSEmpty = kBarSFull + 2,
-    kBarDrain = kBarSEmpty + 2
+    kBarSEmpty = kBarSFull + kBufs,
+    kBarDrain = kBarSEmpty + kBufs
 };
 enum { kMiscTmem = 0, kMiscAbort = 1 };
 
@@ -151,7 +161,7 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
             mbar_init(&bars[kBarFull + i], 1);
             mbar_init(&bars[kBarEmpty + i], 1 + C::kEpiWarps);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kBufs; ++i) {
             mbar_init(&bars[kBarSFull + i], 1);
             mbar_init(&bars[kBarSEmpty + i], C::kEpiWarps);
         }
@@ -223,8 +233,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
                     const uint64_t da = smem_desc_sw128(smem_u32(s_a + s * kTileBytes));
                     const uint64_t db = smem_desc_sw128(smem_u32(s_b + s * kTileBytes));
                     for (int j0 = 0; j0 < 4; j0 += kGroup, ++kg) {
-                        const int gb = kg & 1;
-                        if (!mbar_wait_bounded(&bars[kBarSEmpty + gb], ((kg >> 1) & 1) ^ 1, lim,
+                        const int gb = kg % kBufs;
+                        if (!mbar_wait_bounded(&bars[kBarSEmpty + gb], ((kg / kBufs) & 1) ^ 1, lim,
                                                abort_flag)) {
                             set_abort(misc);
                             ok = false;
@@ -278,36 +288,42 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
                 const float dws[4] = {dw4.x, dw4.y, dw4.z, dw4.w};
 #pragma unroll
                 for (int j0 = 0; j0 < 4; j0 += kGroup, ++kg) {
-                    const int gb = kg & 1;
-                    if (!warp_wait(&bars[kBarSFull + gb], (kg >> 1) & 1, lim, abort_flag)) {
+                    const int gb = kg % kBufs;
+                    if (!warp_wait(&bars[kBarSFull + gb], (kg / kBufs) & 1, lim, abort_flag)) {
                         set_abort(misc);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-#pragma unroll
-                    for (int i = 0; i < kGroup; ++i) {
-                        const int j = j0 + i;
-                        const float dw = dws[j];
-                        const float *dxj = sb + j * a.bn + c0;
-                        const uint32_t tcol = tmem + lane_addr + (gb * kGroup + i) * 128 + c0;
-#if H32_TC_LD_ALL
-                        uint32_t vv[C::kMaxChunks][16];
-#pragma unroll
-                        for (int c = 0; c < C::kMaxChunks; ++c)
-                            if (c < nch) tmem_ld_x16(tcol + c * 16, vv[c]);
-                        tmem_ld_wait();
-#endif
+                    const uint32_t tcol0 = tmem + lane_addr + gb * kGroup * 128 + c0;
+                    if constexpr (!kSums && H32_TC_DUAL) {
+                        // each chunk of every block of the group under one TMEM wait;
+                        // every accumulator still takes the blocks in order
 #pragma unroll
                         for (int c = 0; c < C::kMaxChunks; ++c) {
                             if (c < nch) {
-#if H32_TC_LD_ALL
-                                uint32_t (&v)[16] = vv[c];
-#else
+                                uint32_t v[kGroup][16];
+#pragma unroll
+                                for (int i = 0; i < kGroup; ++i) tmem_ld_x16(tcol0 + i * 128 + c * 16, v[i]);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int i = 0; i < kGroup; ++i)
+                                    fold16(acc + 8 * c, dws[j0 + i], sb + (j0 + i) * a.bn + c0 + 16 * c, v[i]);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < kGroup && (kSums || !H32_TC_DUAL); ++i) {
+                        const int j = j0 + i;
+                        const float dw = dws[j];
+                        const float *dxj = sb + j * a.bn + c0;
+                        const uint32_t tcol = tcol0 + i * 128;
+#pragma unroll
+                        for (int c = 0; c < C::kMaxChunks; ++c) {
+                            if (c < nch) {
                                 uint32_t v[16];
                                 tmem_ld_x16(tcol + c * 16, v);
                                 tmem_ld_wait();
-#endif
                                 fold16(acc + 8 * c, dw, dxj + 16 * c, v);
                                 if constexpr (kSums) {
                                     const int n = ti.n0 + row;

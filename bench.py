@@ -549,15 +549,20 @@ def _events_time(torch, fn, steps, warmup, stream):
 
 
 def suite_chain_routes(torch, h32, dev, stream, steps, warmup):
-    """The pp512 chain on the exact 8-bit route and on the unrotated 4-bit route."""
+    """The pp512 chain on the exact 8-bit route (Q4_0-direct GEMM), on the unrotated
+    4-bit route (tensor-core form) and on the rotated 4-bit route with the Q4_0-direct
+    GEMM."""
     out = []
-    for route in ("q8_rotated", "q4_unrotated"):
+    for route in ("q8_rotated", "q4_unrotated", "q4_rotated_q4_0_direct"):
         rot = route != "q4_unrotated"
+        tc = route == "q4_unrotated"
         bufs = []
         for p in CHAIN:
             cid = wl.CFG_ATTN if p is wl.ATTN else wl.CFG_FFN
             wq, wd = h32.h32_rotate_quantize_weights_q4_0(
                 torch.from_numpy(p.weights(0, cid)).to(dev), rotate=rot)
+            if tc:
+                wq, wd = h32.h32_prepack_weights_q4_0_tc(wq, wd)
             x = torch.from_numpy(p.activations(M_TOKENS, 0, cid).view(np.int16)).view(
                 torch.bfloat16).to(dev)
             bufs.append((wq, wd, x, torch.empty((M_TOKENS, p.N), device=dev)))
@@ -567,6 +572,9 @@ def suite_chain_routes(torch, h32, dev, stream, steps, warmup):
                 if route.startswith("q8"):
                     xq, xd = h32.h32_quantize_act_q8(x, rotate=rot, stream=stream)
                     h32.q4_0_x_q8_gemm(wq, wd, xq, xd, y=y, stream=stream)
+                elif tc:
+                    xw, xdt = h32.h32_quantize_act_q4_tc(x, rotate=rot, stream=stream)
+                    h32.q4_0_x_q4_gemm_tc(wq, wd, xw, xdt, M=M_TOKENS, y=y, stream=stream)
                 else:
                     xq, xd = h32.h32_quantize_act_q4(x, rotate=rot, stream=stream)
                     h32.q4_0_x_q4_gemm(wq, wd, xq, xd, y=y, stream=stream)
@@ -627,7 +635,8 @@ def suite_long(torch, h32, dev, stream, steps, warmup):
     for p in projs:
         wq, wd = h32.h32_rotate_quantize_weights_q4_0(
             torch.from_numpy(p.weights(0, wl.CFG_LONG)).to(dev))
-        weights.append((wq, wd))
+        weights.append(h32.h32_prepack_weights_q4_0_tc(wq, wd))
+        del wq, wd
     mb = 1024
     for M in wl.LONG_MS:
         xs = [torch.from_numpy(p.activations(M, 0, wl.CFG_LONG).view(np.int16)).view(
@@ -636,9 +645,10 @@ def suite_long(torch, h32, dev, stream, steps, warmup):
 
         def step():
             for s0 in range(0, M, mb):
-                for (wq, wd), x, y in zip(weights, xs, ys):
-                    xq, xd = h32.h32_quantize_act_q4(x[s0:s0 + mb], stream=stream)
-                    h32.q4_0_x_q4_gemm(wq, wd, xq, xd, y=y[:min(mb, M - s0)], stream=stream)
+                m = min(mb, M - s0)
+                for (wp, wsc), x, y in zip(weights, xs, ys):
+                    xw, xdt = h32.h32_quantize_act_q4_tc(x[s0:s0 + m], stream=stream)
+                    h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=m, y=y[:m], stream=stream)
         ms = _events_time(torch, step, max(1, steps // max(1, M // 1024)), max(1, warmup // 4),
                           stream)
         out.append({"suite": f"long_prompt_{M}_tokens_1024_microbatches",

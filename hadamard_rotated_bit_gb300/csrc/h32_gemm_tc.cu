@@ -30,10 +30,6 @@
 #ifndef H32_TC_EPI_PER_QUAD
 #define H32_TC_EPI_PER_QUAD 4
 #endif
-// 1: load a chunk of both blocks of a hand-off under one TMEM wait
-#ifndef H32_TC_DUAL
-#define H32_TC_DUAL 1
-#endif
 // poll without sleeping: the waits here are short and on the critical path
 #ifndef H32_WAIT_SLEEP
 #define H32_WAIT_SLEEP 0
@@ -67,7 +63,6 @@ constexpr uint64_t kDrainPolls = 1ull << 22;
 
 template <int EPQ>
 struct TcCfg {
-    static constexpr int kEpiPerQuad = EPQ;
     static constexpr int kEpiWarps = 4 * EPQ;
     static constexpr int kThreads = (2 + kEpiWarps) * 32;
     static constexpr int kMaxChunks = (8 + EPQ - 1) / EPQ;  // 16-column chunks per warp
@@ -122,6 +117,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return d;
 }
 
+// one elected lane of the (converged) warp arrives on `bar`; no branch
+__device__ __forceinline__ void elect_arrive(uint64_t *bar) {
+    asm volatile(
+        "{\n.reg .pred p;\n.reg .b64 st;\nelect.sync _|p, 0xffffffff;\n"
+        "@p mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
 struct TcTile {
     int n0, g0, rows, ncols;
 };
@@ -134,6 +137,94 @@ __device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a) {
     ti.rows = min(a.bn, a.M - ti.g0);
     ti.ncols = (ti.rows + 15) & ~15;
     return ti;
+}
+
+// The epilogue of one warp over all of its tiles, without block sums: ring
+// positions of the shared-memory stages and TMEM buffers are carried as
+// counters and phase bits, arrivals come from one elected lane.  Returns false
+// when a wait gave up.
+template <int EPQ>
+__device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, uint64_t *bars, const float *s_sa,
+                                               const float *s_sb, uint32_t tmem, int warp, int lane,
+                                               volatile int *abort_flag) {
+    using C = TcCfg<EPQ>;
+    const int ew = warp - 2;
+    const int quad = warp & 3;                 // TMEM lanes 32 quad .. 32 quad + 31
+    const int part = ew >> 2;                  // share of the columns
+    const int row = quad * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    const int nst = a.nb / 4;
+    const uint64_t lim = a.wait_limit;
+    uint32_t s = 0, sph = 0, gb = 0, gph = 0;
+    for (int t = blockIdx.x; t < a.total; t += gridDim.x) {
+        const TcTile ti = tc_tile(t, a);
+        const int n16 = ti.ncols >> 4;
+        const int base = n16 / EPQ, rem = n16 % EPQ;
+        const int nch = base + (part < rem ? 1 : 0);
+        const int c0 = 16 * (part * base + min(part, rem));
+        const uint32_t tcol_base = tmem + lane_addr + c0;
+        uint64_t acc[8 * C::kMaxChunks];
+#pragma unroll
+        for (int i = 0; i < 8 * C::kMaxChunks; ++i) acc[i] = 0ull;
+        for (int st = 0; st < nst; ++st) {
+            if (!warp_wait(&bars[kBarFull + s], sph, lim, abort_flag)) return false;
+            const float4 dw4 = *reinterpret_cast<const float4 *>(s_sa + s * (kScaleBytes / 4) + 4 * row);
+            const float dws[4] = {dw4.x, dw4.y, dw4.z, dw4.w};
+            const float *sb = s_sb + s * (kScaleBytes / 4) + c0;   // [4 blocks][bn tokens]
+#pragma unroll
+            for (int j0 = 0; j0 < 4; j0 += kGroup) {
+                if (!warp_wait(&bars[kBarSFull + gb], gph, lim, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t tcol0 = tcol_base + gb * (kGroup * 128);
+                // each chunk of every block of the group under one TMEM wait;
+                // every accumulator still takes the blocks in order
+#pragma unroll
+                for (int c = 0; c < C::kMaxChunks; ++c) {
+                    if (c < nch) {
+                        uint32_t v[kGroup][16];
+#pragma unroll
+                        for (int i = 0; i < kGroup; ++i) tmem_ld_x16(tcol0 + i * 128 + c * 16, v[i]);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < kGroup; ++i)
+                            fold16(acc + 8 * c, dws[j0 + i], sb + (j0 + i) * a.bn + 16 * c, v[i]);
+                    }
+                }
+                // the warp-wide wait above: every lane's TMEM reads of the buffer are done
+                tc_fence_before();
+                elect_arrive(&bars[kBarSEmpty + gb]);
+                if (++gb == kBufs) {
+                    gb = 0;
+                    gph ^= 1;
+                }
+            }
+            __syncwarp();
+            elect_arrive(&bars[kBarEmpty + s]);
+            if (++s == kStages) {
+                s = 0;
+                sph ^= 1;
+            }
+        }
+        const int64_t n = ti.n0 + row;
+        if (n < a.N) {
+#pragma unroll
+            for (int c = 0; c < C::kMaxChunks; ++c) {
+                if (c < nch) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int col = c0 + c * 16 + 2 * q;
+                        const uint64_t pr = acc[8 * c + q];
+                        if (col < ti.rows)
+                            a.y[(ti.g0 + col) * a.ldy + n] = __uint_as_float(static_cast<uint32_t>(pr));
+                        if (col + 1 < ti.rows)
+                            a.y[(ti.g0 + col + 1) * a.ldy + n] =
+                                __uint_as_float(static_cast<uint32_t>(pr >> 32));
+                    }
+                }
+            }
+        }
+    }
+    return true;
 }
 
 template <int EPQ, bool kSums>
@@ -257,8 +348,11 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
             mma_commit(&bars[kBarDrain]);
             mbar_wait_bounded(&bars[kBarDrain], 0, kDrainPolls, nullptr);
         }
-    } else {
+    } else if constexpr (!kSums) {
         // ------------------------------------------------------- epilogue
+        if (!epilogue_tiles<EPQ>(a, bars, s_sa, s_sb, tmem, warp, lane, abort_flag)) set_abort(misc);
+    } else {
+        // ------------------------------------ epilogue with block sums
         const int ew = warp - 2;
         const int quad = warp & 3;                 // TMEM lanes 32*quad .. +31
         const int part = ew >> 2;                  // share of the columns
@@ -296,24 +390,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t tcol0 = tmem + lane_addr + gb * kGroup * 128 + c0;
-                    if constexpr (!kSums && H32_TC_DUAL) {
-                        // each chunk of every block of the group under one TMEM wait;
-                        // every accumulator still takes the blocks in order
 #pragma unroll
-                        for (int c = 0; c < C::kMaxChunks; ++c) {
-                            if (c < nch) {
-                                uint32_t v[kGroup][16];
-#pragma unroll
-                                for (int i = 0; i < kGroup; ++i) tmem_ld_x16(tcol0 + i * 128 + c * 16, v[i]);
-                                tmem_ld_wait();
-#pragma unroll
-                                for (int i = 0; i < kGroup; ++i)
-                                    fold16(acc + 8 * c, dws[j0 + i], sb + (j0 + i) * a.bn + c0 + 16 * c, v[i]);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < kGroup && (kSums || !H32_TC_DUAL); ++i) {
+                    for (int i = 0; i < kGroup; ++i) {
                         const int j = j0 + i;
                         const float dw = dws[j];
                         const float *dxj = sb + j * a.bn + c0;

@@ -621,10 +621,42 @@ def suite_moe(torch, h32, dev, stream, steps, warmup):
     times["down_ms"] = _events_time(torch, lambda: h32.q4_0_x_q4_gemm_experts(
         wq_dn, wd_dn, xq2, xd2, None, offs, R, y=y_dn, stream=stream), steps, warmup, stream)
     ops = 2 * R * (wq_gu.shape[1] * cfg.hidden + wq_dn.shape[1] * cfg.ffn)
-    return [{"suite": "moe_1024_tokens_top8_128_experts", "value": round(cfg.T / (ms / 1e3), 1),
-             "unit": UNIT, "ms_per_step": round(ms, 4),
-             "gemm_ms": {k: round(v, 4) for k, v in times.items()},
-             "gemm_eff_TOPS": round(ops / ((times["gate_up_ms"] + times["down_ms"]) / 1e3) / 1e12, 1)}]
+    out = [{"suite": "moe_1024_tokens_top8_128_experts_q4_0_direct",
+            "value": round(cfg.T / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "gemm_ms": {k: round(v, 4) for k, v in times.items()},
+            "gemm_eff_TOPS": round(ops / ((times["gate_up_ms"] + times["down_ms"]) / 1e3) / 1e12, 1)}]
+
+    # tensor-core form: repacked experts, the gate/up input quantized straight into
+    # grouped order (row gather), the down input already grouped
+    N_gu, N_dn = wq_gu.shape[1], wq_dn.shape[1]
+    wp_gu, ws_gu = h32.h32_prepack_weights_q4_0_tc(wq_gu.reshape(-1, wq_gu.shape[2]),
+                                                    wd_gu.reshape(-1, wd_gu.shape[2]))
+    wp_dn, ws_dn = h32.h32_prepack_weights_q4_0_tc(wq_dn.reshape(-1, wq_dn.shape[2]),
+                                                    wd_dn.reshape(-1, wd_dn.shape[2]))
+    xw_gu = torch.empty((R, cfg.hidden), dtype=torch.uint8, device=dev)
+    xt_gu = torch.zeros((cfg.hidden // 32, R), dtype=torch.float32, device=dev)
+    xw_dn = torch.empty((R, cfg.ffn), dtype=torch.uint8, device=dev)
+    xt_dn = torch.zeros((cfg.ffn // 32, R), dtype=torch.float32, device=dev)
+
+    def step_tc():
+        h32.h32_quantize_act_q4_tc_gather(xg, ridx, xw=xw_gu, xdt=xt_gu, stream=stream)
+        h32.q4_0_x_q4_gemm_tc_experts(wp_gu, ws_gu, xw_gu, xt_gu, offs, N_gu, R=R, y=y_gu,
+                                      stream=stream)
+        h32.h32_quantize_act_q4_tc(xn, xw=xw_dn, xdt=xt_dn, stream=stream)
+        h32.q4_0_x_q4_gemm_tc_experts(wp_dn, ws_dn, xw_dn, xt_dn, offs, N_dn, R=R, y=y_dn,
+                                      stream=stream)
+    ms = _events_time(torch, step_tc, steps, warmup, stream)
+    tt = {"gate_up_ms": _events_time(torch, lambda: h32.q4_0_x_q4_gemm_tc_experts(
+              wp_gu, ws_gu, xw_gu, xt_gu, offs, N_gu, R=R, y=y_gu, stream=stream), steps, warmup,
+              stream),
+          "down_ms": _events_time(torch, lambda: h32.q4_0_x_q4_gemm_tc_experts(
+              wp_dn, ws_dn, xw_dn, xt_dn, offs, N_dn, R=R, y=y_dn, stream=stream), steps, warmup,
+              stream)}
+    out.append({"suite": "moe_1024_tokens_top8_128_experts",
+                "value": round(cfg.T / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+                "operand_form": "tc", "gemm_ms": {k: round(v, 4) for k, v in tt.items()},
+                "gemm_eff_TOPS": round(ops / ((tt["gate_up_ms"] + tt["down_ms"]) / 1e3) / 1e12, 1)})
+    return out
 
 
 def suite_long(torch, h32, dev, stream, steps, warmup):

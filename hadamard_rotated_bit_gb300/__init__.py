@@ -22,7 +22,7 @@ __all__ = [
     "q4_0_x_q4_gemm", "q4_0_x_q8_gemm", "q4_0_x_q4_gemm_experts",
     "h32_device_status", "h32_status_string", "h32_set_wait_limit", "h32_version",
     "h32_last_cuda_error", "h32_quantize_act_q4_tc", "h32_prepack_weights_q4_0_tc",
-    "q4_0_x_q4_gemm_tc",
+    "q4_0_x_q4_gemm_tc", "h32_quantize_act_q4_tc_gather", "q4_0_x_q4_gemm_tc_experts",
 ]
 
 
@@ -55,6 +55,10 @@ _SIGS = {
     "h32_quantize_act_q4_tc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _I64, _INT, _P]),
     "h32_prepack_weights_q4_0_tc": (_INT, [_P, _P, _I64, _I64, _P, _P, _I64, _P]),
     "q4_0_x_q4_gemm_tc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P]),
+    "h32_quantize_act_q4_tc_gather": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _P, _I64,
+                                             _INT, _P]),
+    "q4_0_x_q4_gemm_tc_experts": (_INT, [_P, _P, _I64, ctypes.c_int32, _P, _P, _I64, _P, _I64, _I64,
+                                         _I64, _P, _I64, _P, _P]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -321,4 +325,59 @@ def q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=None, y=None, block_sums=None, stream=
     st = lib().q4_0_x_q4_gemm_tc(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt),
                                  xdt.shape[1], M, N, K, _ptr(y), ldy, _ptr(S), _stream(stream))
     _check("q4_0_x_q4_gemm_tc", st)
+    return (y, S) if S is not None else y
+
+
+def h32_quantize_act_q4_tc_gather(x, row_idx, rotate=True, xw=None, xdt=None, stream=None):
+    """x [T][K] bf16/fp32, row_idx [R] int32 -> (xw [R][K] uint8, xdt [K/32][ldxd] fp32):
+    output row r is the tc-form quantization of x[row_idx[r]]."""
+    torch = _torch()
+    _cuda(x, "x")
+    _cuda(row_idx, "row_idx")
+    if x.dtype == torch.bfloat16:
+        dt = H32_IN_BF16
+    elif x.dtype == torch.float32:
+        dt = H32_IN_F32
+    else:
+        raise ValueError("x must be bf16 or fp32")
+    if row_idx.dtype != torch.int32 or not row_idx.is_contiguous():
+        raise ValueError("row_idx must be a contiguous int32 tensor")
+    ldx = _rows(x, "x")
+    T, K = x.shape
+    R = row_idx.shape[0]
+    if xw is None:
+        xw = torch.empty((R, K), dtype=torch.uint8, device=x.device)
+    if xdt is None:
+        xdt = torch.zeros((K // 32, _round4(R)), dtype=torch.float32, device=x.device)
+    st = lib().h32_quantize_act_q4_tc_gather(_ptr(x), dt, T, K, ldx, _ptr(row_idx), R, _ptr(xw),
+                                             _ptr(xdt), xdt.shape[1], int(bool(rotate)),
+                                             _stream(stream))
+    _check("h32_quantize_act_q4_tc_gather", st)
+    return xw, xdt
+
+
+def q4_0_x_q4_gemm_tc_experts(wp, wsc, xw, xdt, expert_off, N, R=None, y=None, block_sums=None,
+                              stream=None):
+    """Expert-batched tc GEMM.  wp [E*N][K] uint8, wsc [E*N][ldws] fp32 (the experts'
+    repacked planes stacked), xw [R][K] / xdt [K/32][ldxd] in grouped order,
+    expert_off [E+1] int32 -> y [R][N] fp32 in grouped order."""
+    torch = _torch()
+    EN, K = wp.shape
+    if EN % N != 0:
+        raise ValueError("wp rows must be E * N")
+    E = EN // N
+    if R is None:
+        R = xw.shape[0]
+    if y is None:
+        y = torch.empty((R, N), dtype=torch.float32, device=wp.device)
+    ldy = _rows(y, "y") if R > 0 else N
+    S = None
+    if block_sums is True:
+        S = torch.empty((R, N, K // 32), dtype=torch.int32, device=wp.device)
+    elif block_sums is not None and block_sums is not False:
+        S = block_sums
+    st = lib().q4_0_x_q4_gemm_tc_experts(_ptr(wp), _ptr(wsc), wsc.shape[1], E, _ptr(xw), _ptr(xdt),
+                                         xdt.shape[1], _ptr(expert_off), R, N, K, _ptr(y), ldy,
+                                         _ptr(S), _stream(stream))
+    _check("q4_0_x_q4_gemm_tc_experts", st)
     return (y, S) if S is not None else y

@@ -60,6 +60,7 @@ constexpr int kGroup = H32_TC_GROUP;       // blocks per MMA -> epilogue hand-of
 constexpr int kBufs = 4 / kGroup;          // hand-off buffers in TMEM (4 blocks of 128 columns)
 constexpr int kTmemCols = 512;       // kBufs hand-off buffers x kGroup blocks x 128 columns
 constexpr uint64_t kDrainPolls = 1ull << 22;
+constexpr int kMaxExperts = 1024;
 
 template <int EPQ>
 struct TcCfg {
@@ -72,7 +73,8 @@ struct TcCfg {
     static constexpr int kOffSB = kOffSA + kStages * kScaleBytes;
     static constexpr int kOffBar = kOffSB + kStages * kScaleBytes;
     static constexpr int kOffMisc = kOffBar + 32 * 8;
-    static constexpr int kBytes = kOffMisc + 16 * 4;
+    static constexpr int kOffGrp = kOffMisc + 16 * 4;            // row offsets, tile prefix
+    static constexpr int kBytes = kOffGrp + 2 * (kMaxExperts + 1) * 4;
     static constexpr int kSmem = kBytes + 1024;
 };
 
@@ -83,13 +85,14 @@ enum {
     kBarSEmpty = kBarSFull + kBufs,
     kBarDrain = kBarSEmpty + kBufs
 };
-enum { kMiscTmem = 0, kMiscAbort = 1 };
+enum { kMiscTmem = 0, kMiscAbort = 1, kMiscBad = 2, kMiscTotal = 3 };
 
 struct TcArgs {
     float *y;
     int32_t *bsum;
+    const int32_t *expert_off;   // [E+1] row offsets of the expert groups, or null (dense)
     int64_t ldy;
-    int32_t M, N, nb, bn, chunks, total;
+    int32_t M, N, nb, bn, E;     // M: activation rows (all groups)
     uint64_t wait_limit;
 };
 
@@ -125,17 +128,44 @@ __device__ __forceinline__ void elect_arrive(uint64_t *bar) {
         : "memory");
 }
 
+// Tiles: per expert group e (one group of all rows when dense), every 128-row
+// weight tile times every chunk of up to bn token rows.  A group's chunks start
+// at its first row rounded down to a multiple of 4 (so the token-scale box
+// starts on a 16-byte boundary); the rows of the chunk outside the group are
+// computed but not stored.  Tiles are numbered group-major, then weight-tile
+// major (consecutive CTAs share a weight tile).
 struct TcTile {
-    int n0, g0, rows, ncols;
+    int n0;     // first weight row within the expert
+    int wrow;   // its row in the [E * N] weight planes
+    int g0;     // first token row of the chunk
+    int clo, chi;   // columns [clo, chi) of the chunk belong to the group
+    int ncols;  // MMA width: chi rounded up to 16
 };
 
-__device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a) {
+__device__ __forceinline__ int group_chunks(const int *s_off, int e, int bn) {
+    const int lo = s_off[e], hi = s_off[e + 1];
+    return hi > lo ? (hi - (lo & ~3) + bn - 1) / bn : 0;
+}
+
+__device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a, const int *s_off,
+                                          const int *s_tpre) {
+    int lo = 0, hi = a.E;   // the last group whose first tile is <= t
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_tpre[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    const int e = lo;
+    const int local = t - s_tpre[e];
+    const int chunks = group_chunks(s_off, e, a.bn);
+    const int wt = local / chunks, ch = local - wt * chunks;
     TcTile ti;
-    const int nt = t / a.chunks, ch = t - nt * a.chunks;
-    ti.n0 = nt * kBM;
-    ti.g0 = ch * a.bn;
-    ti.rows = min(a.bn, a.M - ti.g0);
-    ti.ncols = (ti.rows + 15) & ~15;
+    ti.n0 = wt * kBM;
+    ti.wrow = e * a.N + ti.n0;
+    ti.g0 = (s_off[e] & ~3) + ch * a.bn;
+    ti.clo = max(0, s_off[e] - ti.g0);
+    ti.chi = min(a.bn, s_off[e + 1] - ti.g0);
+    ti.ncols = (ti.chi + 15) & ~15;
     return ti;
 }
 
@@ -144,7 +174,8 @@ __device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a) {
 // counters and phase bits, arrivals come from one elected lane.  Returns false
 // when a wait gave up.
 template <int EPQ>
-__device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, uint64_t *bars, const float *s_sa,
+__device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const int *s_off,
+                                               const int *s_tpre, uint64_t *bars, const float *s_sa,
                                                const float *s_sb, uint32_t tmem, int warp, int lane,
                                                volatile int *abort_flag) {
     using C = TcCfg<EPQ>;
@@ -156,8 +187,8 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, uint64_t *bars, 
     const int nst = a.nb / 4;
     const uint64_t lim = a.wait_limit;
     uint32_t s = 0, sph = 0, gb = 0, gph = 0;
-    for (int t = blockIdx.x; t < a.total; t += gridDim.x) {
-        const TcTile ti = tc_tile(t, a);
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const TcTile ti = tc_tile(t, a, s_off, s_tpre);
         const int n16 = ti.ncols >> 4;
         const int base = n16 / EPQ, rem = n16 % EPQ;
         const int nch = base + (part < rem ? 1 : 0);
@@ -214,9 +245,9 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, uint64_t *bars, 
                     for (int q = 0; q < 8; ++q) {
                         const int col = c0 + c * 16 + 2 * q;
                         const uint64_t pr = acc[8 * c + q];
-                        if (col < ti.rows)
+                        if (col >= ti.clo && col < ti.chi)
                             a.y[(ti.g0 + col) * a.ldy + n] = __uint_as_float(static_cast<uint32_t>(pr));
-                        if (col + 1 < ti.rows)
+                        if (col + 1 >= ti.clo && col + 1 < ti.chi)
                             a.y[(ti.g0 + col + 1) * a.ldy + n] =
                                 __uint_as_float(static_cast<uint32_t>(pr >> 32));
                     }
@@ -241,11 +272,15 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
     float *s_sb = reinterpret_cast<float *>(smem + C::kOffSB);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
     volatile int *misc = reinterpret_cast<volatile int *>(smem + C::kOffMisc);
+    int *s_off = reinterpret_cast<int *>(smem + C::kOffGrp);
+    int *s_tpre = s_off + kMaxExperts + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nst = a.nb / 4;
     const uint64_t lim = a.wait_limit;
     const uint32_t stage_tx = kTileBytes + a.bn * 128 + kScaleBytes + a.bn * 16;
+    const int E = a.E;
+    const int nt = (a.N + kBM - 1) / kBM;
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -258,8 +293,57 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
         }
         mbar_init(&bars[kBarDrain], 1);
         misc[kMiscAbort] = 0;
+        misc[kMiscBad] = 0;
         fence_barrier_init();
     }
+    // group offsets: checked (0 = off[0] <= ... <= off[E] = M), then the tile
+    // prefix over the groups (warp 0)
+    if (a.expert_off == nullptr) {
+        if (tid == 0) {
+            s_off[0] = 0;
+            s_off[1] = a.M;
+        }
+    } else {
+        for (int i = tid; i <= E; i += C::kThreads) s_off[i] = a.expert_off[i];
+    }
+    __syncthreads();
+    for (int i = tid; i <= E; i += C::kThreads) {
+        const int v = s_off[i];
+        if ((i == 0 && v != 0) || (i == E && v != a.M) || (i < E && s_off[i + 1] < v))
+            misc[kMiscBad] = 1;
+    }
+    __syncthreads();
+    if (warp == 0 && !misc[kMiscBad]) {
+        const int per = (E + 31) / 32;
+        const int e0 = lane * per;
+        int sum = 0;
+        for (int i = 0; i < per; ++i)
+            if (e0 + i < E) sum += nt * group_chunks(s_off, e0 + i, a.bn);
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+        for (int i = 0; i < per; ++i) {
+            if (e0 + i < E) {
+                s_tpre[e0 + i] = run;
+                run += nt * group_chunks(s_off, e0 + i, a.bn);
+            }
+        }
+        if (lane == 31) {
+            s_tpre[E] = incl;
+            misc[kMiscTotal] = incl;
+        }
+    }
+    __syncthreads();
+    if (misc[kMiscBad]) {
+        if (tid == 0 && blockIdx.x == 0) record(kStatusGuard);
+        return;
+    }
+    const int total = misc[kMiscTotal];
+    if (static_cast<int>(blockIdx.x) >= total) return;
     if (warp == 1) {
         __syncwarp();
         tmem_alloc(reinterpret_cast<uint32_t *>(const_cast<int *>(&misc[kMiscTmem])), kTmemCols);
@@ -280,8 +364,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
             prefetch_tmap(&map_sb);
             uint32_t ks = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < a.total && ok; t += gridDim.x) {
-                const TcTile ti = tc_tile(t, a);
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TcTile ti = tc_tile(t, a, s_off, s_tpre);
                 for (int st = 0; st < nst; ++st, ++ks) {
                     const int s = ks % kStages;
                     if (!mbar_wait_bounded(&bars[kBarEmpty + s], ((ks / kStages) & 1) ^ 1, lim,
@@ -291,10 +375,10 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&bars[kBarFull + s], stage_tx);
-                    tma_load_2d(s_a + s * kTileBytes, &map_a, &bars[kBarFull + s], st * 128, ti.n0);
+                    tma_load_2d(s_a + s * kTileBytes, &map_a, &bars[kBarFull + s], st * 128, ti.wrow);
                     tma_load_2d(s_b + s * kTileBytes, &map_b, &bars[kBarFull + s], st * 128, ti.g0);
                     tma_load_2d(s_sa + s * (kScaleBytes / 4), &map_sa, &bars[kBarFull + s], st * 4,
-                                ti.n0);
+                                ti.wrow);
                     tma_load_2d(s_sb + s * (kScaleBytes / 4), &map_sb, &bars[kBarFull + s], ti.g0,
                                 st * 4);
                 }
@@ -310,8 +394,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
         if (lane == 0) {
             uint32_t ks = 0, kg = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < a.total && ok; t += gridDim.x) {
-                const TcTile ti = tc_tile(t, a);
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TcTile ti = tc_tile(t, a, s_off, s_tpre);
                 const uint32_t idesc = idesc_e4m3_f32(kBM, ti.ncols);
                 for (int st = 0; st < nst && ok; ++st, ++ks) {
                     const int s = ks % kStages;
@@ -350,7 +434,9 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
         }
     } else if constexpr (!kSums) {
         // ------------------------------------------------------- epilogue
-        if (!epilogue_tiles<EPQ>(a, bars, s_sa, s_sb, tmem, warp, lane, abort_flag)) set_abort(misc);
+        if (!epilogue_tiles<EPQ>(a, total, s_off, s_tpre, bars, s_sa, s_sb, tmem, warp, lane,
+                                 abort_flag))
+            set_abort(misc);
     } else {
         // ------------------------------------ epilogue with block sums
         const int ew = warp - 2;
@@ -360,8 +446,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         uint32_t ks = 0, kg = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < a.total && ok; t += gridDim.x) {
-            const TcTile ti = tc_tile(t, a);
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const TcTile ti = tc_tile(t, a, s_off, s_tpre);
             const int n16 = ti.ncols >> 4;
             const int base = n16 / EPQ, rem = n16 % EPQ;
             const int nch = base + (part < rem ? 1 : 0);
@@ -409,11 +495,10 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
                                     const int64_t step = static_cast<int64_t>(a.N) * a.nb;
                                     int32_t *bp = a.bsum + (ti.g0 + col0) * step +
                                                   static_cast<int64_t>(n) * a.nb + st * 4 + j;
-                                    const int lim_q = min(16, ti.rows - col0);
                                     if (n < a.N) {
 #pragma unroll
                                         for (int q = 0; q < 16; ++q)
-                                            if (q < lim_q)
+                                            if (col0 + q >= ti.clo && col0 + q < ti.chi)
                                                 bp[q * step] =
                                                     __float2int_rn(__uint_as_float(v[q]));
                                     }
@@ -439,10 +524,10 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
                         for (int q = 0; q < 8; ++q) {
                             const int col = c0 + c * 16 + 2 * q;
                             const uint64_t pr = acc[8 * c + q];
-                            if (col < ti.rows)
+                            if (col >= ti.clo && col < ti.chi)
                                 a.y[(ti.g0 + col) * a.ldy + n] =
                                     __uint_as_float(static_cast<uint32_t>(pr));
-                            if (col + 1 < ti.rows)
+                            if (col + 1 >= ti.clo && col + 1 < ti.chi)
                                 a.y[(ti.g0 + col + 1) * a.ldy + n] =
                                     __uint_as_float(static_cast<uint32_t>(pr >> 32));
                         }
@@ -558,45 +643,76 @@ h32_status tc_read_and_clear_status(cudaStream_t s) {
 
 }  // namespace h32
 
-extern "C" h32_status q4_0_x_q4_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws,
-                                        const uint8_t *xw, const float *xdt, int64_t ldxd,
-                                        int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
-                                        int32_t *block_sums, void *stream) {
-    using namespace h32;
+namespace h32 {
+namespace {
+
+// Shared by the dense and the expert-batched entry points: checks, tensor
+// maps, launch.  E groups of weight rows [E * N][K]; expert_off null = dense.
+h32_status run_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws, int64_t E,
+                       const uint8_t *xw, const float *xdt, int64_t ldxd,
+                       const int32_t *expert_off, int64_t M, int64_t N, int64_t K, float *y,
+                       int64_t ldy, int32_t *block_sums, void *stream) {
     if (M < 0 || N <= 0 || K <= 0 || (K % 128) != 0 || (N % 16) != 0 || ldy < N ||
-        ldws < K / 32 || (ldws % 4) != 0 || ldxd < M || (ldxd % 4) != 0)
+        ldws < K / 32 || (ldws % 4) != 0 || ldxd < M || (ldxd % 4) != 0 || E < 1 ||
+        E > kMaxExperts)
         return H32_ERR_INVALID_ARG;
     if (M == 0) return H32_OK;
     if (!wp || !wsc || !xw || !xdt || !y) return H32_ERR_INVALID_ARG;
     if (!aligned16(wp) || !aligned16(wsc) || !aligned16(xw) || !aligned16(xdt) || !aligned16(y) ||
-        (block_sums && !aligned16(block_sums)) || (ldy % 4) != 0)
+        (block_sums && !aligned16(block_sums)) || (expert_off && !aligned16(expert_off)) ||
+        (ldy % 4) != 0)
         return H32_ERR_ALIGNMENT;
-    if (M > 0x7FFFFFFFll || N > 0x7FFFFFFFll || K > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
+    if (M > 0x7FFFFFFFll || E * N > 0x7FFFFFFFll || K > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
     int sms = 0;
     H32_TRY(check_device(&sms));
-    const int bn = choose_bn_tc(M, N, sms);
+    // dense: the tile width from the schedule simulation; groups: full 128-row chunks
+    const int bn = expert_off ? kBNMax : choose_bn_tc(M, N, sms);
+    int64_t grid = sms;
+    if (!expert_off) {
+        const int64_t total = ((N + kBM - 1) / kBM) * ((M + bn - 1) / bn);
+        if (total > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
+        grid = total < sms ? total : sms;
+    }
     CUtensorMap maps[4];
-    H32_TRY(make_map(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wp, K, N, K, 128, kBM, true));
+    H32_TRY(make_map(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wp, K, E * N, K, 128, kBM, true));
     H32_TRY(make_map(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xw, K, M, K, 128, bn, true));
-    H32_TRY(make_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, wsc, ldws, N, ldws * 4, 4, kBM,
-                     false));
+    H32_TRY(make_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, wsc, ldws, E * N, ldws * 4, 4,
+                     kBM, false));
     H32_TRY(make_map(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, xdt, ldxd, K / 32, ldxd * 4, bn, 4,
                      false));
     TcArgs a{};
     a.y = y;
     a.bsum = block_sums;
+    a.expert_off = expert_off;
     a.ldy = ldy;
     a.M = static_cast<int32_t>(M);
     a.N = static_cast<int32_t>(N);
     a.nb = static_cast<int32_t>(K / 32);
     a.bn = bn;
-    a.chunks = static_cast<int32_t>((M + bn - 1) / bn);
-    const int64_t total = ((N + kBM - 1) / kBM) * a.chunks;
-    if (total > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
-    a.total = static_cast<int32_t>(total);
+    a.E = static_cast<int32_t>(E);
     a.wait_limit = wait_limit();
-    const int grid = static_cast<int>(total < sms ? total : sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return block_sums ? launch_tc<H32_TC_EPI_PER_QUAD, true>(maps, a, grid, s)
-                      : launch_tc<H32_TC_EPI_PER_QUAD, false>(maps, a, grid, s);
+    return block_sums ? launch_tc<H32_TC_EPI_PER_QUAD, true>(maps, a, static_cast<int>(grid), s)
+                      : launch_tc<H32_TC_EPI_PER_QUAD, false>(maps, a, static_cast<int>(grid), s);
+}
+
+}  // namespace
+}  // namespace h32
+
+extern "C" h32_status q4_0_x_q4_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                        const uint8_t *xw, const float *xdt, int64_t ldxd,
+                                        int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
+                                        int32_t *block_sums, void *stream) {
+    return h32::run_gemm_tc(wp, wsc, ldws, 1, xw, xdt, ldxd, nullptr, M, N, K, y, ldy, block_sums,
+                            stream);
+}
+
+extern "C" h32_status q4_0_x_q4_gemm_tc_experts(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                                int32_t E, const uint8_t *xw, const float *xdt,
+                                                int64_t ldxd, const int32_t *expert_off, int64_t R,
+                                                int64_t N, int64_t K, float *y, int64_t ldy,
+                                                int32_t *block_sums, void *stream) {
+    if (!expert_off) return H32_ERR_INVALID_ARG;
+    return h32::run_gemm_tc(wp, wsc, ldws, E, xw, xdt, ldxd, expert_off, R, N, K, y, ldy,
+                            block_sums, stream);
 }

@@ -30,6 +30,8 @@
 namespace h32 {
 namespace {
 
+__device__ uint32_t g_quant_status;   // kStatusGuard: a gathered row index out of range
+
 // fp32 nearest to 1/sqrt(32) (bit pattern 0x3E3504F3)
 constexpr float kInvSqrt32 = 0x1.6a09e6p-3f;
 // 1.5 * 2^23: adding it to |t| < 2^22 leaves round-half-even(t) in the low
@@ -247,11 +249,14 @@ __device__ __forceinline__ uint32_t tc_bytes(uint32_t c) {
 // Rotate + quantize to 4-bit codes in tc form.  Threads walk the blocks in
 // block-major order (g = b * M + row) so that the transposed scale stores of a
 // warp are contiguous; each lane still reads a whole 64-byte (or 128-byte)
-// block row segment and writes a whole 32-byte code segment.
-template <bool kBf16, bool kRotate>
+// block row segment and writes a whole 32-byte code segment.  With kGather,
+// output row r is the quantized input row row_idx[r] (an index outside
+// [0, T) records kStatusGuard and yields zero codes and a zero scale).
+template <bool kBf16, bool kRotate, bool kGather>
 __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restrict__ x, uint32_t nblk,
                                                           uint32_t M, uint32_t K, int64_t ldx,
-                                                          uint8_t *__restrict__ xw,
+                                                          const int32_t *__restrict__ row_idx,
+                                                          int64_t T, uint8_t *__restrict__ xw,
                                                           float *__restrict__ xdt, int64_t ldxd) {
     const uint32_t stride = gridDim.x * blockDim.x;
     const uint32_t sb = stride / M, srow = stride % M;
@@ -259,10 +264,26 @@ __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restric
     uint32_t b = g / M, row = g % M;
     for (; g < nblk; g += stride) {
         float v[32];
+        int64_t src = row;
+        bool valid = true;
+        if constexpr (kGather) {
+            src = __ldg(row_idx + row);
+            valid = src >= 0 && src < T;
+            if (!valid) {
+                atomicOr(&g_quant_status, kStatusGuard);
+                src = 0;
+            }
+        }
         if constexpr (kBf16) {
-            load_block_bf16(reinterpret_cast<const uint16_t *>(x) + int64_t(row) * ldx + 32 * b, v);
+            load_block_bf16(reinterpret_cast<const uint16_t *>(x) + src * ldx + 32 * b, v);
         } else {
-            load_block_f32(reinterpret_cast<const float *>(x) + int64_t(row) * ldx + 32 * b, v);
+            load_block_f32(reinterpret_cast<const float *>(x) + src * ldx + 32 * b, v);
+        }
+        if constexpr (kGather) {
+            if (!valid) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+            }
         }
         if constexpr (kRotate) rotate32(v);
         float amax = 0.0f;
@@ -375,7 +396,17 @@ h32_status quantize_act(const void *x, h32_in_dtype dt, int64_t M, int64_t K, in
 
 }  // namespace
 
-h32_status quant_read_and_clear_status(cudaStream_t) { return H32_OK; }
+h32_status quant_read_and_clear_status(cudaStream_t s) {
+    uint32_t v = 0;
+    const uint32_t z = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_quant_status, 4, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return H32_ERR_CUDA;
+    if (cudaMemcpyToSymbolAsync(g_quant_status, &z, 4, 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return H32_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return H32_ERR_CUDA;
+    if (v & kStatusGuard) return H32_ERR_DEVICE_GUARD;
+    return H32_OK;
+}
 
 namespace {
 int grid_for_tc(uint32_t nblk, int sm_count) { return grid_for(nblk, sm_count); }
@@ -414,17 +445,19 @@ extern "C" h32_status h32_rotate_quantize_weights_q4_0(const float *w, int64_t N
     return launch_status(cudaGetLastError());
 }
 
-extern "C" h32_status h32_quantize_act_q4_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
-                                             int64_t ldx, uint8_t *xw, float *xdt, int64_t ldxd,
-                                             int rotate, void *stream) {
-    using namespace h32;
-    if (M < 0 || K <= 0 || (K % 32) != 0 || ldx < K || ldxd < M || (ldxd % 4) != 0)
+namespace h32 {
+namespace {
+h32_status quantize_act_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K, int64_t ldx,
+                           const int32_t *row_idx, int64_t T, uint8_t *xw, float *xdt,
+                           int64_t ldxd, int rotate, void *stream) {
+    if (M < 0 || K <= 0 || (K % 32) != 0 || ldx < K || ldxd < M || (ldxd % 4) != 0 || T < 0)
         return H32_ERR_INVALID_ARG;
     if (dt != H32_IN_F32 && dt != H32_IN_BF16) return H32_ERR_INVALID_ARG;
     if (M == 0) return H32_OK;
-    if (!x || !xw || !xdt) return H32_ERR_INVALID_ARG;
+    if (!x || !xw || !xdt || (row_idx && T == 0)) return H32_ERR_INVALID_ARG;
     const int64_t esize = (dt == H32_IN_BF16) ? 2 : 4;
-    if (!aligned16(x) || !aligned16(xw) || !aligned16(xdt) || ((ldx * esize) % 16) != 0)
+    if (!aligned16(x) || !aligned16(xw) || !aligned16(xdt) || ((ldx * esize) % 16) != 0 ||
+        (row_idx && !aligned16(row_idx)))
         return H32_ERR_ALIGNMENT;
     if (M * (K / 32) > 0x7FFFFFFFll || M > 0x7FFFFFFFll || K > 0x7FFFFFFFll)
         return H32_ERR_INVALID_ARG;
@@ -434,14 +467,36 @@ extern "C" h32_status h32_quantize_act_q4_tc(const void *x, h32_in_dtype dt, int
     const int grid = grid_for_tc(nblk, sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint32_t m32 = static_cast<uint32_t>(M), k32 = static_cast<uint32_t>(K);
-    if (dt == H32_IN_BF16) {
-        if (rotate) quant_act_tc_kernel<true, true><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, xw, xdt, ldxd);
-        else quant_act_tc_kernel<true, false><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, xw, xdt, ldxd);
-    } else {
-        if (rotate) quant_act_tc_kernel<false, true><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, xw, xdt, ldxd);
-        else quant_act_tc_kernel<false, false><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, xw, xdt, ldxd);
-    }
+#define H32_QTC(BF, ROT, GA)                                                                     \
+    quant_act_tc_kernel<BF, ROT, GA><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, row_idx, T, xw, \
+                                                          xdt, ldxd)
+    const bool bf = dt == H32_IN_BF16, rot = rotate != 0, ga = row_idx != nullptr;
+    if (bf && rot && ga) H32_QTC(true, true, true);
+    else if (bf && rot) H32_QTC(true, true, false);
+    else if (bf && ga) H32_QTC(true, false, true);
+    else if (bf) H32_QTC(true, false, false);
+    else if (rot && ga) H32_QTC(false, true, true);
+    else if (rot) H32_QTC(false, true, false);
+    else if (ga) H32_QTC(false, false, true);
+    else H32_QTC(false, false, false);
+#undef H32_QTC
     return launch_status(cudaGetLastError());
+}
+}  // namespace
+}  // namespace h32
+
+extern "C" h32_status h32_quantize_act_q4_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
+                                             int64_t ldx, uint8_t *xw, float *xdt, int64_t ldxd,
+                                             int rotate, void *stream) {
+    return h32::quantize_act_tc(x, dt, M, K, ldx, nullptr, M, xw, xdt, ldxd, rotate, stream);
+}
+
+extern "C" h32_status h32_quantize_act_q4_tc_gather(const void *x, h32_in_dtype dt, int64_t T,
+                                                    int64_t K, int64_t ldx, const int32_t *row_idx,
+                                                    int64_t R, uint8_t *xw, float *xdt,
+                                                    int64_t ldxd, int rotate, void *stream) {
+    if (!row_idx) return H32_ERR_INVALID_ARG;
+    return h32::quantize_act_tc(x, dt, R, K, ldx, row_idx, T, xw, xdt, ldxd, rotate, stream);
 }
 
 extern "C" h32_status h32_prepack_weights_q4_0_tc(const uint8_t *wq, const uint16_t *wd, int64_t N,

@@ -169,6 +169,21 @@ h32_status h32_quantize_act_q4_tc(const void *x, h32_in_dtype dt, int64_t M, int
                                   void *stream);
 
 /*
+ * The same with a row gather, for expert-batched products ("Where the engine is
+ * going: HRX and the NPU", section "4-bit activations reach the MoE experts"):
+ * output row r is input row row_idx[r] of x[T][ldx], so the rows come out in the
+ * experts' grouped order, ready for q4_0_x_q4_gemm_tc_experts.
+ *   row_idx  [R] int32 device, each in [0, T); an index outside records
+ *            H32_ERR_DEVICE_GUARD (see h32_device_status) and its row gets zero
+ *            codes and a zero scale
+ *   xw       [R][K] out; xdt [K/32][ldxd] out, ldxd >= R, a multiple of 4
+ */
+h32_status h32_quantize_act_q4_tc_gather(const void *x, h32_in_dtype dt, int64_t T, int64_t K,
+                                         int64_t ldx, const int32_t *row_idx, int64_t R,
+                                         uint8_t *xw, float *xdt, int64_t ldxd, int rotate,
+                                         void *stream);
+
+/*
  * Repack Q4_0 weights (as written by h32_rotate_quantize_weights_q4_0) into
  * tc form, once, offline:
  *   wp     [N][K] out: one byte per weight, the e4m3 encoding of q - 8, element order
@@ -193,6 +208,24 @@ h32_status q4_0_x_q4_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws,
                              const uint8_t *xw, const float *xdt, int64_t ldxd, int64_t M,
                              int64_t N, int64_t K, float *y, int64_t ldy, int32_t *block_sums,
                              void *stream);
+
+/*
+ * Expert-batched W4A4 product on tc-form operands (the tc counterpart of
+ * q4_0_x_q4_gemm_experts): rows r in [expert_off[e], expert_off[e+1]) of
+ * xw/xdt (already in grouped order, e.g. from h32_quantize_act_q4_tc_gather)
+ * are multiplied by expert e's weights:
+ *   y[r][n] = same definition as q4_0_x_q4_gemm_tc with the weights of expert e
+ *   wp     [E][N][K] bytes, wsc [E][N][ldws] fp32 (h32_prepack_weights_q4_0_tc of
+ *          the E experts' planes stacked as E * N rows)
+ *   expert_off [E+1] int32 device: 0 = off[0] <= off[1] <= ... <= off[E] = R,
+ *          else H32_ERR_DEVICE_GUARD is recorded and nothing is computed
+ *   y      [R][ldy] fp32 out in grouped order; block_sums nullable int32 [R][N][K/32]
+ * Requires 1 <= E <= 1024, K % 128 == 0 and N % 16 == 0.
+ */
+h32_status q4_0_x_q4_gemm_tc_experts(const uint8_t *wp, const float *wsc, int64_t ldws, int32_t E,
+                                     const uint8_t *xw, const float *xdt, int64_t ldxd,
+                                     const int32_t *expert_off, int64_t R, int64_t N, int64_t K,
+                                     float *y, int64_t ldy, int32_t *block_sums, void *stream);
 
 /*
  * Synchronize `stream`, then report and clear the device status word of every

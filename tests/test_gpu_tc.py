@@ -172,3 +172,121 @@ def test_gemm_tc_pp512_sampled(h32, proj):
     ni = np.concatenate([r.integers(0, p.N, 3000), [p.N - 1, 0]])
     r32, _, _ = oracle.gemm_sampled(wq, wd, xq, xd, p.K, mi, ni)
     assert np.array_equal(y[mi, ni].view(np.uint32), r32.view(np.uint32))
+
+
+# --------------------------------------------------------------------------
+# expert-batched products in tc form ("Where the engine is going: HRX and the
+# NPU", section "4-bit activations reach the MoE experts")
+# --------------------------------------------------------------------------
+def test_quantize_tc_gather_matches_oracle(h32):
+    import torch
+    T, K, R = 37, 256, 101
+    x = wl.f32_to_bf16_bits(wl.act_normal_outliers(T, K, 0.01, 20.0, 0, wl.CFG_TEST, 240))
+    ridx = np.random.default_rng(7).integers(0, T, R).astype(np.int32)
+    xw, xdt = h32.h32_quantize_act_q4_tc_gather(torch_bf16(x), torch_of(ridx))
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    rq, rd = oracle.quantize_act_q4(x[ridx])
+    assert np.array_equal(e4m3_value(np_of(xw)), oracle.decode_act4(rq, K).astype(np.float64))
+    assert np.array_equal(np_of(xdt)[:, :R].T.view(np.uint32), rd.view(np.uint32))
+
+
+def test_quantize_tc_gather_index_guard(h32):
+    import torch
+    x = torch.ones((4, 64), dtype=torch.float32, device="cuda")
+    ridx = torch.tensor([0, 9, 3, -1], dtype=torch.int32, device="cuda")
+    xw, xdt = h32.h32_quantize_act_q4_tc_gather(x, ridx)
+    assert h32.h32_device_status() == h32.H32_ERR_DEVICE_GUARD
+    xw, xdt = np_of(xw), np_of(xdt)
+    assert np.all(xw[[1, 3]] == 0) and np.all(xdt[:, [1, 3]] == 0)
+    assert np.all(xdt[:, [0, 2]] > 0)
+    assert h32.h32_device_status() == 0
+
+
+def _tc_experts(h32, x, w, E, N, ridx, off, block_sums=True):
+    """oracle operands + the tc path: gather-quantize (or plain), repack, experts GEMM."""
+    import torch
+    K = x.shape[1]
+    wq, wd = oracle.quantize_weights_q4_0(w)
+    xq, xd = oracle.quantize_act_q4(x)
+    wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(wq), torch_of(wd.view(np.int16)))
+    xt = torch_bf16(x) if x.dtype == np.uint16 else torch_of(x)
+    if ridx is None:
+        xw, xdt = h32.h32_quantize_act_q4_tc(xt)
+    else:
+        xw, xdt = h32.h32_quantize_act_q4_tc_gather(xt, torch_of(ridx))
+    out = h32.q4_0_x_q4_gemm_tc_experts(wp, wsc, xw, xdt, torch_of(off), N, R=int(off[-1]),
+                                        block_sums=block_sums)
+    torch.cuda.synchronize()
+    st = h32.h32_device_status()
+    if block_sums:
+        y, S = out
+        return (wq.reshape(E, N, K // 2), wd.reshape(E, N, K // 32), xq, xd), np_of(y), np_of(S), st
+    return (wq.reshape(E, N, K // 2), wd.reshape(E, N, K // 32), xq, xd), np_of(out), None, st
+
+
+def test_tc_experts_small_all_outputs(h32):
+    """Ragged groups (empty ones, a 1-row one, one longer than a tile), rows
+    gathered by index, group starts not multiples of 4."""
+    E, N, K, T = 6, 48, 256, 30
+    counts = np.array([3, 0, 140, 1, 17, 0])
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    R = int(off[-1])
+    ridx = np.random.default_rng(5).integers(0, T, R).astype(np.int32)
+    x = wl.act_normal_outliers(T, K, 0.02, 25.0, 0, wl.CFG_TEST, 250)
+    w = wl.weights_normal(E * N, K, 0.02, 0, wl.CFG_TEST, 251)
+    (wq, wd, xq, xd), y, S, st = _tc_experts(h32, x, w, E, N, ridx, off)
+    assert st == 0
+    ri = np.repeat(np.arange(R), N)
+    ni = np.tile(np.arange(N), R)
+    r32, _, rS = oracle.gemm_experts_sampled(wq, wd, xq, xd, ridx, off, N, K, ri, ni, True)
+    assert np.array_equal(S.reshape(R * N, -1).astype(np.int64), rS)
+    assert np.array_equal(y.reshape(-1).view(np.uint32), r32.view(np.uint32))
+
+
+def test_tc_experts_identity_rows(h32):
+    E, N, K = 3, 32, 128
+    off = np.array([0, 5, 5, 21], np.int32)
+    x = wl.act_normal_outliers(21, K, 0.0, 1.0, 0, wl.CFG_TEST, 260)
+    w = wl.weights_normal(E * N, K, 0.02, 0, wl.CFG_TEST, 261)
+    (wq, wd, xq, xd), y, _, st = _tc_experts(h32, x, w, E, N, None, off, block_sums=False)
+    assert st == 0
+    ri = np.repeat(np.arange(21), N)
+    ni = np.tile(np.arange(N), 21)
+    r32, _, _ = oracle.gemm_experts_sampled(wq, wd, xq, xd, None, off, N, K, ri, ni)
+    assert np.array_equal(y.reshape(-1).view(np.uint32), r32.view(np.uint32))
+
+
+def test_tc_experts_bad_offsets_guarded(h32):
+    import torch
+    E, N, K = 2, 16, 128
+    wp = torch.zeros((E * N, K), dtype=torch.uint8, device="cuda")
+    wsc = torch.zeros((E * N, 4), dtype=torch.float32, device="cuda")
+    xw = torch.zeros((8, K), dtype=torch.uint8, device="cuda")
+    xdt = torch.zeros((K // 32, 8), dtype=torch.float32, device="cuda")
+    off = torch.tensor([0, 6, 4], dtype=torch.int32, device="cuda")
+    y = torch.full((4, N), 3.0, dtype=torch.float32, device="cuda")
+    h32.q4_0_x_q4_gemm_tc_experts(wp, wsc, xw, xdt, off, N, R=4, y=y)
+    assert h32.h32_device_status() == h32.H32_ERR_DEVICE_GUARD
+    assert torch.all(y == 3.0)
+    assert h32.h32_device_status() == 0
+
+
+def test_tc_moe_config_sampled(h32):
+    """1024-token micro-batch, 128 experts, top-8 routing: gate/up (rows gathered)
+    and down (rows already grouped)."""
+    cfg = wl.MOE
+    row_idx, off, _ = wl.moe_routing(cfg)
+    x_gu, x_dn = wl.moe_inputs(cfg)
+    w_gu, w_dn = wl.moe_weights(cfg)
+    r = np.random.default_rng(3)
+    for x, w, ridx in ((x_gu, w_gu, row_idx), (x_dn, w_dn, None)):
+        E, N, K = w.shape
+        (wq, wd, xq, xd), y, _, st = _tc_experts(h32, x, w.reshape(E * N, K), E, N, ridx, off,
+                                                  block_sums=False)
+        assert st == 0
+        R = int(off[-1])
+        ri = np.concatenate([r.integers(0, R, 3000), off[1:-1].astype(np.int64), [R - 1]])
+        ni = r.integers(0, N, ri.size)
+        r32, _, _ = oracle.gemm_experts_sampled(wq, wd, xq, xd, ridx, off, N, K, ri, ni)
+        assert np.array_equal(y[ri, ni].view(np.uint32), r32.view(np.uint32))

@@ -89,3 +89,35 @@ def test_no_device_is_reported_not_hidden(lib):
     p = ctypes.c_void_p(256)
     s = ctypes.c_void_p(0)
     assert _call("h32_quantize_act_q4", p, 1, 4, 64, 64, p, p, 1, s) == h32.H32_ERR_UNSUPPORTED
+
+
+def test_tc_form_bad_arguments(lib):
+    p = ctypes.c_void_p(256)
+    bad = ctypes.c_void_p(260)
+    s = ctypes.c_void_p(0)
+    # quantizer: ldxd < M, ldxd not a multiple of 4
+    assert _call("h32_quantize_act_q4_tc", p, 1, 8, 64, 64, p, p, 4, 1, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_quantize_act_q4_tc", p, 1, 8, 64, 64, p, p, 10, 1, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_quantize_act_q4_tc", p, 1, 8, 64, 64, bad, p, 8, 1, s) == h32.H32_ERR_ALIGNMENT
+    # gather: null index, misaligned index
+    assert _call("h32_quantize_act_q4_tc_gather", p, 1, 4, 64, 64, None, 8, p, p, 8, 1,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_quantize_act_q4_tc_gather", p, 1, 4, 64, 64, bad, 8, p, p, 8, 1,
+                 s) == h32.H32_ERR_ALIGNMENT
+    # repack: ldws < K/32
+    assert _call("h32_prepack_weights_q4_0_tc", p, p, 16, 256, p, p, 4, s) == h32.H32_ERR_INVALID_ARG
+    # GEMM: K % 128, N % 16, ldxd < M
+    assert _call("q4_0_x_q4_gemm_tc", p, p, 4, p, p, 8, 8, 16, 96, p, 16, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc", p, p, 4, p, p, 8, 8, 24, 128, p, 24, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc", p, p, 4, p, p, 4, 8, 16, 128, p, 16, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    # experts: E out of range, null offsets
+    assert _call("q4_0_x_q4_gemm_tc_experts", p, p, 4, 0, p, p, 8, p, 8, 16, 128, p, 16, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc_experts", p, p, 4, 1025, p, p, 8, p, 8, 16, 128, p, 16, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc_experts", p, p, 4, 2, p, p, 8, None, 8, 16, 128, p, 16, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc", p, p, 4, p, p, 8, 0, 16, 128, p, 16, None, s) == h32.H32_OK

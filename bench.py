@@ -549,13 +549,14 @@ def _events_time(torch, fn, steps, warmup, stream):
 
 
 def suite_chain_routes(torch, h32, dev, stream, steps, warmup):
-    """The pp512 chain on the exact 8-bit route (Q4_0-direct GEMM), on the unrotated
-    4-bit route (tensor-core form) and on the rotated 4-bit route with the Q4_0-direct
-    GEMM."""
+    """The pp512 chain on the exact 8-bit route (tensor-core form and Q4_0-direct),
+    on the unrotated 4-bit route (tensor-core form) and on the rotated 4-bit route
+    with the Q4_0-direct GEMM."""
     out = []
-    for route in ("q8_rotated", "q4_unrotated", "q4_rotated_q4_0_direct"):
+    for route in ("q8_rotated_tc", "q8_rotated_q4_0_direct", "q4_unrotated",
+                  "q4_rotated_q4_0_direct"):
         rot = route != "q4_unrotated"
-        tc = route == "q4_unrotated"
+        tc = route in ("q4_unrotated", "q8_rotated_tc")
         bufs = []
         for p in CHAIN:
             cid = wl.CFG_ATTN if p is wl.ATTN else wl.CFG_FFN
@@ -569,7 +570,10 @@ def suite_chain_routes(torch, h32, dev, stream, steps, warmup):
 
         def step():
             for wq, wd, x, y in bufs:
-                if route.startswith("q8"):
+                if route == "q8_rotated_tc":
+                    xw8, xdt = h32.h32_quantize_act_q8_tc(x, rotate=rot, stream=stream)
+                    h32.q4_0_x_q8_gemm_tc(wq, wd, xw8, xdt, M=M_TOKENS, y=y, stream=stream)
+                elif route.startswith("q8"):
                     xq, xd = h32.h32_quantize_act_q8(x, rotate=rot, stream=stream)
                     h32.q4_0_x_q8_gemm(wq, wd, xq, xd, y=y, stream=stream)
                 elif tc:

@@ -23,6 +23,7 @@ __all__ = [
     "h32_device_status", "h32_status_string", "h32_set_wait_limit", "h32_version",
     "h32_last_cuda_error", "h32_quantize_act_q4_tc", "h32_prepack_weights_q4_0_tc",
     "q4_0_x_q4_gemm_tc", "h32_quantize_act_q4_tc_gather", "q4_0_x_q4_gemm_tc_experts",
+    "h32_quantize_act_q8_tc", "q4_0_x_q8_gemm_tc",
 ]
 
 
@@ -55,6 +56,8 @@ _SIGS = {
     "h32_quantize_act_q4_tc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _I64, _INT, _P]),
     "h32_prepack_weights_q4_0_tc": (_INT, [_P, _P, _I64, _I64, _P, _P, _I64, _P]),
     "q4_0_x_q4_gemm_tc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P]),
+    "h32_quantize_act_q8_tc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _I64, _INT, _P]),
+    "q4_0_x_q8_gemm_tc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P]),
     "h32_quantize_act_q4_tc_gather": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _P, _I64,
                                              _INT, _P]),
     "q4_0_x_q4_gemm_tc_experts": (_INT, [_P, _P, _I64, ctypes.c_int32, _P, _P, _I64, _P, _I64, _I64,
@@ -271,6 +274,16 @@ def _round4(n: int) -> int:
 def h32_quantize_act_q4_tc(x, rotate=True, xw=None, xdt=None, stream=None):
     """x [M][K] bf16/fp32 -> (xw [M][K] uint8 tc-form codes, xdt [K/32][ldxd] fp32 scales,
     block-major, ldxd = M rounded up to a multiple of 4)."""
+    return _quantize_tc("h32_quantize_act_q4_tc", 1, x, rotate, xw, xdt, stream)
+
+
+def h32_quantize_act_q8_tc(x, rotate=True, xw=None, xdt=None, stream=None):
+    """x [M][K] bf16/fp32 -> (xw8 [M][2K] uint8: per 32-block the e4m3 bytes of 16 h
+    then of l, code = 16 h + l; xdt [K/32][ldxd] fp32 scales)."""
+    return _quantize_tc("h32_quantize_act_q8_tc", 2, x, rotate, xw, xdt, stream)
+
+
+def _quantize_tc(fn, bytes_per_code, x, rotate, xw, xdt, stream):
     torch = _torch()
     _cuda(x, "x")
     if x.dtype == torch.bfloat16:
@@ -282,12 +295,12 @@ def h32_quantize_act_q4_tc(x, rotate=True, xw=None, xdt=None, stream=None):
     ldx = _rows(x, "x")
     M, K = x.shape
     if xw is None:
-        xw = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+        xw = torch.empty((M, K * bytes_per_code), dtype=torch.uint8, device=x.device)
     if xdt is None:
         xdt = torch.zeros((K // 32, _round4(M)), dtype=torch.float32, device=x.device)
-    st = lib().h32_quantize_act_q4_tc(_ptr(x), dt, M, K, ldx, _ptr(xw), _ptr(xdt), xdt.shape[1],
-                                      int(bool(rotate)), _stream(stream))
-    _check("h32_quantize_act_q4_tc", st)
+    st = getattr(lib(), fn)(_ptr(x), dt, M, K, ldx, _ptr(xw), _ptr(xdt), xdt.shape[1],
+                            int(bool(rotate)), _stream(stream))
+    _check(fn, st)
     return xw, xdt
 
 
@@ -310,6 +323,15 @@ def h32_prepack_weights_q4_0_tc(wq, wd, wp=None, wsc=None, stream=None):
 
 def q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=None, y=None, block_sums=None, stream=None):
     """The W4A4 product on tc-form operands (bit-identical to q4_0_x_q4_gemm)."""
+    return _gemm_tc("q4_0_x_q4_gemm_tc", wp, wsc, xw, xdt, M, y, block_sums, stream)
+
+
+def q4_0_x_q8_gemm_tc(wp, wsc, xw8, xdt, M=None, y=None, block_sums=None, stream=None):
+    """The W4A8 product on tc-form operands (bit-identical to q4_0_x_q8_gemm)."""
+    return _gemm_tc("q4_0_x_q8_gemm_tc", wp, wsc, xw8, xdt, M, y, block_sums, stream)
+
+
+def _gemm_tc(fn, wp, wsc, xw, xdt, M, y, block_sums, stream):
     torch = _torch()
     N, K = wp.shape
     if M is None:
@@ -322,9 +344,9 @@ def q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=None, y=None, block_sums=None, stream=
         S = torch.empty((M, N, K // 32), dtype=torch.int32, device=wp.device)
     elif block_sums is not None and block_sums is not False:
         S = block_sums
-    st = lib().q4_0_x_q4_gemm_tc(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt),
-                                 xdt.shape[1], M, N, K, _ptr(y), ldy, _ptr(S), _stream(stream))
-    _check("q4_0_x_q4_gemm_tc", st)
+    st = getattr(lib(), fn)(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt), xdt.shape[1],
+                            M, N, K, _ptr(y), ldy, _ptr(S), _stream(stream))
+    _check(fn, st)
     return (y, S) if S is not None else y
 
 

@@ -50,7 +50,7 @@ __device__ uint32_t g_tc_status;
 
 constexpr int kBM = 128;             // weight rows per tile (MMA M, TMEM lanes)
 constexpr int kBNMax = 128;          // tokens per tile (MMA N)
-constexpr int kStages = 5;           // 128-element K stages in flight
+constexpr int kMaxStages = 5;        // 128-element K stages in flight (at most)
 constexpr int kTileBytes = 16384;    // 128 rows x 128 bytes
 constexpr int kScaleBytes = 2048;    // 4 blocks x 128 fp32
 #ifndef H32_TC_GROUP
@@ -62,14 +62,19 @@ constexpr int kTmemCols = 512;       // kBufs hand-off buffers x kGroup blocks x
 constexpr uint64_t kDrainPolls = 1ull << 22;
 constexpr int kMaxExperts = 1024;
 
-template <int EPQ>
+// XB = 4: one activation byte per code.  XB = 8: two bytes per code, the e4m3
+// bytes of 16 h and of l where the 8-bit code is 16 h + l (0 <= l <= 15), so a
+// 128-element stage carries two activation tiles.
+template <int EPQ, int XB>
 struct TcCfg {
+    static constexpr int kStages = XB == 8 ? 4 : 5;
+    static constexpr int kBTile = XB == 8 ? 2 * kTileBytes : kTileBytes;   // activations per stage
     static constexpr int kEpiWarps = 4 * EPQ;
     static constexpr int kThreads = (2 + kEpiWarps) * 32;
     static constexpr int kMaxChunks = (8 + EPQ - 1) / EPQ;  // 16-column chunks per warp
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kTileBytes;
-    static constexpr int kOffSA = kOffB + kStages * kTileBytes;
+    static constexpr int kOffSA = kOffB + kStages * kBTile;
     static constexpr int kOffSB = kOffSA + kStages * kScaleBytes;
     static constexpr int kOffBar = kOffSB + kStages * kScaleBytes;
     static constexpr int kOffMisc = kOffBar + 32 * 8;
@@ -80,8 +85,8 @@ struct TcCfg {
 
 enum {
     kBarFull = 0,
-    kBarEmpty = kBarFull + kStages,
-    kBarSFull = kBarEmpty + kStages,
+    kBarEmpty = kBarFull + kMaxStages,
+    kBarSFull = kBarEmpty + kMaxStages,
     kBarSEmpty = kBarSFull + kBufs,
     kBarDrain = kBarSEmpty + kBufs
 };
@@ -173,12 +178,12 @@ __device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a, const int *s_o
 // positions of the shared-memory stages and TMEM buffers are carried as
 // counters and phase bits, arrivals come from one elected lane.  Returns false
 // when a wait gave up.
-template <int EPQ>
+template <int EPQ, int XB>
 __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const int *s_off,
                                                const int *s_tpre, uint64_t *bars, const float *s_sa,
                                                const float *s_sb, uint32_t tmem, int warp, int lane,
                                                volatile int *abort_flag) {
-    using C = TcCfg<EPQ>;
+    using C = TcCfg<EPQ, XB>;
     const int ew = warp - 2;
     const int quad = warp & 3;                 // TMEM lanes 32 quad .. 32 quad + 31
     const int part = ew >> 2;                  // share of the columns
@@ -231,7 +236,7 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
             }
             __syncwarp();
             elect_arrive(&bars[kBarEmpty + s]);
-            if (++s == kStages) {
+            if (++s == C::kStages) {
                 s = 0;
                 sph ^= 1;
             }
@@ -258,12 +263,13 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
     return true;
 }
 
-template <int EPQ, bool kSums>
-__global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
+template <int EPQ, int XB, bool kSums>
+__global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_sa,
                    const __grid_constant__ CUtensorMap map_sb, const TcArgs a) {
-    using C = TcCfg<EPQ>;
+    using C = TcCfg<EPQ, XB>;
+    constexpr int kStages = C::kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *s_a = smem + C::kOffA;
@@ -278,7 +284,7 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nst = a.nb / 4;
     const uint64_t lim = a.wait_limit;
-    const uint32_t stage_tx = kTileBytes + a.bn * 128 + kScaleBytes + a.bn * 16;
+    const uint32_t stage_tx = kTileBytes + (XB / 4) * a.bn * 128 + kScaleBytes + a.bn * 16;
     const int E = a.E;
     const int nt = (a.N + kBM - 1) / kBM;
 
@@ -376,7 +382,11 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
                     }
                     mbar_arrive_expect_tx(&bars[kBarFull + s], stage_tx);
                     tma_load_2d(s_a + s * kTileBytes, &map_a, &bars[kBarFull + s], st * 128, ti.wrow);
-                    tma_load_2d(s_b + s * kTileBytes, &map_b, &bars[kBarFull + s], st * 128, ti.g0);
+                    tma_load_2d(s_b + s * C::kBTile, &map_b, &bars[kBarFull + s], st * 128 * (XB / 4),
+                                ti.g0);
+                    if constexpr (XB == 8)
+                        tma_load_2d(s_b + s * C::kBTile + kTileBytes, &map_b, &bars[kBarFull + s],
+                                    st * 256 + 128, ti.g0);
                     tma_load_2d(s_sa + s * (kScaleBytes / 4), &map_sa, &bars[kBarFull + s], st * 4,
                                 ti.wrow);
                     tma_load_2d(s_sb + s * (kScaleBytes / 4), &map_sb, &bars[kBarFull + s], ti.g0,
@@ -406,7 +416,7 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
                     }
                     tc_fence_after();
                     const uint64_t da = smem_desc_sw128(smem_u32(s_a + s * kTileBytes));
-                    const uint64_t db = smem_desc_sw128(smem_u32(s_b + s * kTileBytes));
+                    const uint64_t db = smem_desc_sw128(smem_u32(s_b + s * C::kBTile));
                     for (int j0 = 0; j0 < 4; j0 += kGroup, ++kg) {
                         const int gb = kg % kBufs;
                         if (!mbar_wait_bounded(&bars[kBarSEmpty + gb], ((kg / kBufs) & 1) ^ 1, lim,
@@ -418,10 +428,20 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
                         tc_fence_after();
 #pragma unroll
                         for (int i = 0; i < kGroup; ++i) {
-                            // block j's 32 bytes start 32 j bytes into each 128-byte row
-                            const uint64_t koff = (32 * (j0 + i)) >> 4;
-                            mma_f8f6f4(tmem + (gb * kGroup + i) * 128, da + koff, db + koff, idesc,
-                                       0);
+                            const int j = j0 + i;
+                            // block j's 32 weight bytes start 32 j bytes into each 128-byte row
+                            const uint64_t koff = (32 * j) >> 4;
+                            const uint32_t slot = tmem + (gb * kGroup + i) * 128;
+                            if constexpr (XB == 4) {
+                                mma_f8f6f4(slot, da + koff, db + koff, idesc, 0);
+                            } else {
+                                // S = sum w (16 h) + sum w l: two MMAs into one accumulator
+                                // (every partial sum is an integer below 2^24: exact)
+                                const uint64_t dbj = db + ((j >> 1) * kTileBytes >> 4) +
+                                                     (((j & 1) * 64) >> 4);
+                                mma_f8f6f4(slot, da + koff, dbj, idesc, 0);
+                                mma_f8f6f4(slot, da + koff, dbj + (32 >> 4), idesc, 1);
+                            }
                         }
                         mma_commit(&bars[kBarSFull + gb]);
                     }
@@ -434,8 +454,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ>::kThreads, 1)
         }
     } else if constexpr (!kSums) {
         // ------------------------------------------------------- epilogue
-        if (!epilogue_tiles<EPQ>(a, total, s_off, s_tpre, bars, s_sa, s_sb, tmem, warp, lane,
-                                 abort_flag))
+        if (!epilogue_tiles<EPQ, XB>(a, total, s_off, s_tpre, bars, s_sa, s_sb, tmem, warp, lane,
+                                     abort_flag))
             set_abort(misc);
     } else {
         // ------------------------------------ epilogue with block sums
@@ -615,14 +635,14 @@ int choose_bn_tc(int64_t M, int64_t N, int sms) {
     return best;
 }
 
-template <int EPQ, bool kSums>
+template <int EPQ, int XB, bool kSums>
 h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStream_t s) {
-    using C = TcCfg<EPQ>;
-    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, kSums>,
+    using C = TcCfg<EPQ, XB>;
+    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kSums>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return launch_status(e);
-    gemm_tc_kernel<EPQ, kSums><<<grid, C::kThreads, C::kSmem, s>>>(maps[0], maps[1], maps[2], maps[3],
-                                                                     a);
+    gemm_tc_kernel<EPQ, XB, kSums><<<grid, C::kThreads, C::kSmem, s>>>(maps[0], maps[1], maps[2],
+                                                                         maps[3], a);
     return launch_status(cudaGetLastError());
 }
 
@@ -648,7 +668,7 @@ namespace {
 
 // Shared by the dense and the expert-batched entry points: checks, tensor
 // maps, launch.  E groups of weight rows [E * N][K]; expert_off null = dense.
-h32_status run_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws, int64_t E,
+h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t ldws, int64_t E,
                        const uint8_t *xw, const float *xdt, int64_t ldxd,
                        const int32_t *expert_off, int64_t M, int64_t N, int64_t K, float *y,
                        int64_t ldy, int32_t *block_sums, void *stream) {
@@ -675,7 +695,8 @@ h32_status run_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws, int64_
     }
     CUtensorMap maps[4];
     H32_TRY(make_map(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wp, K, E * N, K, 128, kBM, true));
-    H32_TRY(make_map(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xw, K, M, K, 128, bn, true));
+    const int64_t xrow = K * (xbits / 4);   // activation bytes per row
+    H32_TRY(make_map(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xw, xrow, M, xrow, 128, bn, true));
     H32_TRY(make_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, wsc, ldws, E * N, ldws * 4, 4,
                      kBM, false));
     H32_TRY(make_map(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, xdt, ldxd, K / 32, ldxd * 4, bn, 4,
@@ -692,8 +713,12 @@ h32_status run_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws, int64_
     a.E = static_cast<int32_t>(E);
     a.wait_limit = wait_limit();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return block_sums ? launch_tc<H32_TC_EPI_PER_QUAD, true>(maps, a, static_cast<int>(grid), s)
-                      : launch_tc<H32_TC_EPI_PER_QUAD, false>(maps, a, static_cast<int>(grid), s);
+    const int g = static_cast<int>(grid);
+    if (xbits == 8)
+        return block_sums ? launch_tc<H32_TC_EPI_PER_QUAD, 8, true>(maps, a, g, s)
+                          : launch_tc<H32_TC_EPI_PER_QUAD, 8, false>(maps, a, g, s);
+    return block_sums ? launch_tc<H32_TC_EPI_PER_QUAD, 4, true>(maps, a, g, s)
+                      : launch_tc<H32_TC_EPI_PER_QUAD, 4, false>(maps, a, g, s);
 }
 
 }  // namespace
@@ -703,8 +728,16 @@ extern "C" h32_status q4_0_x_q4_gemm_tc(const uint8_t *wp, const float *wsc, int
                                         const uint8_t *xw, const float *xdt, int64_t ldxd,
                                         int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
                                         int32_t *block_sums, void *stream) {
-    return h32::run_gemm_tc(wp, wsc, ldws, 1, xw, xdt, ldxd, nullptr, M, N, K, y, ldy, block_sums,
-                            stream);
+    return h32::run_gemm_tc(4, wp, wsc, ldws, 1, xw, xdt, ldxd, nullptr, M, N, K, y, ldy,
+                            block_sums, stream);
+}
+
+extern "C" h32_status q4_0_x_q8_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                        const uint8_t *xw8, const float *xdt, int64_t ldxd,
+                                        int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
+                                        int32_t *block_sums, void *stream) {
+    return h32::run_gemm_tc(8, wp, wsc, ldws, 1, xw8, xdt, ldxd, nullptr, M, N, K, y, ldy,
+                            block_sums, stream);
 }
 
 extern "C" h32_status q4_0_x_q4_gemm_tc_experts(const uint8_t *wp, const float *wsc, int64_t ldws,
@@ -713,6 +746,6 @@ extern "C" h32_status q4_0_x_q4_gemm_tc_experts(const uint8_t *wp, const float *
                                                 int64_t N, int64_t K, float *y, int64_t ldy,
                                                 int32_t *block_sums, void *stream) {
     if (!expert_off) return H32_ERR_INVALID_ARG;
-    return h32::run_gemm_tc(wp, wsc, ldws, E, xw, xdt, ldxd, expert_off, R, N, K, y, ldy,
+    return h32::run_gemm_tc(4, wp, wsc, ldws, E, xw, xdt, ldxd, expert_off, R, N, K, y, ldy,
                             block_sums, stream);
 }

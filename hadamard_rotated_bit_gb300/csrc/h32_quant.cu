@@ -239,11 +239,36 @@ __device__ __forceinline__ uint32_t e4m3_of_magnitudes(uint32_t mag) {
     return r | (((mag >> 3) & 0x01010101u) * 0x50u);
 }
 
+// four values 0..15 (one per byte) -> their e4m3 bytes: 0..7 from the table
+// (selector nibbles 8..15 select in sign-replicate mode and give 0x00), 8..15 are
+// 1.l2 l1 l0 x 2^3 = 0x48 + value
+__device__ __forceinline__ uint32_t e4m3_of_0_15(uint32_t v) {
+    const uint32_t sel = (v & 0xFu) | ((v >> 4) & 0xF0u) | ((v >> 8) & 0xF00u) |
+                         ((v >> 12) & 0xF000u);
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(0x44403800u), "r"(0x4E4C4A48u), "r"(sel));
+    const uint32_t big = ((v >> 3) & 0x01010101u) * 0xFFu;
+    return r | ((v + 0x48484848u) & big);
+}
+
 // four int8 codes in [-8, 8] -> four e4m3 bytes (sign bit | e4m3 of |c|)
 __device__ __forceinline__ uint32_t tc_bytes(uint32_t c) {
     const uint32_t m = byte_sign_mask(c);                       // 0xFF where negative
     const uint32_t mag = (c ^ m) + (m & 0x01010101u);           // |c| per byte, no carries
     return e4m3_of_magnitudes(mag) | (m & 0x80808080u);
+}
+
+// four int8 codes c = 16 h + l (0 <= l <= 15, -8 <= h <= 7) -> the e4m3 bytes
+// of 16 h (hi) and of l (lo).  16 h is h with the exponent raised by 4: 0x20
+// added to every non-zero byte.
+__device__ __forceinline__ void tc_bytes_q8(uint32_t c, uint32_t &hi, uint32_t &lo) {
+    const uint32_t l = c & 0x0F0F0F0Fu;
+    const uint32_t hn = (c >> 4) & 0x0F0F0F0Fu;                        // h as a 4-bit pattern
+    const uint32_t hs = hn | (byte_sign_mask(hn << 4) & 0xF0F0F0F0u);  // sign-extended bytes
+    const uint32_t h8 = tc_bytes(hs);
+    const uint32_t nz = ((h8 & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) & 0x80808080u;
+    hi = h8 + (nz >> 2);
+    lo = e4m3_of_0_15(l);
 }
 
 // Rotate + quantize to 4-bit codes in tc form.  Threads walk the blocks in
@@ -252,7 +277,7 @@ __device__ __forceinline__ uint32_t tc_bytes(uint32_t c) {
 // block row segment and writes a whole 32-byte code segment.  With kGather,
 // output row r is the quantized input row row_idx[r] (an index outside
 // [0, T) records kStatusGuard and yields zero codes and a zero scale).
-template <bool kBf16, bool kRotate, bool kGather>
+template <bool kBf16, int kBits, bool kRotate, bool kGather>
 __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restrict__ x, uint32_t nblk,
                                                           uint32_t M, uint32_t K, int64_t ldx,
                                                           const int32_t *__restrict__ row_idx,
@@ -286,17 +311,19 @@ __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restric
             }
         }
         if constexpr (kRotate) rotate32(v);
+        constexpr float kQmax = (kBits == 4) ? 7.0f : 127.0f;
+        constexpr float kQmin = (kBits == 4) ? -8.0f : -127.0f;
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        const float d = __fdiv_rn(amax, 7.0f);
+        const float d = __fdiv_rn(amax, kQmax);
         const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
         uint32_t bits[32];
         if (!(amax < INFINITY) || isinf(id)) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 float t = __fmul_rn(v[i], id);
-                t = fminf(fmaxf(t, -8.0f), 7.0f);
+                t = fminf(fmaxf(t, kQmin), kQmax);
                 bits[i] = __float_as_uint(__fadd_rn(t, kRoundMagic));
             }
         } else {
@@ -304,14 +331,29 @@ __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restric
             for (int i = 0; i < 32; ++i)
                 bits[i] = __float_as_uint(__fadd_rn(__fmul_rn(v[i], id), kRoundMagic));
         }
-        uint32_t w[8];
+        if constexpr (kBits == 4) {
+            uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            w[k] = tc_bytes(
-                pack_low_bytes(bits[4 * k], bits[4 * k + 1], bits[4 * k + 2], bits[4 * k + 3]));
-        uint4 *dst = reinterpret_cast<uint4 *>(xw + int64_t(row) * K + 32 * b);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            for (int k = 0; k < 8; ++k)
+                w[k] = tc_bytes(
+                    pack_low_bytes(bits[4 * k], bits[4 * k + 1], bits[4 * k + 2], bits[4 * k + 3]));
+            uint4 *dst = reinterpret_cast<uint4 *>(xw + int64_t(row) * K + 32 * b);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else {
+            // 64 bytes per block: the 32 bytes of 16 h, then the 32 bytes of l
+            uint32_t wh[8], wl[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                tc_bytes_q8(pack_low_bytes(bits[4 * k], bits[4 * k + 1], bits[4 * k + 2],
+                                           bits[4 * k + 3]),
+                            wh[k], wl[k]);
+            uint4 *dst = reinterpret_cast<uint4 *>(xw + int64_t(row) * 2 * K + 64 * b);
+            dst[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            dst[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
+            dst[2] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            dst[3] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+        }
         xdt[int64_t(b) * ldxd + row] = d;
         b += sb;
         row += srow;
@@ -447,6 +489,7 @@ extern "C" h32_status h32_rotate_quantize_weights_q4_0(const float *w, int64_t N
 
 namespace h32 {
 namespace {
+template <int kBits>
 h32_status quantize_act_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K, int64_t ldx,
                            const int32_t *row_idx, int64_t T, uint8_t *xw, float *xdt,
                            int64_t ldxd, int rotate, void *stream) {
@@ -468,8 +511,8 @@ h32_status quantize_act_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint32_t m32 = static_cast<uint32_t>(M), k32 = static_cast<uint32_t>(K);
 #define H32_QTC(BF, ROT, GA)                                                                     \
-    quant_act_tc_kernel<BF, ROT, GA><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, row_idx, T, xw, \
-                                                          xdt, ldxd)
+    quant_act_tc_kernel<BF, kBits, ROT, GA><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, row_idx, \
+                                                                 T, xw, xdt, ldxd)
     const bool bf = dt == H32_IN_BF16, rot = rotate != 0, ga = row_idx != nullptr;
     if (bf && rot && ga) H32_QTC(true, true, true);
     else if (bf && rot) H32_QTC(true, true, false);
@@ -488,7 +531,13 @@ h32_status quantize_act_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
 extern "C" h32_status h32_quantize_act_q4_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
                                              int64_t ldx, uint8_t *xw, float *xdt, int64_t ldxd,
                                              int rotate, void *stream) {
-    return h32::quantize_act_tc(x, dt, M, K, ldx, nullptr, M, xw, xdt, ldxd, rotate, stream);
+    return h32::quantize_act_tc<4>(x, dt, M, K, ldx, nullptr, M, xw, xdt, ldxd, rotate, stream);
+}
+
+extern "C" h32_status h32_quantize_act_q8_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
+                                             int64_t ldx, uint8_t *xw8, float *xdt, int64_t ldxd,
+                                             int rotate, void *stream) {
+    return h32::quantize_act_tc<8>(x, dt, M, K, ldx, nullptr, M, xw8, xdt, ldxd, rotate, stream);
 }
 
 extern "C" h32_status h32_quantize_act_q4_tc_gather(const void *x, h32_in_dtype dt, int64_t T,
@@ -496,7 +545,7 @@ extern "C" h32_status h32_quantize_act_q4_tc_gather(const void *x, h32_in_dtype 
                                                     int64_t R, uint8_t *xw, float *xdt,
                                                     int64_t ldxd, int rotate, void *stream) {
     if (!row_idx) return H32_ERR_INVALID_ARG;
-    return h32::quantize_act_tc(x, dt, R, K, ldx, row_idx, T, xw, xdt, ldxd, rotate, stream);
+    return h32::quantize_act_tc<4>(x, dt, R, K, ldx, row_idx, T, xw, xdt, ldxd, rotate, stream);
 }
 
 extern "C" h32_status h32_prepack_weights_q4_0_tc(const uint8_t *wq, const uint16_t *wd, int64_t N,

@@ -169,6 +169,19 @@ h32_status h32_quantize_act_q4_tc(const void *x, h32_in_dtype dt, int64_t M, int
                                   void *stream);
 
 /*
+ * The exact 8-bit route in tc form ("509 tokens a second of prompt: the
+ * Hadamard route ships", section "Why prompts are a matrix-unit problem"):
+ * codes and scales exactly as h32_quantize_act_q8; each code c = 16 h + l with
+ * 0 <= l <= 15 (so -8 <= h <= 7) is stored as two e4m3 bytes, both exact:
+ *   xw8    [M][2K] out: per 32-block 64 bytes, the 32 bytes of 16 h, then the
+ *          32 bytes of l (element order within each half)
+ *   xdt    [K/32][ldxd] out as for h32_quantize_act_q4_tc
+ */
+h32_status h32_quantize_act_q8_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
+                                  int64_t ldx, uint8_t *xw8, float *xdt, int64_t ldxd, int rotate,
+                                  void *stream);
+
+/*
  * The same with a row gather, for expert-batched products ("Where the engine is
  * going: HRX and the NPU", section "4-bit activations reach the MoE experts"):
  * output row r is input row row_idx[r] of x[T][ldx], so the rows come out in the
@@ -206,6 +219,18 @@ h32_status h32_prepack_weights_q4_0_tc(const uint8_t *wq, const uint16_t *wd, in
  */
 h32_status q4_0_x_q4_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws,
                              const uint8_t *xw, const float *xdt, int64_t ldxd, int64_t M,
+                             int64_t N, int64_t K, float *y, int64_t ldy, int32_t *block_sums,
+                             void *stream);
+
+/*
+ * The W4A8 product of q4_0_x_q8_gemm on tc-form operands (weights from
+ * h32_prepack_weights_q4_0_tc, activations from h32_quantize_act_q8_tc):
+ * S = sum w (16 h) + sum w l per block (two MMAs into one accumulator, every
+ * partial sum an integer below 2^24, so S is exact), then the same epilogue;
+ * bit-identical to q4_0_x_q8_gemm.  Requires K % 128 == 0 and N % 16 == 0.
+ */
+h32_status q4_0_x_q8_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws,
+                             const uint8_t *xw8, const float *xdt, int64_t ldxd, int64_t M,
                              int64_t N, int64_t K, float *y, int64_t ldy, int32_t *block_sums,
                              void *stream);
 

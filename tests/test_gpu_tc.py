@@ -290,3 +290,115 @@ def test_tc_moe_config_sampled(h32):
         ni = r.integers(0, N, ri.size)
         r32, _, _ = oracle.gemm_experts_sampled(wq, wd, xq, xd, ridx, off, N, K, ri, ni)
         assert np.array_equal(y[ri, ni].view(np.uint32), r32.view(np.uint32))
+
+
+# --------------------------------------------------------------------------
+# the exact 8-bit route in tc form: code = 16 h + l, both parts exact in e4m3
+# --------------------------------------------------------------------------
+def _q8_codes_from_tc(xw8, K):
+    M = xw8.shape[0]
+    v = e4m3_value(xw8).reshape(M, K // 32, 2, 32)
+    return (v[:, :, 0, :] + v[:, :, 1, :]).reshape(M, K), v
+
+
+@pytest.mark.parametrize("M,K", [(3, 128), (45, 256), (512, 5120)])
+def test_quantize_q8_tc_matches_oracle(h32, M, K):
+    x = wl.f32_to_bf16_bits(wl.act_normal_outliers(M, K, 0.005, 30.0, 0, wl.CFG_TEST, 270 + M))
+    xw8, xdt = h32.h32_quantize_act_q8_tc(torch_bf16(x))
+    xw8, xdt = np_of(xw8), np_of(xdt)
+    rq, rd = oracle.quantize_act_q8(x)
+    codes, parts = _q8_codes_from_tc(xw8, K)
+    assert np.array_equal(codes, rq.astype(np.float64))
+    # the parts are the digits: l in 0..15, 16 h with h in -8..7
+    assert parts[:, :, 1, :].min() >= 0 and parts[:, :, 1, :].max() <= 15
+    assert np.all(np.mod(parts[:, :, 0, :], 16) == 0)
+    assert np.array_equal(xdt[:, :M].T.view(np.uint32), rd.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 16, 128), (33, 144, 256), (130, 128, 512)])
+def test_gemm_q8_tc_bit_exact(h32, M, N, K):
+    import torch
+    x = wl.f32_to_bf16_bits(wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, 280 + M))
+    w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, 281 + N)
+    wq, wd = oracle.quantize_weights_q4_0(w)
+    xq, xd = oracle.quantize_act_q8(x)
+    wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(wq), torch_of(wd.view(np.int16)))
+    xw8, xdt = h32.h32_quantize_act_q8_tc(torch_bf16(x))
+    y, S = h32.q4_0_x_q8_gemm_tc(wp, wsc, xw8, xdt, M=M, block_sums=True)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r32, _, rS = oracle.gemm(wq, wd, xq, xd, K, want_block_sums=True)
+    assert np.array_equal(np_of(S).astype(np.int64), rS)
+    assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
+
+
+def test_gemm_q8_tc_extreme_codes(h32):
+    """Codes +-127 against weight values -8 and +7: the largest 8-bit block sums
+    (|S| = 32512), built here from the byte definition."""
+    import torch
+    M, N, K = 24, 32, 128
+    xc = np.full((M, K), -127, np.int64)
+    xc[::2] = 127
+    xc[1::3] = 0
+    xc[2::5, ::3] = -1
+    wc = np.full((N, K), -8, np.int64)
+    wc[1::2] = 7
+
+    lut = {0: 0x00, 1: 0x38, 2: 0x40, 3: 0x44, 4: 0x48, 5: 0x4A, 6: 0x4C, 7: 0x4E, 8: 0x50}
+
+    def e4m3_int(v):   # |v| <= 15 or a multiple of 16 up to 128: exact
+        a = abs(int(v))
+        if a <= 8:
+            b = lut[a]
+        elif a < 16:
+            b = 0x48 + a
+        else:
+            b = lut[a // 16] + 0x20
+        return b | (0x80 if v < 0 else 0)
+
+    xb = np.zeros((M, 2 * K), np.uint8)
+    for m in range(M):
+        for k in range(K):
+            c = int(xc[m, k])
+            l = c & 15
+            h = (c - l) // 16
+            blk, j = divmod(k, 32)
+            xb[m, 64 * blk + j] = e4m3_int(16 * h)
+            xb[m, 64 * blk + 32 + j] = e4m3_int(l)
+    assert np.array_equal(_q8_codes_from_tc(xb, K)[0], xc.astype(np.float64))
+    wb = np.vectorize(e4m3_int)(wc).astype(np.uint8)
+    xd = np.full((M, K // 32), 0.25, np.float32)
+    wd = oracle.f32_to_f16(np.full((N, K // 32), 0.5, np.float32))
+    wsc = wd.view(np.float16).astype(np.float32)
+    xdt = np.ascontiguousarray(xd.T)
+    y, S = h32.q4_0_x_q8_gemm_tc(torch_of(wb), torch_of(wsc), torch_of(xb), torch_of(xdt), M=M,
+                                 block_sums=True)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    def pack(u):
+        u = u.reshape(u.shape[0], -1, 32)
+        return ((u[:, :, :16] & 15) | ((u[:, :, 16:] & 15) << 4)).reshape(u.shape[0], -1).astype(np.uint8)
+    wq = pack(wc + 8)
+    r32, _, rS = oracle.gemm(wq, wd, xc.astype(np.int8), xd, K, want_block_sums=True)
+    assert np.abs(rS).max() == 32512
+    assert np.array_equal(np_of(S).astype(np.int64), rS)
+    assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
+
+
+def test_gemm_q8_tc_pp512_sampled(h32):
+    import torch
+    p = wl.ATTN
+    x = p.activations(512, 0, wl.CFG_ATTN)
+    w = p.weights(0, wl.CFG_ATTN)
+    wq, wd = oracle.quantize_weights_q4_0(w)
+    xq, xd = oracle.quantize_act_q8(x)
+    wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(wq), torch_of(wd.view(np.int16)))
+    xw8, xdt = h32.h32_quantize_act_q8_tc(torch_bf16(x))
+    y = np_of(h32.q4_0_x_q8_gemm_tc(wp, wsc, xw8, xdt, M=512))
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r = np.random.default_rng(2)
+    mi = np.concatenate([r.integers(0, 512, 3000), [511]])
+    ni = np.concatenate([r.integers(0, p.N, 3000), [p.N - 1]])
+    r32, _, _ = oracle.gemm_sampled(wq, wd, xq, xd, p.K, mi, ni)
+    assert np.array_equal(y[mi, ni].view(np.uint32), r32.view(np.uint32))

@@ -56,6 +56,8 @@ def _load():
                 "o_f16_to_f32": [_P, _P, _I64],
                 "o_fwht32_f32": [_P, _P, _I64],
                 "o_fwht32_f64": [_P, _P, _I64],
+                "o_fwht_n_f32": [_P, _P, _I64, ctypes.c_int],
+                "o_fwht_n_f64": [_P, _P, _I64, ctypes.c_int],
                 "o_quantize_act": [_P, _I64, _I64, ctypes.c_int, ctypes.c_int, _P, _P],
                 "o_quantize_weights_q4_0": [_P, _I64, _I64, ctypes.c_int, _P, _P],
                 "o_decode_act4": [_P, _I64, _I64, _P],
@@ -71,6 +73,8 @@ def _load():
                 fn.restype = None
             lib.o_h32_scale.argtypes = []
             lib.o_h32_scale.restype = ctypes.c_float
+            lib.o_rot_scale.argtypes = [ctypes.c_int]
+            lib.o_rot_scale.restype = ctypes.c_float
             _lib = lib
     return _lib
 
@@ -138,6 +142,44 @@ def fwht32_f64(x: np.ndarray) -> np.ndarray:
     return out
 
 
+# the larger rotations (the pages' next step: 64 and 128 points, scales per 32)
+ROTATIONS = (32, 64, 128)
+
+
+def rot_points(rotate) -> int:
+    """The quantizers' `rotate` argument -> points of the transform (0 = none):
+    False/0 -> 0, True/1/32 -> 32, 64 -> 64, 128 -> 128."""
+    if rotate is True or rotate == 1:
+        return 32
+    if rotate is False or rotate == 0 or rotate is None:
+        return 0
+    n = int(rotate)
+    assert n in ROTATIONS, f"rotation of {n} points is not supported"
+    return n
+
+
+def rot_scale(n: int) -> float:
+    """The fp32 constant an n-point rotation multiplies by (nearest 1/sqrt(n))."""
+    return float(_load().o_rot_scale(int(n)))
+
+
+def fwht_n(x: np.ndarray, n: int) -> np.ndarray:
+    """Rotate every consecutive n-block of ``x`` (fp32, size % n == 0)."""
+    x = _c(x, np.float32)
+    assert x.size % n == 0 and n in ROTATIONS
+    out = np.empty_like(x)
+    _load().o_fwht_n_f32(_ptr(x), _ptr(out), x.size, n)
+    return out
+
+
+def fwht_n_f64(x: np.ndarray, n: int) -> np.ndarray:
+    x = _c(x, np.float64)
+    assert x.size % n == 0 and n in ROTATIONS
+    out = np.empty_like(x)
+    _load().o_fwht_n_f64(_ptr(x), _ptr(out), x.size, n)
+    return out
+
+
 # --------------------------------------------------------------------------
 # activation quantizers (4-bit route and the exact 8-bit route)
 # --------------------------------------------------------------------------
@@ -147,36 +189,41 @@ def _widen(x: np.ndarray) -> np.ndarray:
     return _c(x, np.float32)
 
 
-def quantize_act_q4(x: np.ndarray, rotate: bool = True):
-    """x [M][K] (fp32, or bf16 as uint16 bits) -> (xq [M][K/2] u8, xd [M][K/32] f32)."""
+def quantize_act_q4(x: np.ndarray, rotate=True):
+    """x [M][K] (fp32, or bf16 as uint16 bits) -> (xq [M][K/2] u8, xd [M][K/32] f32).
+    rotate: False / True (32 points) / 64 / 128."""
     xf = _widen(x)
     M, K = xf.shape
-    assert K % 32 == 0
+    n = rot_points(rotate)
+    assert K % 32 == 0 and K % max(n, 1) == 0
     xq = np.empty((M, K // 2), np.uint8)
     xd = np.empty((M, K // 32), np.float32)
-    _load().o_quantize_act(_ptr(xf), M, K, 4, int(bool(rotate)), _ptr(xq), _ptr(xd))
+    _load().o_quantize_act(_ptr(xf), M, K, 4, n, _ptr(xq), _ptr(xd))
     return xq, xd
 
 
-def quantize_act_q8(x: np.ndarray, rotate: bool = True):
-    """x [M][K] -> (xq [M][K] int8, xd [M][K/32] f32)."""
+def quantize_act_q8(x: np.ndarray, rotate=True):
+    """x [M][K] -> (xq [M][K] int8, xd [M][K/32] f32).  rotate as for quantize_act_q4."""
     xf = _widen(x)
     M, K = xf.shape
-    assert K % 32 == 0
+    n = rot_points(rotate)
+    assert K % 32 == 0 and K % max(n, 1) == 0
     xq = np.empty((M, K), np.int8)
     xd = np.empty((M, K // 32), np.float32)
-    _load().o_quantize_act(_ptr(xf), M, K, 8, int(bool(rotate)), _ptr(xq), _ptr(xd))
+    _load().o_quantize_act(_ptr(xf), M, K, 8, n, _ptr(xq), _ptr(xd))
     return xq, xd
 
 
-def quantize_weights_q4_0(w: np.ndarray, rotate: bool = True):
-    """w [N][K] fp32 -> (wq [N][K/2] u8 codes 0..15, wd [N][K/32] fp16 bits as u16)."""
+def quantize_weights_q4_0(w: np.ndarray, rotate=True):
+    """w [N][K] fp32 -> (wq [N][K/2] u8 codes 0..15, wd [N][K/32] fp16 bits as u16).
+    rotate as for quantize_act_q4."""
     w = _c(w, np.float32)
     N, K = w.shape
-    assert K % 32 == 0
+    n = rot_points(rotate)
+    assert K % 32 == 0 and K % max(n, 1) == 0
     wq = np.empty((N, K // 2), np.uint8)
     wd = np.empty((N, K // 32), np.uint16)
-    _load().o_quantize_weights_q4_0(_ptr(w), N, K, int(bool(rotate)), _ptr(wq), _ptr(wd))
+    _load().o_quantize_weights_q4_0(_ptr(w), N, K, n, _ptr(wq), _ptr(wd))
     return wq, wd
 
 

@@ -130,6 +130,73 @@ static void fwht32_f64(double v[32])
     for (int i = 0; i < 32; ++i) v[i] = v[i] * s;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Larger rotations, 64 and 128 points, with the scales still per 32-block   */
+/* ("Qwen3.8-27B at 45.7 tok/s ...", section "What's next": a larger         */
+/* rotation is the next step).  Same Sylvester transform and stage order:    */
+/* strides 1, 2, ..., n/2, then one multiply by the fp32 nearest 1/sqrt(n).  */
+/* ------------------------------------------------------------------------ */
+
+static float rot_scale_f32(int n) { return (float)(1.0 / sqrt((double)n)); }
+
+static void fwht_n_f32(float *v, int n)
+{
+    for (int h = 1; h < n; h <<= 1) {
+        for (int i = 0; i < n; ++i) {
+            if ((i & h) == 0) {
+                float a = v[i];
+                float c = v[i + h];
+                v[i] = a + c;
+                v[i + h] = a - c;
+            }
+        }
+    }
+    const float s = rot_scale_f32(n);
+    for (int i = 0; i < n; ++i) v[i] = v[i] * s;
+}
+
+static void fwht_n_f64(double *v, int n)
+{
+    for (int h = 1; h < n; h <<= 1) {
+        for (int i = 0; i < n; ++i) {
+            if ((i & h) == 0) {
+                double a = v[i];
+                double c = v[i + h];
+                v[i] = a + c;
+                v[i + h] = a - c;
+            }
+        }
+    }
+    const double s = 1.0 / sqrt((double)n);
+    for (int i = 0; i < n; ++i) v[i] = v[i] * s;
+}
+
+/* Rotate consecutive n-blocks (n = 32, 64 or 128); `count` values in all. */
+void o_fwht_n_f32(const float *in, float *out, int64_t count, int n)
+{
+    for (int64_t b = 0; b + n <= count; b += n) {
+        float v[128];
+        memcpy(v, in + b, sizeof(float) * (size_t)n);
+        fwht_n_f32(v, n);
+        memcpy(out + b, v, sizeof(float) * (size_t)n);
+    }
+}
+
+void o_fwht_n_f64(const double *in, double *out, int64_t count, int n)
+{
+    for (int64_t b = 0; b + n <= count; b += n) {
+        double v[128];
+        memcpy(v, in + b, sizeof(double) * (size_t)n);
+        fwht_n_f64(v, n);
+        memcpy(out + b, v, sizeof(double) * (size_t)n);
+    }
+}
+
+float o_rot_scale(int n) { return rot_scale_f32(n); }
+
+/* rotate argument of the quantizers: 0 = none, 1 or 32 = 32 points, 64, 128 */
+static int rot_points(int rotate) { return rotate == 1 ? 32 : rotate; }
+
 /* Rotate n consecutive 32-blocks. */
 void o_fwht32_f32(const float *in, float *out, int64_t nblocks)
 {
@@ -180,18 +247,31 @@ static void quantize_block_sym(const float y[32], int qmin, int qmax, int q[32],
 /* x: fp32 activations [M][K] row-major (bf16 inputs are widened first with
  * o_bf16_to_f32).  bits = 4: xq is [M][K/2] bytes in Q4_0 nibble order,
  * two's-complement nibbles.  bits = 8: xq is [M][K] int8.  xd is [M][K/32].
- * rotate = 0 skips the Walsh-Hadamard step (the unrotated 4-bit route). */
+ * rotate = 0 skips the Walsh-Hadamard step (the unrotated 4-bit route); 1 or 32
+ * rotates each 32-block; 64 or 128 rotates each 64- or 128-block (K a multiple
+ * of it) and still takes one scale per 32-block of the rotated values. */
 void o_quantize_act(const float *x, int64_t M, int64_t K, int bits, int rotate,
                     uint8_t *xq, float *xd)
 {
     const int64_t nb = K / 32;
     const int qmax = (bits == 4) ? 7 : 127;
     const int qmin = (bits == 4) ? -8 : -127;
+    const int n = rot_points(rotate);
     for (int64_t m = 0; m < M; ++m) {
+        float row[128];
         for (int64_t b = 0; b < nb; ++b) {
             float v[32];
-            memcpy(v, x + m * K + 32 * b, sizeof v);
-            if (rotate) fwht32_f32(v);
+            if (n > 32) {
+                /* the first block of each n-block rotates all n values */
+                if ((32 * b) % n == 0) {
+                    memcpy(row, x + m * K + 32 * b, sizeof(float) * (size_t)n);
+                    fwht_n_f32(row, n);
+                }
+                memcpy(v, row + (32 * b) % n, sizeof v);
+            } else {
+                memcpy(v, x + m * K + 32 * b, sizeof v);
+                if (n == 32) fwht32_f32(v);
+            }
             int q[32];
             float d;
             quantize_block_sym(v, qmin, qmax, q, &d);
@@ -238,16 +318,27 @@ static void q4_0_block(const float y[32], uint8_t qs[16], uint16_t *d16)
 }
 
 /* w: fp32 [N][K] -> wq [N][K/2] (codes 0..15, Q4_0 nibble order),
- * wd [N][K/32] fp16 bits.  rotate = 0 gives plain Q4_0. */
+ * wd [N][K/32] fp16 bits.  rotate = 0 gives plain Q4_0; 1/32, 64, 128 as for
+ * the activations. */
 void o_quantize_weights_q4_0(const float *w, int64_t N, int64_t K, int rotate,
                              uint8_t *wq, uint16_t *wd)
 {
     const int64_t nb = K / 32;
+    const int rn = rot_points(rotate);
     for (int64_t n = 0; n < N; ++n) {
+        float row[128];
         for (int64_t b = 0; b < nb; ++b) {
             float v[32];
-            memcpy(v, w + n * K + 32 * b, sizeof v);
-            if (rotate) fwht32_f32(v);
+            if (rn > 32) {
+                if ((32 * b) % rn == 0) {
+                    memcpy(row, w + n * K + 32 * b, sizeof(float) * (size_t)rn);
+                    fwht_n_f32(row, rn);
+                }
+                memcpy(v, row + (32 * b) % rn, sizeof v);
+            } else {
+                memcpy(v, w + n * K + 32 * b, sizeof v);
+                if (rn == 32) fwht32_f32(v);
+            }
             q4_0_block(v, wq + n * (K / 2) + 16 * b, wd + n * nb + b);
         }
     }

@@ -452,3 +452,129 @@ def test_experts_sampled_vs_numpy():
         assert np.array_equal(S[i], sb)
         ref = (wd[e, n].view(np.float16).astype(np.float64) * xd[row_idx[rr]] * sb).sum()
         assert abs(y64[i] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+# --------------------------------------------------------------------------
+# larger rotations, 64 and 128 points, scales still per 32-block ("Qwen3.8-27B
+# at 45.7 tok/s ...", section "What's next")
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("n", [64, 128])
+def test_rot_scale_is_nearest_fp32(n):
+    getcontext().prec = 60
+    exact = Decimal(1) / Decimal(n).sqrt()
+    c = np.float32(oracle.rot_scale(n))
+    for nb in (np.nextafter(c, np.float32(1)), np.nextafter(c, np.float32(0))):
+        assert abs(Decimal(float(c)) - exact) <= abs(Decimal(float(nb)) - exact)
+    if n == 64:
+        assert c == np.float32(0.125)
+    assert np.float32(oracle.rot_scale(32)) == np.float32(oracle.h32_scale())
+
+
+def _materialize_hn(n):
+    eye = np.eye(n, dtype=np.float32)
+    return oracle.fwht_n(eye.reshape(-1), n).reshape(n, n).T.astype(np.float64)
+
+
+@pytest.mark.parametrize("n", [64, 128])
+def test_hn_entries_are_sylvester_signs_times_c(n):
+    H = _materialize_hn(n)
+    c = np.float64(np.float32(oracle.rot_scale(n)))
+    ref = scipy.linalg.hadamard(n).astype(np.float64) * c
+    assert np.array_equal(H, ref)
+    for i in (0, 3, n - 1):
+        for k in (0, 5, n // 2, n - 1):
+            assert H[i, k] == (-1) ** _popcount(i & k) * c
+    assert np.abs(H @ H.T - np.eye(n)).max() <= 1e-6
+
+
+@pytest.mark.parametrize("n", [64, 128])
+def test_fwht_n_vs_dense_matrix_and_invariance(n):
+    r = np.random.default_rng(11)
+    x = r.standard_normal((50, n))
+    ref = x @ (scipy.linalg.hadamard(n) / np.sqrt(float(n))).T
+    y64 = oracle.fwht_n_f64(x.reshape(-1), n).reshape(50, n)
+    assert np.abs(y64 - ref).max() <= 1e-13 * np.abs(x).sum(axis=1).max()
+    for K in (n, 4 * n, 5120):
+        a, b = r.standard_normal(K), r.standard_normal(K)
+        ha, hb = oracle.fwht_n_f64(a, n), oracle.fwht_n_f64(b, n)
+        assert abs(float(a @ b) - float(ha @ hb)) <= 1e-9 * float(np.abs(a * b).sum())
+
+
+@pytest.mark.parametrize("n", [64, 128])
+def test_one_hot_closed_form_larger_rotation(n):
+    """A unit vector in an n-block spreads to +-C_n at every position, so each of
+    its n/32 scale blocks gets d = C_n / 7 and codes +-7 with Sylvester signs;
+    the Q4_0 weight rule takes each 32-block's first element as its signed max
+    s C_n, giving d = -s C_n / 8 and codes 0 where the sign is s, 15 elsewhere."""
+    c = np.float32(oracle.rot_scale(n))
+    K = 2 * n
+    for k in (0, 1, n // 2 + 3, n - 1):
+        x = np.zeros((1, K), np.float32)
+        x[0, n + k] = 1.0      # second n-block; the first stays zero
+        sign = np.array([(-1) ** _popcount(i & k) for i in range(n)], np.float32)
+        xq, xd = oracle.quantize_act_q4(x, n)
+        codes = oracle.decode_act4(xq, K)[0]
+        assert np.all(codes[:n] == 0) and np.all(xd[0, : n // 32] == 0)
+        assert np.array_equal(codes[n:], (7 * sign).astype(np.int8))
+        assert np.all(xd[0, n // 32:] == np.float32(c / np.float32(7)))
+        q8, _ = oracle.quantize_act_q8(x, n)
+        assert np.array_equal(q8[0, n:], (127 * sign).astype(np.int8))
+        wq, wd = oracle.quantize_weights_q4_0(x, n)
+        wc = oracle.decode_w4(wq, K)[0] + 8
+        dw = oracle.f16_to_f32(wd[0])
+        for j in range(n // 32):
+            s0 = sign[32 * j]          # the block's signed max is its first element
+            blk = sign[32 * j: 32 * j + 32]
+            assert np.array_equal(wc[n + 32 * j: n + 32 * j + 32], np.where(blk == s0, 0, 15))
+            d = oracle.f16_to_f32(oracle.f32_to_f16(np.array([-s0 * c / 8], np.float32)))[0]
+            assert dw[n // 32 + j] == d
+
+
+@pytest.mark.parametrize("n", [64, 128])
+def test_constant_block_larger_rotation(n):
+    """A constant n-block rotates to (n c C_n, 0, ..., 0): the first 32-block
+    gets code 7 at position 0, the other blocks of the n-block are all zero
+    with d = 0."""
+    for val in (0.75, -3.0):
+        x = np.full((1, n), val, np.float32)
+        y = oracle.fwht_n(x.reshape(-1), n)
+        assert y[0] == np.float32(np.float32(n * val) * np.float32(oracle.rot_scale(n)))
+        assert np.all(y[1:] == 0)
+        xq, xd = oracle.quantize_act_q4(x, n)
+        codes = oracle.decode_act4(xq, n)[0]
+        expect = np.zeros(n, np.int8)
+        expect[0] = 7 if val > 0 else -7
+        assert np.array_equal(codes, expect)
+        assert np.all(xd[0, 1:] == 0) and xd[0, 0] > 0
+
+
+@pytest.mark.parametrize("n", [64, 128])
+def test_larger_rotation_route_approximates_exact_product(n):
+    r = np.random.default_rng(12)
+    M, N, K = 8, 16, 512
+    x = wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, 300)
+    w = (0.02 * r.standard_normal((N, K))).astype(np.float32)
+    wq, wd = oracle.quantize_weights_q4_0(w, n)
+    xq, xd = oracle.quantize_act_q4(x, n)
+    _, y64, _ = oracle.gemm(wq, wd, xq, xd, K)
+    ref = x.astype(np.float64) @ w.astype(np.float64).T
+    assert np.linalg.norm(y64 - ref) / np.linalg.norm(ref) < 0.12
+    # weights rotated with 32 points, activations with n: the product is destroyed
+    wq32, wd32 = oracle.quantize_weights_q4_0(w, 32)
+    _, ybad, _ = oracle.gemm(wq32, wd32, xq, xd, K)
+    assert np.linalg.norm(ybad - ref) / np.linalg.norm(ref) > 0.5
+
+
+@pytest.mark.parametrize("n", [64, 128])
+def test_larger_rotation_stage_order(n):
+    """Hand-derived: x[0] = 2^24, x[1] = 1, x[n/2] = -2^24.  With strides in
+    ascending order the stride-1 stage rounds 2^24 + 1 to 2^24 first (ties to
+    even); the last stage then gives y[0] = 0, y[1] = -1, y[n/2] = 2^25 and
+    y[n/2 + 1] = fl(2^25 - 1) = 2^25, each times C_n.  Descending strides would
+    give y[0] = C_n instead."""
+    c = np.float32(oracle.rot_scale(n))
+    x = np.zeros(n, np.float32)
+    x[0], x[1], x[n // 2] = 2.0 ** 24, 1.0, -(2.0 ** 24)
+    y = oracle.fwht_n(x, n)
+    assert y[0] == 0 and y[1] == -c
+    assert y[n // 2] == np.float32(2.0 ** 25) * c and y[n // 2 + 1] == np.float32(2.0 ** 25) * c

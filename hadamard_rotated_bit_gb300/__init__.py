@@ -123,6 +123,15 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def _rot_arg(rotate) -> int:
+    """rotate: False/0 (none), True/1/32 (32 points), 64 or 128 points."""
+    if rotate is True:
+        return 1
+    if rotate is False or rotate is None:
+        return 0
+    return int(rotate)
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -164,7 +173,7 @@ def _quantize_act(fn_name, bits, x, rotate, xq, xd, stream):
                          dtype=torch.uint8 if bits == 4 else torch.int8, device=x.device)
     if xd is None:
         xd = torch.empty((M, K // 32), dtype=torch.float32, device=x.device)
-    st = getattr(lib(), fn_name)(_ptr(x), dt, M, K, ldx, _ptr(xq), _ptr(xd), int(bool(rotate)),
+    st = getattr(lib(), fn_name)(_ptr(x), dt, M, K, ldx, _ptr(xq), _ptr(xd), _rot_arg(rotate),
                                  _stream(stream))
     _check(fn_name, st)
     return xq, xd
@@ -191,7 +200,7 @@ def h32_rotate_quantize_weights_q4_0(w, rotate=True, wq=None, wd=None, stream=No
         wq = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
     if wd is None:
         wd = torch.empty((N, K // 32), dtype=torch.int16, device=w.device)
-    st = lib().h32_rotate_quantize_weights_q4_0(_ptr(w), N, K, int(bool(rotate)), _ptr(wq),
+    st = lib().h32_rotate_quantize_weights_q4_0(_ptr(w), N, K, _rot_arg(rotate), _ptr(wq),
                                                 _ptr(wd), _stream(stream))
     _check("h32_rotate_quantize_weights_q4_0", st)
     return wq, wd
@@ -299,7 +308,7 @@ def _quantize_tc(fn, bytes_per_code, x, rotate, xw, xdt, stream):
     if xdt is None:
         xdt = torch.zeros((K // 32, _round4(M)), dtype=torch.float32, device=x.device)
     st = getattr(lib(), fn)(_ptr(x), dt, M, K, ldx, _ptr(xw), _ptr(xdt), xdt.shape[1],
-                            int(bool(rotate)), _stream(stream))
+                            _rot_arg(rotate), _stream(stream))
     _check(fn, st)
     return xw, xdt
 
@@ -372,7 +381,7 @@ def h32_quantize_act_q4_tc_gather(x, row_idx, rotate=True, xw=None, xdt=None, st
     if xdt is None:
         xdt = torch.zeros((K // 32, _round4(R)), dtype=torch.float32, device=x.device)
     st = lib().h32_quantize_act_q4_tc_gather(_ptr(x), dt, T, K, ldx, _ptr(row_idx), R, _ptr(xw),
-                                             _ptr(xdt), xdt.shape[1], int(bool(rotate)),
+                                             _ptr(xdt), xdt.shape[1], _rot_arg(rotate),
                                              _stream(stream))
     _check("h32_quantize_act_q4_tc_gather", st)
     return xw, xdt

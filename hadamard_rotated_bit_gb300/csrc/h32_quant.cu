@@ -34,6 +34,7 @@ __device__ uint32_t g_quant_status;   // kStatusGuard: a gathered row index out 
 
 // fp32 nearest to 1/sqrt(32) (bit pattern 0x3E3504F3)
 constexpr float kInvSqrt32 = 0x1.6a09e6p-3f;
+constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;   // half of kInvSqrt32: the fp32 nearest 1/sqrt(128)
 // 1.5 * 2^23: adding it to |t| < 2^22 leaves round-half-even(t) in the low
 // mantissa bits as a two's-complement integer
 constexpr float kRoundMagic = 12582912.0f;
@@ -70,7 +71,8 @@ __device__ __forceinline__ void load_block_f32(const float *__restrict__ p, floa
 // ----------------------------------------------------------------------------
 // the rotation: butterfly with strides 1, 2, 4, 8, 16, then the 1/sqrt(32) scale
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ void rotate32(float (&v)[32]) {
+// strides 1, 2, 4, 8, 16: the in-thread stages of every rotation size
+__device__ __forceinline__ void butterfly32(float (&v)[32]) {
 #pragma unroll
     for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
@@ -82,8 +84,46 @@ __device__ __forceinline__ void rotate32(float (&v)[32]) {
             }
         }
     }
+}
+
+__device__ __forceinline__ void rotate32(float (&v)[32]) {
+    butterfly32(v);
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], kInvSqrt32);
+}
+
+// The kRot-point rotation (0 = none, 32, 64, 128) of the thread's 32-block,
+// which is 32-block `pos` (0 .. kRot/32 - 1) of its kRot-block.  The other
+// 32-blocks of the kRot-block are held by the lanes that differ from this one
+// in the low bits pos covers (lane ^ 1, lane ^ 2); those lanes are in `mask`.
+// Strides 32 and 64 pair element i of two blocks: the lower block takes
+// a + c, the upper a - c (a the lower block's value), as in strides 1..16.
+template <int kRot>
+__device__ __forceinline__ void rotate_block(float (&v)[32], uint32_t pos, unsigned mask) {
+    if constexpr (kRot == 32) {
+        rotate32(v);
+    } else if constexpr (kRot > 32) {
+        butterfly32(v);
+#pragma unroll
+        for (int hb = 1; hb < kRot / 32; hb <<= 1) {
+            const bool lower = (pos & hb) == 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float c = __shfl_xor_sync(mask, v[i], hb);
+                v[i] = lower ? __fadd_rn(v[i], c) : __fsub_rn(c, v[i]);
+            }
+        }
+        const float sc = (kRot == 64) ? 0.125f : kInvSqrt128;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], sc);
+    }
+}
+
+// the rotate argument of the entry points: 0 = none, 1 or 32, 64, 128 points
+// (-1 = not supported)
+int rot_points(int rotate) {
+    return rotate == 0 ? 0 : rotate == 1 || rotate == 32 ? 32 : rotate == 64 ? 64
+         : rotate == 128 ? 128 : -1;
 }
 
 // low byte of each of four words -> one word
@@ -96,7 +136,7 @@ __device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint3
 // ----------------------------------------------------------------------------
 // activation quantizer
 // ----------------------------------------------------------------------------
-template <bool kBf16, int kBits, bool kRotate>
+template <bool kBf16, int kBits, int kRot>
 __global__ void __launch_bounds__(256) quant_act_kernel(const void *__restrict__ x, uint32_t nblk,
                                                        uint32_t nb, int64_t ldx,
                                                        uint8_t *__restrict__ xq,
@@ -110,13 +150,16 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const void *__restrict__
     uint32_t g = blockIdx.x * blockDim.x + threadIdx.x;
     uint32_t row = g / nb, b = g % nb;
     for (; g < nblk; g += stride) {
+        const unsigned mask = __activemask();
         float v[32];
         if constexpr (kBf16) {
             load_block_bf16(reinterpret_cast<const uint16_t *>(x) + int64_t(row) * ldx + 32 * b, v);
         } else {
             load_block_f32(reinterpret_cast<const float *>(x) + int64_t(row) * ldx + 32 * b, v);
         }
-        if constexpr (kRotate) rotate32(v);
+        // the kRot/32 blocks of a kRot-block sit in adjacent lanes: nb, the
+        // grid stride and nblk are multiples of kRot/32
+        rotate_block<kRot>(v, b, mask);
 
         float amax = 0.0f;
 #pragma unroll
@@ -176,15 +219,16 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const void *__restrict__
 // ----------------------------------------------------------------------------
 // offline weights: rotate, then the Q4_0 rule
 // ----------------------------------------------------------------------------
-template <bool kRotate>
+template <int kRot>
 __global__ void __launch_bounds__(256) quant_w_kernel(const float *__restrict__ w, uint32_t nblk,
                                                      uint8_t *__restrict__ wq,
                                                      uint16_t *__restrict__ wd) {
     const uint32_t stride = gridDim.x * blockDim.x;
     for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < nblk; g += stride) {
+        const unsigned mask = __activemask();
         float v[32];
         load_block_f32(w + int64_t(g) * 32, v);
-        if constexpr (kRotate) rotate32(v);
+        rotate_block<kRot>(v, g, mask);   // g = row * nb + b with nb a multiple of kRot/32
         // signed value of largest magnitude, first one on ties
         float amax = 0.0f, mx = 0.0f;
 #pragma unroll
@@ -277,17 +321,27 @@ __device__ __forceinline__ void tc_bytes_q8(uint32_t c, uint32_t &hi, uint32_t &
 // block row segment and writes a whole 32-byte code segment.  With kGather,
 // output row r is the quantized input row row_idx[r] (an index outside
 // [0, T) records kStatusGuard and yields zero codes and a zero scale).
-template <bool kBf16, int kBits, bool kRotate, bool kGather>
+template <bool kBf16, int kBits, int kRot, bool kGather>
 __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restrict__ x, uint32_t nblk,
                                                           uint32_t M, uint32_t K, int64_t ldx,
                                                           const int32_t *__restrict__ row_idx,
                                                           int64_t T, uint8_t *__restrict__ xw,
                                                           float *__restrict__ xdt, int64_t ldxd) {
+    // kRot <= 32: block-major walk g = b * M + row.  kRot > 32: the G = kRot/32
+    // blocks of a kRot-block must sit in adjacent lanes, so
+    // g = ((b / G) * M + row) * G + b % G
+    constexpr uint32_t G = kRot > 32 ? kRot / 32 : 1;
     const uint32_t stride = gridDim.x * blockDim.x;
     const uint32_t sb = stride / M, srow = stride % M;
     uint32_t g = blockIdx.x * blockDim.x + threadIdx.x;
     uint32_t b = g / M, row = g % M;
     for (; g < nblk; g += stride) {
+        const unsigned mask = __activemask();
+        if constexpr (G > 1) {
+            const uint32_t rest = g / G;
+            row = rest % M;
+            b = (rest / M) * G + g % G;
+        }
         float v[32];
         int64_t src = row;
         bool valid = true;
@@ -310,7 +364,7 @@ __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restric
                 for (int i = 0; i < 32; ++i) v[i] = 0.0f;
             }
         }
-        if constexpr (kRotate) rotate32(v);
+        rotate_block<kRot>(v, b, mask);
         constexpr float kQmax = (kBits == 4) ? 7.0f : 127.0f;
         constexpr float kQmin = (kBits == 4) ? -8.0f : -127.0f;
         float amax = 0.0f;
@@ -411,6 +465,8 @@ template <int kBits>
 h32_status quantize_act(const void *x, h32_in_dtype dt, int64_t M, int64_t K, int64_t ldx,
                         void *xq, float *xd, int rotate, void *stream) {
     if (M < 0 || K <= 0 || (K % 32) != 0 || ldx < K) return H32_ERR_INVALID_ARG;
+    if (rot_points(rotate) < 0 || (rot_points(rotate) > 0 && K % rot_points(rotate) != 0))
+        return H32_ERR_INVALID_ARG;
     if (dt != H32_IN_F32 && dt != H32_IN_BF16) return H32_ERR_INVALID_ARG;
     if (M == 0) return H32_OK;
     if (!x || !xq || !xd) return H32_ERR_INVALID_ARG;
@@ -426,13 +482,15 @@ h32_status quantize_act(const void *x, h32_in_dtype dt, int64_t M, int64_t K, in
     const int grid = grid_for(nblk, sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *q = reinterpret_cast<uint8_t *>(xq);
-    if (dt == H32_IN_BF16) {
-        if (rotate) quant_act_kernel<true, kBits, true><<<grid, 256, 0, s>>>(x, nblk, f, ldx, q, xd);
-        else quant_act_kernel<true, kBits, false><<<grid, 256, 0, s>>>(x, nblk, f, ldx, q, xd);
-    } else {
-        if (rotate) quant_act_kernel<false, kBits, true><<<grid, 256, 0, s>>>(x, nblk, f, ldx, q, xd);
-        else quant_act_kernel<false, kBits, false><<<grid, 256, 0, s>>>(x, nblk, f, ldx, q, xd);
+    const bool bf = dt == H32_IN_BF16;
+#define H32_QA(BF, R) quant_act_kernel<BF, kBits, R><<<grid, 256, 0, s>>>(x, nblk, f, ldx, q, xd)
+    switch (rot_points(rotate)) {
+        case 0: if (bf) H32_QA(true, 0); else H32_QA(false, 0); break;
+        case 32: if (bf) H32_QA(true, 32); else H32_QA(false, 32); break;
+        case 64: if (bf) H32_QA(true, 64); else H32_QA(false, 64); break;
+        default: if (bf) H32_QA(true, 128); else H32_QA(false, 128); break;
     }
+#undef H32_QA
     return launch_status(cudaGetLastError());
 }
 
@@ -473,6 +531,8 @@ extern "C" h32_status h32_rotate_quantize_weights_q4_0(const float *w, int64_t N
                                                        void *stream) {
     using namespace h32;
     if (N < 0 || K <= 0 || (K % 32) != 0) return H32_ERR_INVALID_ARG;
+    if (rot_points(rotate) < 0 || (rot_points(rotate) > 0 && K % rot_points(rotate) != 0))
+        return H32_ERR_INVALID_ARG;
     if (N == 0) return H32_OK;
     if (!w || !wq || !wd) return H32_ERR_INVALID_ARG;
     if (!aligned16(w) || !aligned16(wq) || !aligned16(wd)) return H32_ERR_ALIGNMENT;
@@ -482,8 +542,12 @@ extern "C" h32_status h32_rotate_quantize_weights_q4_0(const float *w, int64_t N
     const uint32_t nblk = static_cast<uint32_t>(N * (K / 32));
     const int grid = grid_for(nblk, sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (rotate) quant_w_kernel<true><<<grid, 256, 0, s>>>(w, nblk, wq, wd);
-    else quant_w_kernel<false><<<grid, 256, 0, s>>>(w, nblk, wq, wd);
+    switch (rot_points(rotate)) {
+        case 0: quant_w_kernel<0><<<grid, 256, 0, s>>>(w, nblk, wq, wd); break;
+        case 32: quant_w_kernel<32><<<grid, 256, 0, s>>>(w, nblk, wq, wd); break;
+        case 64: quant_w_kernel<64><<<grid, 256, 0, s>>>(w, nblk, wq, wd); break;
+        default: quant_w_kernel<128><<<grid, 256, 0, s>>>(w, nblk, wq, wd); break;
+    }
     return launch_status(cudaGetLastError());
 }
 
@@ -494,6 +558,8 @@ h32_status quantize_act_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
                            const int32_t *row_idx, int64_t T, uint8_t *xw, float *xdt,
                            int64_t ldxd, int rotate, void *stream) {
     if (M < 0 || K <= 0 || (K % 32) != 0 || ldx < K || ldxd < M || (ldxd % 4) != 0 || T < 0)
+        return H32_ERR_INVALID_ARG;
+    if (rot_points(rotate) < 0 || (rot_points(rotate) > 0 && K % rot_points(rotate) != 0))
         return H32_ERR_INVALID_ARG;
     if (dt != H32_IN_F32 && dt != H32_IN_BF16) return H32_ERR_INVALID_ARG;
     if (M == 0) return H32_OK;
@@ -513,15 +579,21 @@ h32_status quantize_act_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
 #define H32_QTC(BF, ROT, GA)                                                                     \
     quant_act_tc_kernel<BF, kBits, ROT, GA><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, row_idx, \
                                                                  T, xw, xdt, ldxd)
-    const bool bf = dt == H32_IN_BF16, rot = rotate != 0, ga = row_idx != nullptr;
-    if (bf && rot && ga) H32_QTC(true, true, true);
-    else if (bf && rot) H32_QTC(true, true, false);
-    else if (bf && ga) H32_QTC(true, false, true);
-    else if (bf) H32_QTC(true, false, false);
-    else if (rot && ga) H32_QTC(false, true, true);
-    else if (rot) H32_QTC(false, true, false);
-    else if (ga) H32_QTC(false, false, true);
-    else H32_QTC(false, false, false);
+#define H32_QTC_R(ROT)                    \
+    do {                                  \
+        if (bf && ga) H32_QTC(true, ROT, true);   \
+        else if (bf) H32_QTC(true, ROT, false);   \
+        else if (ga) H32_QTC(false, ROT, true);   \
+        else H32_QTC(false, ROT, false);          \
+    } while (0)
+    const bool bf = dt == H32_IN_BF16, ga = row_idx != nullptr;
+    switch (rot_points(rotate)) {
+        case 0: H32_QTC_R(0); break;
+        case 32: H32_QTC_R(32); break;
+        case 64: H32_QTC_R(64); break;
+        default: H32_QTC_R(128); break;
+    }
+#undef H32_QTC_R
 #undef H32_QTC
     return launch_status(cudaGetLastError());
 }

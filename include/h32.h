@@ -69,7 +69,15 @@ typedef enum h32_in_dtype {
  *   x      [M][ldx] activations of type `dt`, ldx >= K
  *   xq     [M][K/2] out: two's-complement 4-bit codes, Q4_0 nibble order
  *   xd     [M][K/32] out: fp32 scales d
- *   rotate 1 = rotate first (the Hadamard route); 0 = plain 4-bit route
+ *   rotate 1 (or 32) = rotate first (the Hadamard route); 0 = plain 4-bit route;
+ *          64 or 128 = the larger rotation the pages name as the next step
+ *          ("Qwen3.8-27B at 45.7 tok/s ...", section "What's next"): the same
+ *          Sylvester butterfly over each 64- or 128-block (strides 1 .. n/2,
+ *          then one multiply by the fp32 nearest 1/sqrt(n)), scales still one
+ *          per 32-block; K must be a multiple of n.  Any other value:
+ *          H32_ERR_INVALID_ARG.  The same argument, with the same meaning, is
+ *          taken by every quantizer below and by the weight quantizer; weights
+ *          and activations of one product must use the same rotation.
  */
 h32_status h32_quantize_act_q4(const void *x, h32_in_dtype dt, int64_t M, int64_t K, int64_t ldx,
                                uint8_t *xq, float *xd, int rotate, void *stream);
@@ -86,7 +94,8 @@ h32_status h32_quantize_act_q8(const void *x, h32_in_dtype dt, int64_t M, int64_
 /*
  * Offline weight step ("Making the file is part of the engine": rotate the
  * projections, then quantize to Q4_0).  Each 32-block of a weight row is
- * rotated with the same transform as the activations (if rotate = 1), then
+ * rotated with the same transform as the activations (rotate as for
+ * h32_quantize_act_q4: 0, 1/32, 64 or 128 points), then
  * rounded by the Q4_0 rule: the signed value of largest magnitude (first on
  * ties) maps to code 0, d = max / -8, code = min(15, trunc(y * (1/d) + 8.5)),
  * d stored as fp16 rounded to nearest even.

@@ -121,3 +121,15 @@ def test_tc_form_bad_arguments(lib):
     assert _call("q4_0_x_q4_gemm_tc_experts", p, p, 4, 2, p, p, 8, None, 8, 16, 128, p, 16, None,
                  s) == h32.H32_ERR_INVALID_ARG
     assert _call("q4_0_x_q4_gemm_tc", p, p, 4, p, p, 8, 0, 16, 128, p, 16, None, s) == h32.H32_OK
+
+
+def test_rotation_size_validated(lib):
+    p = ctypes.c_void_p(256)
+    s = ctypes.c_void_p(0)
+    # unsupported size, and K not a multiple of the rotation
+    assert _call("h32_quantize_act_q4", p, 1, 4, 64, 64, p, p, 16, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_quantize_act_q8", p, 1, 4, 96, 96, p, p, 64, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_rotate_quantize_weights_q4_0", p, 4, 192, 128, p, p,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_quantize_act_q4_tc", p, 1, 8, 64, 64, p, p, 8, 128, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_quantize_act_q4", p, 1, 0, 128, 128, p, p, 128, s) == h32.H32_OK

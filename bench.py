@@ -589,6 +589,43 @@ def suite_chain_routes(torch, h32, dev, stream, steps, warmup):
     return out
 
 
+def suite_rotations(torch, h32, dev, stream, steps, warmup):
+    """Rotation size A/B on the tensor-core-form 4-bit route: the pp512 chain's
+    throughput with no rotation and with 32-, 64- and 128-point rotations, and the
+    error of the attention projection's output against the exact fp64 product
+    x . W^T on 64 sampled token rows (the accuracy side of the pages' claim)."""
+    out = []
+    p0 = wl.ATTN
+    x_att = p0.activations(M_TOKENS, 0, wl.CFG_ATTN)
+    w_att = p0.weights(0, wl.CFG_ATTN)
+    rows = np.random.default_rng(4).choice(M_TOKENS, 64, replace=False)
+    exact = wl.bf16_bits_to_f32(x_att[rows]).astype(np.float64) @ w_att.astype(np.float64).T
+    for rot in (0, 32, 64, 128):
+        bufs = []
+        for p in CHAIN:
+            cid = wl.CFG_ATTN if p is wl.ATTN else wl.CFG_FFN
+            wq, wd = h32.h32_rotate_quantize_weights_q4_0(
+                torch.from_numpy(p.weights(0, cid)).to(dev), rotate=rot)
+            wp, wsc = h32.h32_prepack_weights_q4_0_tc(wq, wd)
+            del wq, wd
+            x = torch.from_numpy(p.activations(M_TOKENS, 0, cid).view(np.int16)).view(
+                torch.bfloat16).to(dev)
+            bufs.append((wp, wsc, x, torch.empty((M_TOKENS, p.N), device=dev)))
+
+        def step():
+            for wp, wsc, x, y in bufs:
+                xw, xdt = h32.h32_quantize_act_q4_tc(x, rotate=rot, stream=stream)
+                h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M_TOKENS, y=y, stream=stream)
+        ms = _events_time(torch, step, steps, warmup, stream)
+        y_att = bufs[0][3][torch.from_numpy(rows).to(dev)].cpu().numpy().astype(np.float64)
+        rel = float(np.linalg.norm(y_att - exact) / np.linalg.norm(exact))
+        out.append({"suite": f"pp512_chain_q4_rotation_{rot}", "value": round(M_TOKENS / (ms / 1e3), 1),
+                    "unit": UNIT, "ms_per_step": round(ms, 4),
+                    "attn_output_rel_error_vs_exact_fp64": round(rel, 5)})
+        del bufs
+    return out
+
+
 def suite_moe(torch, h32, dev, stream, steps, warmup):
     """One 1024-token MoE micro-batch: quantize, expert gate/up GEMM, quantize the
     down input, expert down GEMM (routing, SwiGLU and combine are outside the path)."""
@@ -724,6 +761,7 @@ def run_suite(args):
     lines = []
     lines += suite_quant_stream(torch, h32, dev, stream, steps, warmup, peaks)
     lines += suite_chain_routes(torch, h32, dev, stream, steps, warmup)
+    lines += suite_rotations(torch, h32, dev, stream, steps, warmup)
     lines += suite_moe(torch, h32, dev, stream, steps, warmup)
     lines += suite_long(torch, h32, dev, stream, steps, warmup)
     if h32.h32_device_status(stream) != 0:

@@ -626,6 +626,38 @@ def suite_rotations(torch, h32, dev, stream, steps, warmup):
     return out
 
 
+def suite_fused_producer(torch, h32, dev, stream, steps, warmup):
+    """The attention projection (512 x 5120 x 5120) followed by the quantization of
+    its output for the next projection: separately (GEMM writes y, the quantizer
+    reads it back) and fused into the GEMM's epilogue (with and without y)."""
+    p = wl.ATTN
+    wq, wd = h32.h32_rotate_quantize_weights_q4_0(torch.from_numpy(p.weights(0, wl.CFG_ATTN)).to(dev))
+    wp, wsc = h32.h32_prepack_weights_q4_0_tc(wq, wd)
+    x = torch.from_numpy(p.activations(M_TOKENS, 0, wl.CFG_ATTN).view(np.int16)).view(
+        torch.bfloat16).to(dev)
+    xw, xdt = h32.h32_quantize_act_q4_tc(x)
+    y = torch.empty((M_TOKENS, p.N), device=dev)
+    xn = torch.empty((M_TOKENS, p.N), dtype=torch.uint8, device=dev)
+    xnd = torch.zeros((p.N // 32, M_TOKENS), dtype=torch.float32, device=dev)
+
+    def separate():
+        h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M_TOKENS, y=y, stream=stream)
+        h32.h32_quantize_act_q4_tc(y, xw=xn, xdt=xnd, stream=stream)
+
+    def fused_y():
+        h32.q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=M_TOKENS, y=y, xw_next=xn,
+                                         xdt_next=xnd, stream=stream)
+
+    def fused():
+        h32.q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=M_TOKENS, want_y=False, xw_next=xn,
+                                         xdt_next=xnd, stream=stream)
+    out = {}
+    for name, fn in (("separate", separate), ("fused_with_y", fused_y), ("fused", fused)):
+        out[name] = round(_events_time(torch, fn, steps, warmup, stream), 4)
+    return [{"suite": "attn_gemm_then_next_quantization_pp512", "unit": "ms", "ms": out,
+             "value": out["fused"]}]
+
+
 def suite_moe(torch, h32, dev, stream, steps, warmup):
     """One 1024-token MoE micro-batch: quantize, expert gate/up GEMM, quantize the
     down input, expert down GEMM (routing, SwiGLU and combine are outside the path)."""
@@ -762,6 +794,7 @@ def run_suite(args):
     lines += suite_quant_stream(torch, h32, dev, stream, steps, warmup, peaks)
     lines += suite_chain_routes(torch, h32, dev, stream, steps, warmup)
     lines += suite_rotations(torch, h32, dev, stream, steps, warmup)
+    lines += suite_fused_producer(torch, h32, dev, stream, steps, warmup)
     lines += suite_moe(torch, h32, dev, stream, steps, warmup)
     lines += suite_long(torch, h32, dev, stream, steps, warmup)
     if h32.h32_device_status(stream) != 0:

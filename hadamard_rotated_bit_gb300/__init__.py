@@ -23,7 +23,7 @@ __all__ = [
     "h32_device_status", "h32_status_string", "h32_set_wait_limit", "h32_version",
     "h32_last_cuda_error", "h32_quantize_act_q4_tc", "h32_prepack_weights_q4_0_tc",
     "q4_0_x_q4_gemm_tc", "h32_quantize_act_q4_tc_gather", "q4_0_x_q4_gemm_tc_experts",
-    "h32_quantize_act_q8_tc", "q4_0_x_q8_gemm_tc",
+    "h32_quantize_act_q8_tc", "q4_0_x_q8_gemm_tc", "q4_0_x_q4_gemm_tc_quant_next",
 ]
 
 
@@ -56,6 +56,8 @@ _SIGS = {
     "h32_quantize_act_q4_tc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _I64, _INT, _P]),
     "h32_prepack_weights_q4_0_tc": (_INT, [_P, _P, _I64, _I64, _P, _P, _I64, _P]),
     "q4_0_x_q4_gemm_tc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P]),
+    "q4_0_x_q4_gemm_tc_quant_next": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P,
+                                            _I64, _P, _P, _I64, _INT, _P]),
     "h32_quantize_act_q8_tc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _I64, _INT, _P]),
     "q4_0_x_q8_gemm_tc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P]),
     "h32_quantize_act_q4_tc_gather": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _P, _I64,
@@ -412,3 +414,27 @@ def q4_0_x_q4_gemm_tc_experts(wp, wsc, xw, xdt, expert_off, N, R=None, y=None, b
                                          _ptr(S), _stream(stream))
     _check("q4_0_x_q4_gemm_tc_experts", st)
     return (y, S) if S is not None else y
+
+
+def q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=None, y=None, want_y=True, rotate_next=True,
+                                 xw_next=None, xdt_next=None, stream=None):
+    """The tc W4A4 product with its output also quantized for the next projection
+    in the same kernel.  Returns (y or None, xw_next [M][N] uint8, xdt_next
+    [N/32][ldxd] fp32)."""
+    torch = _torch()
+    N, K = wp.shape
+    if M is None:
+        M = xw.shape[0]
+    if y is None and want_y:
+        y = torch.empty((M, N), dtype=torch.float32, device=wp.device)
+    ldy = _rows(y, "y") if y is not None else N
+    if xw_next is None:
+        xw_next = torch.empty((M, N), dtype=torch.uint8, device=wp.device)
+    if xdt_next is None:
+        xdt_next = torch.zeros((N // 32, _round4(M)), dtype=torch.float32, device=wp.device)
+    st = lib().q4_0_x_q4_gemm_tc_quant_next(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt),
+                                            xdt.shape[1], M, N, K, _ptr(y), ldy, _ptr(xw_next),
+                                            _ptr(xdt_next), xdt_next.shape[1],
+                                            _rot_arg(rotate_next), _stream(stream))
+    _check("q4_0_x_q4_gemm_tc_quant_next", st)
+    return y, xw_next, xdt_next

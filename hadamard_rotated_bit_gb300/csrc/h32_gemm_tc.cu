@@ -42,6 +42,7 @@
 
 #include "h32_common.cuh"
 #include "h32_epilogue.cuh"
+#include "h32_tcform.cuh"
 
 namespace h32 {
 namespace {
@@ -93,13 +94,41 @@ enum {
 enum { kMiscTmem = 0, kMiscAbort = 1, kMiscBad = 2, kMiscTotal = 3 };
 
 struct TcArgs {
-    float *y;
+    float *y;                    // nullable when qn is set
     int32_t *bsum;
     const int32_t *expert_off;   // [E+1] row offsets of the expert groups, or null (dense)
-    int64_t ldy;
+    uint8_t *qn;                 // the output quantized for the next projection, or null:
+    float *qnd;                  //   codes [M][N] (tc form), scales [N/32][ldqnd]
+    int64_t ldy, ldqnd;
     int32_t M, N, nb, bn, E;     // M: activation rows (all groups)
+    int32_t qn_rot;              // 0 or 32: rotate the next projection's 32-blocks
     uint64_t wait_limit;
 };
+
+// One 32-block of the next projection's input, held one value per lane (the
+// warp's 32 TMEM lanes are 32 consecutive output features of one token):
+// rotate it across the lanes (strides 1 .. 16 by shuffles, then the fp32
+// 1/sqrt(32)), quantize it to a 4-bit code like the activation quantizer, and
+// return the lane's tc-form byte; *d gets the block's scale.  Warp-collective.
+__device__ __forceinline__ uint32_t quant_lane_block(float v, int lane, bool rot, float *d) {
+    if (rot) {
+#pragma unroll
+        for (int h = 1; h < 32; h <<= 1) {
+            const float p = __shfl_xor_sync(0xFFFFFFFFu, v, h);
+            v = (lane & h) ? __fsub_rn(p, v) : __fadd_rn(v, p);
+        }
+        v = __fmul_rn(v, kInvSqrt32);
+    }
+    float amax = fabsf(v);
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, h));
+    const float dd = __fdiv_rn(amax, 7.0f);
+    const float id = (dd != 0.0f) ? __frcp_rn(dd) : 0.0f;
+    float t = __fmul_rn(v, id);
+    if (!(amax < INFINITY) || isinf(id)) t = fminf(fmaxf(t, -8.0f), 7.0f);
+    *d = dd;
+    return tc_bytes(__float_as_uint(__fadd_rn(t, kRoundMagic)) & 0xFFu) & 0xFFu;
+}
 
 __device__ __forceinline__ void record(uint32_t bits) { atomicOr(&g_tc_status, bits); }
 
@@ -178,7 +207,7 @@ __device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a, const int *s_o
 // positions of the shared-memory stages and TMEM buffers are carried as
 // counters and phase bits, arrivals come from one elected lane.  Returns false
 // when a wait gave up.
-template <int EPQ, int XB>
+template <int EPQ, int XB, bool kQN>
 __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const int *s_off,
                                                const int *s_tpre, uint64_t *bars, const float *s_sa,
                                                const float *s_sb, uint32_t tmem, int warp, int lane,
@@ -242,7 +271,7 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
             }
         }
         const int64_t n = ti.n0 + row;
-        if (n < a.N) {
+        if (n < a.N && (!kQN || a.y)) {
 #pragma unroll
             for (int c = 0; c < C::kMaxChunks; ++c) {
                 if (c < nch) {
@@ -259,17 +288,44 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
                 }
             }
         }
+        // the output quantized for the next projection: this warp's 32 lanes are
+        // one 32-block of it for every token column (N % 32 == 0, so a block is
+        // all inside or all outside the N rows)
+        if (kQN && ti.n0 + quad * 32 < a.N) {
+            const int nb0 = (ti.n0 + quad * 32) >> 5;
+#pragma unroll
+            for (int c = 0; c < C::kMaxChunks; ++c) {
+                if (c < nch) {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int col = c0 + c * 16 + q;
+                        const uint64_t pr = acc[8 * c + (q >> 1)];
+                        const float v = __uint_as_float(static_cast<uint32_t>(pr >> (32 * (q & 1))));
+                        float d;
+                        const uint32_t byte = quant_lane_block(v, lane, a.qn_rot != 0, &d);
+                        if (col >= ti.clo && col < ti.chi) {
+                            const int64_t g = ti.g0 + col;
+                            a.qn[g * a.N + n] = static_cast<uint8_t>(byte);
+                            if (lane == 0) a.qnd[nb0 * a.ldqnd + g] = d;
+                        }
+                    }
+                }
+            }
+        }
     }
     return true;
 }
 
-template <int EPQ, int XB, bool kSums>
+// kEpi: 0 = y only, 1 = y and the block sums, 2 = y (optional) and the output
+// quantized for the next projection
+template <int EPQ, int XB, int kEpi>
 __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_sa,
                    const __grid_constant__ CUtensorMap map_sb, const TcArgs a) {
     using C = TcCfg<EPQ, XB>;
     constexpr int kStages = C::kStages;
+    constexpr bool kSums = kEpi == 1;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *s_a = smem + C::kOffA;
@@ -454,7 +510,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
         }
     } else if constexpr (!kSums) {
         // ------------------------------------------------------- epilogue
-        if (!epilogue_tiles<EPQ, XB>(a, total, s_off, s_tpre, bars, s_sa, s_sb, tmem, warp, lane,
+        if (!epilogue_tiles<EPQ, XB, kEpi == 2>(a, total, s_off, s_tpre, bars, s_sa, s_sb, tmem,
+                                                warp, lane,
                                      abort_flag))
             set_abort(misc);
     } else {
@@ -635,14 +692,14 @@ int choose_bn_tc(int64_t M, int64_t N, int sms) {
     return best;
 }
 
-template <int EPQ, int XB, bool kSums>
+template <int EPQ, int XB, int kEpi>
 h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStream_t s) {
     using C = TcCfg<EPQ, XB>;
-    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kSums>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return launch_status(e);
-    gemm_tc_kernel<EPQ, XB, kSums><<<grid, C::kThreads, C::kSmem, s>>>(maps[0], maps[1], maps[2],
-                                                                         maps[3], a);
+    gemm_tc_kernel<EPQ, XB, kEpi><<<grid, C::kThreads, C::kSmem, s>>>(maps[0], maps[1], maps[2],
+                                                                        maps[3], a);
     return launch_status(cudaGetLastError());
 }
 
@@ -671,16 +728,21 @@ namespace {
 h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t ldws, int64_t E,
                        const uint8_t *xw, const float *xdt, int64_t ldxd,
                        const int32_t *expert_off, int64_t M, int64_t N, int64_t K, float *y,
-                       int64_t ldy, int32_t *block_sums, void *stream) {
-    if (M < 0 || N <= 0 || K <= 0 || (K % 128) != 0 || (N % 16) != 0 || ldy < N ||
+                       int64_t ldy, int32_t *block_sums, void *stream, uint8_t *qn = nullptr,
+                       float *qnd = nullptr, int64_t ldqnd = 0, int qn_rot = 0) {
+    if (M < 0 || N <= 0 || K <= 0 || (K % 128) != 0 || (N % 16) != 0 || (y && ldy < N) ||
         ldws < K / 32 || (ldws % 4) != 0 || ldxd < M || (ldxd % 4) != 0 || E < 1 ||
         E > kMaxExperts)
         return H32_ERR_INVALID_ARG;
+    if (qn && ((N % 32) != 0 || !qnd || ldqnd < M || block_sums ||
+               (qn_rot != 0 && qn_rot != 1 && qn_rot != 32)))
+        return H32_ERR_INVALID_ARG;
     if (M == 0) return H32_OK;
-    if (!wp || !wsc || !xw || !xdt || !y) return H32_ERR_INVALID_ARG;
-    if (!aligned16(wp) || !aligned16(wsc) || !aligned16(xw) || !aligned16(xdt) || !aligned16(y) ||
+    if (!wp || !wsc || !xw || !xdt || (!y && !qn)) return H32_ERR_INVALID_ARG;
+    if (!aligned16(wp) || !aligned16(wsc) || !aligned16(xw) || !aligned16(xdt) ||
+        (y && !aligned16(y)) || (qn && (!aligned16(qn) || !aligned16(qnd))) ||
         (block_sums && !aligned16(block_sums)) || (expert_off && !aligned16(expert_off)) ||
-        (ldy % 4) != 0)
+        (y && (ldy % 4) != 0))
         return H32_ERR_ALIGNMENT;
     if (M > 0x7FFFFFFFll || E * N > 0x7FFFFFFFll || K > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
     int sms = 0;
@@ -706,6 +768,10 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     a.bsum = block_sums;
     a.expert_off = expert_off;
     a.ldy = ldy;
+    a.qn = qn;
+    a.qnd = qnd;
+    a.ldqnd = ldqnd;
+    a.qn_rot = qn_rot;
     a.M = static_cast<int32_t>(M);
     a.N = static_cast<int32_t>(N);
     a.nb = static_cast<int32_t>(K / 32);
@@ -715,10 +781,11 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int g = static_cast<int>(grid);
     if (xbits == 8)
-        return block_sums ? launch_tc<H32_TC_EPI_PER_QUAD, 8, true>(maps, a, g, s)
-                          : launch_tc<H32_TC_EPI_PER_QUAD, 8, false>(maps, a, g, s);
-    return block_sums ? launch_tc<H32_TC_EPI_PER_QUAD, 4, true>(maps, a, g, s)
-                      : launch_tc<H32_TC_EPI_PER_QUAD, 4, false>(maps, a, g, s);
+        return block_sums ? launch_tc<H32_TC_EPI_PER_QUAD, 8, 1>(maps, a, g, s)
+                          : launch_tc<H32_TC_EPI_PER_QUAD, 8, 0>(maps, a, g, s);
+    if (qn) return launch_tc<H32_TC_EPI_PER_QUAD, 4, 2>(maps, a, g, s);
+    return block_sums ? launch_tc<H32_TC_EPI_PER_QUAD, 4, 1>(maps, a, g, s)
+                      : launch_tc<H32_TC_EPI_PER_QUAD, 4, 0>(maps, a, g, s);
 }
 
 }  // namespace
@@ -730,6 +797,18 @@ extern "C" h32_status q4_0_x_q4_gemm_tc(const uint8_t *wp, const float *wsc, int
                                         int32_t *block_sums, void *stream) {
     return h32::run_gemm_tc(4, wp, wsc, ldws, 1, xw, xdt, ldxd, nullptr, M, N, K, y, ldy,
                             block_sums, stream);
+}
+
+extern "C" h32_status q4_0_x_q4_gemm_tc_quant_next(const uint8_t *wp, const float *wsc,
+                                                   int64_t ldws, const uint8_t *xw,
+                                                   const float *xdt, int64_t ldxd, int64_t M,
+                                                   int64_t N, int64_t K, float *y, int64_t ldy,
+                                                   uint8_t *xw_next, float *xdt_next,
+                                                   int64_t ldxd_next, int rotate_next,
+                                                   void *stream) {
+    if (!xw_next) return H32_ERR_INVALID_ARG;
+    return h32::run_gemm_tc(4, wp, wsc, ldws, 1, xw, xdt, ldxd, nullptr, M, N, K, y, ldy, nullptr,
+                            stream, xw_next, xdt_next, ldxd_next, rotate_next);
 }
 
 extern "C" h32_status q4_0_x_q8_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws,

@@ -1,0 +1,70 @@
+// The tensor-core operand form shared by the quantizers and the GEMM
+// epilogue that quantizes its own output for the next projection: rounding
+// constants and the byte encodings of integer codes as e4m3.
+#pragma once
+
+#include <stdint.h>
+
+namespace h32 {
+
+// fp32 nearest to 1/sqrt(32) (bit pattern 0x3E3504F3)
+constexpr float kInvSqrt32 = 0x1.6a09e6p-3f;
+constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;   // half of kInvSqrt32: the fp32 nearest 1/sqrt(128)
+// 1.5 * 2^23: adding it to |t| < 2^22 leaves round-half-even(t) in the low
+// mantissa bits as a two's-complement integer
+constexpr float kRoundMagic = 12582912.0f;
+
+// tensor-core form: one byte per code, the e4m3 encoding of the integer code
+__device__ __forceinline__ uint32_t byte_sign_mask(uint32_t x) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(r) : "r"(x));
+    return r;
+}
+
+// four magnitudes 0..8 (one per byte) -> their e4m3 bytes.  e4m3 (bias 7,
+// 3 mantissa bits) holds every integer up to 16 exactly: 1 = 0x38, 2 = 0x40,
+// 3 = 0x44, 4 = 0x48, 5 = 0x4A, 6 = 0x4C, 7 = 0x4E, 8 = 0x50.  A byte permute
+// looks 0..7 up in an 8-byte table; the selector nibble 8 picks table byte 0
+// (0x00) in sign-replicate mode, which stays 0x00, and 8 is then or-ed in.
+__device__ __forceinline__ uint32_t e4m3_of_magnitudes(uint32_t mag) {
+    const uint32_t sel = (mag & 0xFu) | ((mag >> 4) & 0xF0u) | ((mag >> 8) & 0xF00u) |
+                         ((mag >> 12) & 0xF000u);
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(0x44403800u), "r"(0x4E4C4A48u), "r"(sel));
+    return r | (((mag >> 3) & 0x01010101u) * 0x50u);
+}
+
+// four values 0..15 (one per byte) -> their e4m3 bytes: 0..7 from the table
+// (selector nibbles 8..15 select in sign-replicate mode and give 0x00), 8..15 are
+// 1.l2 l1 l0 x 2^3 = 0x48 + value
+__device__ __forceinline__ uint32_t e4m3_of_0_15(uint32_t v) {
+    const uint32_t sel = (v & 0xFu) | ((v >> 4) & 0xF0u) | ((v >> 8) & 0xF00u) |
+                         ((v >> 12) & 0xF000u);
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(0x44403800u), "r"(0x4E4C4A48u), "r"(sel));
+    const uint32_t big = ((v >> 3) & 0x01010101u) * 0xFFu;
+    return r | ((v + 0x48484848u) & big);
+}
+
+// four int8 codes in [-8, 8] -> four e4m3 bytes (sign bit | e4m3 of |c|)
+__device__ __forceinline__ uint32_t tc_bytes(uint32_t c) {
+    const uint32_t m = byte_sign_mask(c);                       // 0xFF where negative
+    const uint32_t mag = (c ^ m) + (m & 0x01010101u);           // |c| per byte, no carries
+    return e4m3_of_magnitudes(mag) | (m & 0x80808080u);
+}
+
+// four int8 codes c = 16 h + l (0 <= l <= 15, -8 <= h <= 7) -> the e4m3 bytes
+// of 16 h (hi) and of l (lo).  16 h is h with the exponent raised by 4: 0x20
+// added to every non-zero byte.
+__device__ __forceinline__ void tc_bytes_q8(uint32_t c, uint32_t &hi, uint32_t &lo) {
+    const uint32_t l = c & 0x0F0F0F0Fu;
+    const uint32_t hn = (c >> 4) & 0x0F0F0F0Fu;                        // h as a 4-bit pattern
+    const uint32_t hs = hn | (byte_sign_mask(hn << 4) & 0xF0F0F0F0u);  // sign-extended bytes
+    const uint32_t h8 = tc_bytes(hs);
+    const uint32_t nz = ((h8 & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) & 0x80808080u;
+    hi = h8 + (nz >> 2);
+    lo = e4m3_of_0_15(l);
+}
+
+
+}  // namespace h32

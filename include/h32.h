@@ -232,6 +232,24 @@ h32_status q4_0_x_q4_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws,
                              void *stream);
 
 /*
+ * q4_0_x_q4_gemm_tc with its output also quantized, in the same kernel, for the
+ * next projection (a fused producer: the output never makes an extra HBM round
+ * trip before the next projection's activation quantizer).  The rows of the
+ * output (the next projection's K dimension) are cut into 32-blocks; each is
+ * rotated (rotate_next = 1 or 32) or not (0) and quantized exactly as
+ * h32_quantize_act_q4_tc would quantize the fp32 output y, bit for bit.
+ *   y          [M][ldy] fp32 out, or null (then only the quantized form is written)
+ *   xw_next    [M][N] out: tc-form codes of y, as h32_quantize_act_q4_tc's xw
+ *   xdt_next   [N/32][ldxd_next] out: fp32 scales, ldxd_next >= M
+ * Requires N % 32 == 0 (and the conditions of q4_0_x_q4_gemm_tc).
+ */
+h32_status q4_0_x_q4_gemm_tc_quant_next(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                        const uint8_t *xw, const float *xdt, int64_t ldxd,
+                                        int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
+                                        uint8_t *xw_next, float *xdt_next, int64_t ldxd_next,
+                                        int rotate_next, void *stream);
+
+/*
  * The W4A8 product of q4_0_x_q8_gemm on tc-form operands (weights from
  * h32_prepack_weights_q4_0_tc, activations from h32_quantize_act_q8_tc):
  * S = sum w (16 h) + sum w l per block (two MMAs into one accumulator, every

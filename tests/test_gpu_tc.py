@@ -402,3 +402,53 @@ def test_gemm_q8_tc_pp512_sampled(h32):
     ni = np.concatenate([r.integers(0, p.N, 3000), [p.N - 1]])
     r32, _, _ = oracle.gemm_sampled(wq, wd, xq, xd, p.K, mi, ni)
     assert np.array_equal(y[mi, ni].view(np.uint32), r32.view(np.uint32))
+
+
+# --------------------------------------------------------------------------
+# the fused producer: the product quantized for the next projection in the
+# GEMM's own epilogue
+# --------------------------------------------------------------------------
+def test_gemm_tc_quant_next_pp512_sampled_rows(h32):
+    """The attention projection at pp512 (512 x 5120 x 5120): 8 whole token rows
+    of the next projection's input against the oracle's quantizer applied to
+    the oracle's output rows."""
+    import torch
+    p = wl.ATTN
+    x = p.activations(512, 0, wl.CFG_ATTN)
+    w = p.weights(0, wl.CFG_ATTN)
+    (wq, wd, xq, xd), (wp, wsc, xw, xdt) = _tc_operands(h32, x, w)
+    _, xn, xnd = h32.q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=512, want_y=False)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    rows = np.array([0, 1, 77, 200, 311, 400, 510, 511])
+    mi = np.repeat(rows, p.N)
+    ni = np.tile(np.arange(p.N), rows.size)
+    r32, _, _ = oracle.gemm_sampled(wq, wd, xq, xd, p.K, mi, ni)
+    nq, nd = oracle.quantize_act_q4(r32.reshape(rows.size, p.N))
+    assert np.array_equal(e4m3_value(np_of(xn)[rows]),
+                          oracle.decode_act4(nq, p.N).astype(np.float64))
+    assert np.array_equal(np_of(xnd)[:, rows].T.view(np.uint32), nd.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,N,K,rot", [(70, 160, 256, True), (17, 96, 128, False),
+                                       (130, 256, 512, True)])
+def test_gemm_tc_quant_next_matches_oracle(h32, M, N, K, rot):
+    import torch
+    x = wl.f32_to_bf16_bits(wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, 290 + M))
+    w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, 291 + N)
+    (wq, wd, xq, xd), (wp, wsc, xw, xdt) = _tc_operands(h32, x, w)
+    y, xn, xnd = h32.q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=M, rotate_next=rot)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r32, _, _ = oracle.gemm(wq, wd, xq, xd, K)
+    assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
+    # the next projection's input: the oracle's quantizer on the oracle's output
+    nq, nd = oracle.quantize_act_q4(r32, rot)
+    assert np.array_equal(e4m3_value(np_of(xn)), oracle.decode_act4(nq, N).astype(np.float64))
+    assert np.array_equal(np_of(xnd)[:, :M].T.view(np.uint32), nd.view(np.uint32))
+    # without y: the same codes
+    y2, xn2, xnd2 = h32.q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=M, want_y=False,
+                                                      rotate_next=rot)
+    torch.cuda.synchronize()
+    assert y2 is None
+    assert np.array_equal(np_of(xn2), np_of(xn)) and np.array_equal(np_of(xnd2), np_of(xnd))

@@ -133,3 +133,17 @@ def test_rotation_size_validated(lib):
                  s) == h32.H32_ERR_INVALID_ARG
     assert _call("h32_quantize_act_q4_tc", p, 1, 8, 64, 64, p, p, 8, 128, s) == h32.H32_ERR_INVALID_ARG
     assert _call("h32_quantize_act_q4", p, 1, 0, 128, 128, p, p, 128, s) == h32.H32_OK
+
+
+def test_quant_next_bad_arguments(lib):
+    p = ctypes.c_void_p(256)
+    s = ctypes.c_void_p(0)
+    # N not a multiple of 32; no next codes; bad rotation; ldxd_next < M
+    assert _call("q4_0_x_q4_gemm_tc_quant_next", p, p, 4, p, p, 8, 8, 48, 128, p, 48, p, p, 8, 1,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc_quant_next", p, p, 4, p, p, 8, 8, 64, 128, p, 64, None, p, 8, 1,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc_quant_next", p, p, 4, p, p, 8, 8, 64, 128, p, 64, p, p, 8, 64,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc_quant_next", p, p, 4, p, p, 8, 8, 64, 128, None, 64, p, p, 4, 1,
+                 s) == h32.H32_ERR_INVALID_ARG

@@ -452,3 +452,43 @@ def test_gemm_tc_quant_next_matches_oracle(h32, M, N, K, rot):
     torch.cuda.synchronize()
     assert y2 is None
     assert np.array_equal(np_of(xn2), np_of(xn)) and np.array_equal(np_of(xnd2), np_of(xnd))
+
+
+def test_gemm_tc_long_prompt_microbatch_sampled(h32):
+    """The long-prompt sweep's micro-batch: 1024 tokens through FFN gate/up
+    (1024 x 34816 x 5120), sampled outputs against the oracle."""
+    import torch
+    p = wl.LONG_GATE_UP
+    x = p.activations(1024, 0, wl.CFG_LONG)
+    w = p.weights(0, wl.CFG_LONG)
+    (wq, wd, xq, xd), (wp, wsc, xw, xdt) = _tc_operands(h32, x, w)
+    y = np_of(h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=1024))
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r = np.random.default_rng(8)
+    mi = np.concatenate([r.integers(0, 1024, 3000), [1023, 0]])
+    ni = np.concatenate([r.integers(0, p.N, 3000), [p.N - 1, 0]])
+    r32, _, _ = oracle.gemm_sampled(wq, wd, xq, xd, p.K, mi, ni)
+    assert np.array_equal(y[mi, ni].view(np.uint32), r32.view(np.uint32))
+
+
+def test_gemm_tc_output_pitch_and_zero_rows(h32):
+    """y written into a wider buffer (ldy > N) leaves the padding untouched; M = 0
+    is a no-op."""
+    import torch
+    M, N, K = 33, 96, 256
+    x = wl.f32_to_bf16_bits(wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, 310))
+    w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, 311)
+    (wq, wd, xq, xd), (wp, wsc, xw, xdt) = _tc_operands(h32, x, w)
+    big = torch.full((M, N + 32), 7.0, dtype=torch.float32, device="cuda")
+    h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M, y=big[:, :N])
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r32, _, _ = oracle.gemm(wq, wd, xq, xd, K)
+    got = np_of(big)
+    assert np.array_equal(got[:, :N].view(np.uint32), r32.view(np.uint32))
+    assert np.all(got[:, N:] == 7.0)
+    y0 = torch.empty((0, N), dtype=torch.float32, device="cuda")
+    h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=0, y=y0)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0

@@ -98,13 +98,8 @@ struct Cfg {
     // tile's 16-column chunks)
     static constexpr int kEpiPerQuad = (XB == 4) ? H32_Q4_EPI_PER_QUAD : 2;
     static constexpr int kEpiWarps = 4 * kEpiPerQuad;
-    static constexpr int kEpiThreads = kEpiWarps * 32;
     static constexpr int kMaxChunks = (8 + kEpiPerQuad - 1) / kEpiPerQuad;  // 16-column chunks
     static constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
-    // the register file (64K) is granted per 128-thread group of warps
-    static constexpr int kMaxRegs = (65536 / ((kThreads + 127) / 128 * 128)) & ~7;
-    // two TMEM loads in flight per wait when the registers allow it
-    static constexpr bool kPairLoads = kMaxChunks <= 3;
     // shared memory map (offsets from a 1024-aligned base)
     static constexpr int kOffNib = 0;
     static constexpr int kOffA = kOffNib + kNibStages * kNibBytes;

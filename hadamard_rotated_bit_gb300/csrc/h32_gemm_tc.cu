@@ -680,7 +680,9 @@ int choose_bn_tc(int64_t M, int64_t N, int sms) {
             for (int64_t t = c; t < tiles; t += grid) {
                 const int64_t ch = t % chunks;
                 const int64_t rows = (ch == chunks - 1) ? M - ch * bn : bn;
-                cost += ((rows + 15) / 16) * 16 + 24;
+                // a tile costs its MMA width plus a fixed part that, measured on
+                // GB300, is about the work of 64 more columns
+                cost += ((rows + 15) / 16) * 16 + 64;
             }
             if (cost > worst) worst = cost;
         }
@@ -784,8 +786,14 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
         return block_sums ? launch_tc<H32_TC_EPI_PER_QUAD, 8, 1>(maps, a, g, s)
                           : launch_tc<H32_TC_EPI_PER_QUAD, 8, 0>(maps, a, g, s);
     if (qn) return launch_tc<H32_TC_EPI_PER_QUAD, 4, 2>(maps, a, g, s);
-    return block_sums ? launch_tc<H32_TC_EPI_PER_QUAD, 4, 1>(maps, a, g, s)
-                      : launch_tc<H32_TC_EPI_PER_QUAD, 4, 0>(maps, a, g, s);
+    if (block_sums) return launch_tc<H32_TC_EPI_PER_QUAD, 4, 1>(maps, a, g, s);
+    // the tile's 16-column chunks in even shares: 12 epilogue warps (3 per lane
+    // quarter) when 16 would leave one warp with twice the others' chunks
+    // (5 or 6 chunks: measured 5-8% faster on the pp512 attention and FFN-down
+    // shapes), 16 otherwise
+    const int n16 = bn / 16;
+    if (n16 % 4 == 1 || n16 % 4 == 2) return launch_tc<3, 4, 0>(maps, a, g, s);
+    return launch_tc<H32_TC_EPI_PER_QUAD, 4, 0>(maps, a, g, s);
 }
 
 }  // namespace

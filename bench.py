@@ -805,6 +805,18 @@ def suite_quant_stream(torch, h32, dev, stream, steps, warmup, peaks):
         out.append({"suite": f"quantize_q{bits}_stream_16384x17408_bf16", "value": round(gbs, 1),
                     "unit": "GB/s", "ms_per_call": round(ms, 4),
                     "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_call": nbytes})
+    # the tensor-core form: one byte (4-bit) or two bytes (8-bit) per code,
+    # scales block-major
+    for bits in (4, 8):
+        xw = torch.empty((M, K * (bits // 4)), dtype=torch.uint8, device=dev)
+        xdt = torch.zeros((K // 32, M), dtype=torch.float32, device=dev)
+        fn = h32.h32_quantize_act_q4_tc if bits == 4 else h32.h32_quantize_act_q8_tc
+        ms = _events_time(torch, lambda: fn(x, xw=xw, xdt=xdt, stream=stream), steps, warmup, stream)
+        nbytes = M * K * 2 + xw.numel() + xdt.numel() * 4
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out.append({"suite": f"quantize_q{bits}_tc_stream_16384x17408_bf16", "value": round(gbs, 1),
+                    "unit": "GB/s", "ms_per_call": round(ms, 4),
+                    "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_call": nbytes})
     return out
 
 

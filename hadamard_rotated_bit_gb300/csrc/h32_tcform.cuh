@@ -67,4 +67,14 @@ __device__ __forceinline__ void tc_bytes_q8(uint32_t c, uint32_t &hi, uint32_t &
 }
 
 
+// four integer-valued floats (each exactly representable in e4m3: |c| <= 16,
+// or a multiple of 16 up to 128) -> their e4m3 bytes, c0 in the lowest byte.
+// The hardware conversion is exact for such values.
+__device__ __forceinline__ uint32_t e4m3x4_of_ints(float c0, float c1, float c2, float c3) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(c1), "f"(c0));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(c3), "f"(c2));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
 }  // namespace h32

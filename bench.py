@@ -558,6 +558,48 @@ def run_only_gemm(args):
             "steps": args.steps, "warmup": args.warmup}
 
 
+def run_only_quant(args):
+    """The activation quantizer alone, streaming a 16384 x 17408 bf16 matrix
+    (`warmup + steps` launches, CUDA events)."""
+    import torch
+    import hadamard_rotated_bit_gb300 as h32
+    from hadamard_rotated_bit_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", 0)
+    M, K = 16384, 17408
+    g = torch.Generator(device=dev).manual_seed(0)
+    x = torch.randn((M, K), device=dev, generator=g).to(torch.bfloat16)
+    kind = args.only_quant
+    if kind in ("q4", "q8"):
+        out = torch.empty((M, K // 2 if kind == "q4" else K), dtype=torch.uint8, device=dev)
+        sc = torch.empty((M, K // 32), dtype=torch.float32, device=dev)
+        fn = h32.h32_quantize_act_q4 if kind == "q4" else h32.h32_quantize_act_q8
+
+        def call():
+            fn(x, xq=out, xd=sc)
+    else:
+        out = torch.empty((M, K * (1 if kind == "q4_tc" else 2)), dtype=torch.uint8, device=dev)
+        sc = torch.zeros((K // 32, M), dtype=torch.float32, device=dev)
+        fn = h32.h32_quantize_act_q4_tc if kind == "q4_tc" else h32.h32_quantize_act_q8_tc
+
+        def call():
+            fn(x, xw=out, xdt=sc)
+    for _ in range(args.warmup):
+        call()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record()
+    for _ in range(args.steps):
+        call()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    nbytes = M * K * 2 + out.numel() + sc.numel() * 4
+    return {"only_quant": kind, "ms_per_launch": round(ms, 5),
+            "GBps": round(nbytes / (ms / 1e3) / 1e9, 1), "bytes_per_launch": nbytes,
+            "steps": args.steps, "warmup": args.warmup}
+
+
 # --------------------------------------------------------------------------
 # --suite: the other configurations of the path (one JSON line each)
 # --------------------------------------------------------------------------
@@ -857,6 +899,9 @@ def main(argv=None):
                          "long prompts, streaming quantizer), one JSON line each")
     ap.add_argument("--only-gemm", choices=[p.name for p in CHAIN], default=None,
                     help="time one projection's GEMM alone (a small case for profilers)")
+    ap.add_argument("--only-quant", choices=["q4", "q8", "q4_tc", "q8_tc"], default=None,
+                    help="time the activation quantizer alone on a 16384 x 17408 bf16 matrix "
+                         "(a streaming case for profilers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -866,6 +911,8 @@ def main(argv=None):
         return
     if args.only_gemm:
         line = run_only_gemm(args)
+    elif args.only_quant:
+        line = run_only_quant(args)
     elif args.impl == "reference":
         line = run_reference(args)
     else:

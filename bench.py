@@ -51,7 +51,7 @@ PROFILE_SUMMARY = {"tc": os.path.join(ROOT, "profiles", "gemm_tc_w4a4_pp512_ffn_
 # the sources a GEMM kernel is compiled from (the profile's traffic is only
 # reported while they are unchanged)
 GEMM_SOURCES = {"tc": [os.path.join(_CSRC, f) for f in ("h32_gemm_tc.cu", "h32_common.cuh",
-                                                        "h32_epilogue.cuh")],
+                                                        "h32_epilogue.cuh", "h32_tcform.cuh")],
                 "q4_0": [os.path.join(_CSRC, f) for f in ("h32_gemm.cu", "h32_common.cuh",
                                                           "h32_epilogue.cuh")]}
 SMS = 152

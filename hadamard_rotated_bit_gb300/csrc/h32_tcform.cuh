@@ -34,18 +34,6 @@ __device__ __forceinline__ uint32_t e4m3_of_magnitudes(uint32_t mag) {
     return r | (((mag >> 3) & 0x01010101u) * 0x50u);
 }
 
-// four values 0..15 (one per byte) -> their e4m3 bytes: 0..7 from the table
-// (selector nibbles 8..15 select in sign-replicate mode and give 0x00), 8..15 are
-// 1.l2 l1 l0 x 2^3 = 0x48 + value
-__device__ __forceinline__ uint32_t e4m3_of_0_15(uint32_t v) {
-    const uint32_t sel = (v & 0xFu) | ((v >> 4) & 0xF0u) | ((v >> 8) & 0xF00u) |
-                         ((v >> 12) & 0xF000u);
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(0x44403800u), "r"(0x4E4C4A48u), "r"(sel));
-    const uint32_t big = ((v >> 3) & 0x01010101u) * 0xFFu;
-    return r | ((v + 0x48484848u) & big);
-}
-
 // four int8 codes in [-8, 8] -> four e4m3 bytes (sign bit | e4m3 of |c|)
 __device__ __forceinline__ uint32_t tc_bytes(uint32_t c) {
     const uint32_t m = byte_sign_mask(c);                       // 0xFF where negative
@@ -53,17 +41,28 @@ __device__ __forceinline__ uint32_t tc_bytes(uint32_t c) {
     return e4m3_of_magnitudes(mag) | (m & 0x80808080u);
 }
 
+// Sixteen-entry byte table lookup: each byte v (0..15) of `v` -> byte v of the
+// table t0..t3 (t0 holding entries 0..3 from its low byte up).  Two byte
+// permutes look up v & 7 in each half of the table; bit 3 of v picks the half.
+__device__ __forceinline__ uint32_t lut16(uint32_t v, uint32_t t0, uint32_t t1, uint32_t t2,
+                                          uint32_t t3) {
+    const uint32_t s = v & 0x07070707u;
+    uint32_t sel, a, b;
+    asm("prmt.b32 %0, %1, 0, 0x4420;" : "=r"(sel) : "r"(s | (s >> 4)));   // 4 nibbles
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(a) : "r"(t0), "r"(t1), "r"(sel));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(b) : "r"(t2), "r"(t3), "r"(sel));
+    const uint32_t m = byte_sign_mask(v << 4);                               // 0xFF where v >= 8
+    return (a & ~m) | (b & m);
+}
+
 // four int8 codes c = 16 h + l (0 <= l <= 15, -8 <= h <= 7) -> the e4m3 bytes
-// of 16 h (hi) and of l (lo).  16 h is h with the exponent raised by 4: 0x20
-// added to every non-zero byte.
+// of 16 h (hi) and of l (lo), by table: l = 0..7 as in e4m3_of_magnitudes,
+// 8..15 = 0x50..0x57; 16 h for the 4-bit pattern of h = 0..7: 0x00, 0x58, 0x60,
+// 0x64, 0x68, 0x6A, 0x6C, 0x6E, and for h = -8..-1: 0xF0, 0xEE, 0xEC, 0xEA, 0xE8,
+// 0xE4, 0xE0, 0xD8.
 __device__ __forceinline__ void tc_bytes_q8(uint32_t c, uint32_t &hi, uint32_t &lo) {
-    const uint32_t l = c & 0x0F0F0F0Fu;
-    const uint32_t hn = (c >> 4) & 0x0F0F0F0Fu;                        // h as a 4-bit pattern
-    const uint32_t hs = hn | (byte_sign_mask(hn << 4) & 0xF0F0F0F0u);  // sign-extended bytes
-    const uint32_t h8 = tc_bytes(hs);
-    const uint32_t nz = ((h8 & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) & 0x80808080u;
-    hi = h8 + (nz >> 2);
-    lo = e4m3_of_0_15(l);
+    lo = lut16(c & 0x0F0F0F0Fu, 0x44403800u, 0x4E4C4A48u, 0x53525150u, 0x57565554u);
+    hi = lut16((c >> 4) & 0x0F0F0F0Fu, 0x64605800u, 0x6E6C6A68u, 0xEAECEEF0u, 0xD8E0E4E8u);
 }
 
 

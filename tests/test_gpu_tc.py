@@ -492,3 +492,22 @@ def test_gemm_tc_output_pitch_and_zero_rows(h32):
     h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=0, y=y0)
     torch.cuda.synchronize()
     assert h32.h32_device_status() == 0
+
+
+def test_gemm_tc_many_tiles_per_cta_sampled(h32):
+    """8192 tokens through the 5120x5120 projection in one call: every CTA of
+    the persistent grid walks many tiles, so the stage and TMEM-buffer rings
+    wrap many times; sampled outputs against the oracle, bit for bit."""
+    import torch
+    p = wl.ATTN
+    x = p.activations(8192, 3, wl.CFG_ATTN)
+    w = p.weights(0, wl.CFG_ATTN)
+    (wq, wd, xq, xd), (wp, wsc, xw, xdt) = _tc_operands(h32, x, w)
+    y = np_of(h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=8192))
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r = np.random.default_rng(9)
+    mi = np.concatenate([r.integers(0, 8192, 4000), [8191, 0]])
+    ni = np.concatenate([r.integers(0, p.N, 4000), [p.N - 1, 0]])
+    r32, _, _ = oracle.gemm_sampled(wq, wd, xq, xd, p.K, mi, ni)
+    assert np.array_equal(y[mi, ni].view(np.uint32), r32.view(np.uint32))

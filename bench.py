@@ -56,6 +56,9 @@ GEMM_SOURCES = {"tc": [os.path.join(_CSRC, f) for f in ("h32_gemm_tc.cu", "h32_c
                                                           "h32_epilogue.cuh")]}
 SMS = 152
 FP32_LANES_PER_SM = 128   # FP32 FMA/FMUL lanes per SM per clock
+# measured on GB300: interleaved mul.f32x2 / fma.f32x2 issue at 0.89 packed operations per
+# clock per sub-partition, 57 fp32 lane operations, 1.78x the 32 lanes of the unit count
+FP32_MIX_OVER_UNITS = 1.78
 
 
 # --------------------------------------------------------------------------
@@ -341,7 +344,8 @@ def run_gpu(args):
                     "peak_source": f"{SMS} SMs x {FP32_LANES_PER_SM} FP32 lanes x "
                                    f"{clock_mhz:.0f} MHz ({peak_src} max SM clock)",
                     "algorithmic_per_launch": alg["gemm_alu_ops"],
-                    "ms_per_launch": round(per_kernel[dom], 5)}
+                    "ms_per_launch": round(per_kernel[dom], 5),
+                    "frac_of_measured_fp32_mix": round(achieved / (alu_peak * FP32_MIX_OVER_UNITS), 4)}
     else:
         achieved = alg["quant_bytes"] / (per_kernel[dom] / 1e3) / 1e9
         roofline = {"kernel": names[dom], "bound": "hbm", "achieved": round(achieved, 1),

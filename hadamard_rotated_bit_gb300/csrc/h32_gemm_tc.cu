@@ -19,9 +19,12 @@
 //               (128 rows x 4 blocks) and the token scales (4 blocks x tokens)
 //   warp 1      TMEM allocator and MMA issuer: one K=32 MMA per block into one
 //               of four 128-column TMEM slots; a commit per two blocks
-//   warps 2..   epilogue (16 warps, four per TMEM lane quarter, each a
-//               quarter of the tile's columns): tcgen05.ld each block's S, fold
-//               the scales in with packed fp32 operations, store rows of y
+//   warps 2, 3  idle (with 16 epilogue warps: they complete the producers'
+//               warpgroup, which hands its registers to the epilogue)
+//   the rest    epilogue (16 warps, four per TMEM lane quarter, each a
+//               quarter of the tile's columns; or 12 warps, three per quarter):
+//               tcgen05.ld each block's S, fold the scales in with packed fp32
+//               operations, store rows of y
 // The MMA and the epilogue hand off two blocks per synchronization; measured
 // on GB300, one block per hand-off (four buffers) is slower, as every hand-off
 // puts all epilogue warps in step.  Every wait is bounded.
@@ -71,7 +74,17 @@ struct TcCfg {
     static constexpr int kStages = XB == 8 ? 4 : 5;
     static constexpr int kBTile = XB == 8 ? 2 * kTileBytes : kTileBytes;   // activations per stage
     static constexpr int kEpiWarps = 4 * EPQ;
-    static constexpr int kThreads = (2 + kEpiWarps) * 32;
+    // With 16 epilogue warps the producers form a warpgroup of their own (TMA,
+    // MMA and two idle warps) that hands registers to the epilogue
+    // (setmaxnreg): 96 a thread at launch, then 32 for the producer warpgroup
+    // and 112 for the epilogue, 4 x 32 x 32 + 16 x 32 x 112 = 640 x 96.
+    static constexpr bool kRegSplit = EPQ == 4;
+    static constexpr int kProdWarps = kRegSplit ? 4 : 2;
+    static constexpr int kThreads = (kProdWarps + kEpiWarps) * 32;
+    static constexpr int kLaunchRegs = 96, kProdRegs = 32, kEpiRegs = 112;
+    static_assert(!kRegSplit || (kProdWarps * kProdRegs + kEpiWarps * kEpiRegs) * 32 <=
+                                    kThreads * kLaunchRegs,
+                  "register split above the launch's registers");
     static constexpr int kMaxChunks = (8 + EPQ - 1) / EPQ;  // 16-column chunks per warp
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kTileBytes;
@@ -131,6 +144,16 @@ __device__ __forceinline__ uint32_t quant_lane_block(float v, int lane, bool rot
 }
 
 __device__ __forceinline__ void record(uint32_t bits) { atomicOr(&g_tc_status, bits); }
+
+// per-warpgroup register budgets (every warp of the warpgroup executes the same one)
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 __device__ __forceinline__ void set_abort(volatile int *misc) {
     misc[kMiscAbort] = 1;
@@ -213,7 +236,7 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
                                                const float *s_sb, uint32_t tmem, int warp, int lane,
                                                volatile int *abort_flag) {
     using C = TcCfg<EPQ, XB>;
-    const int ew = warp - 2;
+    const int ew = warp - C::kProdWarps;
     const int quad = warp & 3;                 // TMEM lanes 32 quad .. 32 quad + 31
     const int part = ew >> 2;                  // share of the columns
     const int row = quad * 32 + lane;
@@ -241,18 +264,19 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
                 if (!warp_wait(&bars[kBarSFull + gb], gph, lim, abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t tcol0 = tcol_base + gb * (kGroup * 128);
-                // each chunk of every block of the group under one TMEM wait;
-                // every accumulator still takes the blocks in order
+                // one 16-column chunk of one block per TMEM wait (measured: fewer
+                // live load registers beat fewer waits); every accumulator takes
+                // the blocks in order
 #pragma unroll
                 for (int c = 0; c < C::kMaxChunks; ++c) {
                     if (c < nch) {
-                        uint32_t v[kGroup][16];
 #pragma unroll
-                        for (int i = 0; i < kGroup; ++i) tmem_ld_x16(tcol0 + i * 128 + c * 16, v[i]);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < kGroup; ++i)
-                            fold16(acc + 8 * c, dws[j0 + i], sb + (j0 + i) * a.bn + 16 * c, v[i]);
+                        for (int i = 0; i < kGroup; ++i) {
+                            uint32_t v[16];
+                            tmem_ld_x16(tcol0 + i * 128 + c * 16, v);
+                            tmem_ld_wait();
+                            fold16(acc + 8 * c, dws[j0 + i], sb + (j0 + i) * a.bn + 16 * c, v);
+                        }
                     }
                 }
                 // the warp-wide wait above: every lane's TMEM reads of the buffer are done
@@ -419,6 +443,7 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
+        if constexpr (C::kRegSplit) reg_dealloc<C::kProdRegs>();
         if (lane == 0) {
             prefetch_tmap(&map_a);
             prefetch_tmap(&map_b);
@@ -457,6 +482,7 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
+        if constexpr (C::kRegSplit) reg_dealloc<C::kProdRegs>();
         if (lane == 0) {
             uint32_t ks = 0, kg = 0;
             bool ok = true;
@@ -508,15 +534,20 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
             mma_commit(&bars[kBarDrain]);
             mbar_wait_bounded(&bars[kBarDrain], 0, kDrainPolls, nullptr);
         }
+    } else if (warp < C::kProdWarps) {
+        // the producer warpgroup's two idle warps
+        if constexpr (C::kRegSplit) reg_dealloc<C::kProdRegs>();
     } else if constexpr (!kSums) {
         // ------------------------------------------------------- epilogue
+        if constexpr (C::kRegSplit) reg_alloc<C::kEpiRegs>();
         if (!epilogue_tiles<EPQ, XB, kEpi == 2>(a, total, s_off, s_tpre, bars, s_sa, s_sb, tmem,
                                                 warp, lane,
                                      abort_flag))
             set_abort(misc);
     } else {
         // ------------------------------------ epilogue with block sums
-        const int ew = warp - 2;
+        if constexpr (C::kRegSplit) reg_alloc<C::kEpiRegs>();
+        const int ew = warp - C::kProdWarps;
         const int quad = warp & 3;                 // TMEM lanes 32*quad .. +31
         const int part = ew >> 2;                  // share of the columns
         const int row = quad * 32 + lane;
@@ -700,6 +731,21 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
     const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return launch_status(e);
+    if constexpr (C::kRegSplit) {
+        // the epilogue's setmaxnreg.inc waits until the pool holds its registers:
+        // never launch with fewer registers a thread than the split assumes
+        static int regs = -1;
+        if (regs < 0) {
+            cudaFuncAttributes fa{};
+            const cudaError_t ea = cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi>);
+            if (ea != cudaSuccess) return launch_status(ea);
+            regs = fa.numRegs;
+        }
+        if (((regs + 7) / 8) * 8 < C::kLaunchRegs) {
+            note_error("tc GEMM compiled with fewer registers than its warpgroup split needs");
+            return H32_ERR_UNSUPPORTED;
+        }
+    }
     gemm_tc_kernel<EPQ, XB, kEpi><<<grid, C::kThreads, C::kSmem, s>>>(maps[0], maps[1], maps[2],
                                                                         maps[3], a);
     return launch_status(cudaGetLastError());

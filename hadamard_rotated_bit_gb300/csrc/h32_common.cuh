@@ -38,6 +38,26 @@ h32_status tc_read_and_clear_status(cudaStream_t s);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+#if defined(__CUDACC__)
+// launch `kernel` so that it may overlap the tail of the previous kernel of the
+// stream (programmatic dependent launch; the kernel calls pdl_wait() first)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+#endif
+
 #define H32_TRY(expr)                  \
     do {                               \
         h32_status _st = (expr);       \
@@ -49,6 +69,18 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// programmatic dependent launch ---------------------------------------------
+// A kernel launched with the programmatic-serialization attribute may start
+// while the previous kernel of its stream is still finishing; it must not touch
+// global memory (read or write) before pdl_wait(), which returns once that
+// kernel has completed and its writes are visible.  pdl_trigger() lets the next
+// kernel of the stream start early in the same way.  Both are no-ops for a
+// kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // mbarrier ------------------------------------------------------------------

@@ -382,6 +382,10 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
         misc[kMiscBad] = 0;
         fence_barrier_init();
     }
+    // the previous kernel of the stream (launched ahead of this one) is done
+    // before anything here touches global memory
+    pdl_wait();
+    pdl_trigger();
     // group offsets: checked (0 = off[0] <= ... <= off[E] = M), then the tile
     // prefix over the groups (warp 0)
     if (a.expert_off == nullptr) {
@@ -746,9 +750,9 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
             return H32_ERR_UNSUPPORTED;
         }
     }
-    gemm_tc_kernel<EPQ, XB, kEpi><<<grid, C::kThreads, C::kSmem, s>>>(maps[0], maps[1], maps[2],
-                                                                        maps[3], a);
-    return launch_status(cudaGetLastError());
+    const cudaError_t el = launch_pdl(gemm_tc_kernel<EPQ, XB, kEpi>, dim3(grid), dim3(C::kThreads),
+                                      C::kSmem, s, maps[0], maps[1], maps[2], maps[3], a);
+    return launch_status(el != cudaSuccess ? el : cudaGetLastError());
 }
 
 }  // namespace

@@ -273,6 +273,8 @@ __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restric
     // block column land in one 16-byte run of the block-major scale array, and
     // the kRot/32 blocks of a kRot-block sit in adjacent lanes (kRot/32 divides 8).
     (void)nblk;
+    pdl_wait();
+    pdl_trigger();
     const uint32_t nb = K / 32;
     const uint32_t tiles_b = (nb + 7) / 8, ntiles = ((M + 3) / 4) * tiles_b;
     const uint32_t lane = threadIdx.x & 31;
@@ -517,9 +519,9 @@ h32_status quantize_act_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
     const int grid = grid_for_tc(nblk, sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint32_t m32 = static_cast<uint32_t>(M), k32 = static_cast<uint32_t>(K);
-#define H32_QTC(BF, ROT, GA)                                                                     \
-    quant_act_tc_kernel<BF, kBits, ROT, GA><<<grid, 256, 0, s>>>(x, nblk, m32, k32, ldx, row_idx, \
-                                                                 T, xw, xdt, ldxd)
+#define H32_QTC(BF, ROT, GA)                                                                  \
+    e = launch_pdl(quant_act_tc_kernel<BF, kBits, ROT, GA>, dim3(grid), dim3(256), 0, s, x, nblk, \
+                   m32, k32, ldx, row_idx, T, xw, xdt, ldxd)
 #define H32_QTC_R(ROT)                    \
     do {                                  \
         if (bf && ga) H32_QTC(true, ROT, true);   \
@@ -528,6 +530,7 @@ h32_status quantize_act_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
         else H32_QTC(false, ROT, false);          \
     } while (0)
     const bool bf = dt == H32_IN_BF16, ga = row_idx != nullptr;
+    cudaError_t e = cudaSuccess;
     switch (rot_points(rotate)) {
         case 0: H32_QTC_R(0); break;
         case 32: H32_QTC_R(32); break;
@@ -536,7 +539,7 @@ h32_status quantize_act_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
     }
 #undef H32_QTC_R
 #undef H32_QTC
-    return launch_status(cudaGetLastError());
+    return launch_status(e != cudaSuccess ? e : cudaGetLastError());
 }
 }  // namespace
 }  // namespace h32

@@ -738,14 +738,14 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
     if constexpr (C::kRegSplit) {
         // the epilogue's setmaxnreg.inc waits until the pool holds its registers:
         // never launch with fewer registers a thread than the split assumes
-        static int regs = -1;
-        if (regs < 0) {
+        // (read once per kernel; a failed read leaves -1 and refuses every launch)
+        static const int regs = [] {
             cudaFuncAttributes fa{};
-            const cudaError_t ea = cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi>);
-            if (ea != cudaSuccess) return launch_status(ea);
-            regs = fa.numRegs;
-        }
-        if (((regs + 7) / 8) * 8 < C::kLaunchRegs) {
+            return cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi>) == cudaSuccess
+                       ? fa.numRegs
+                       : -1;
+        }();
+        if (regs < 0 || ((regs + 7) / 8) * 8 < C::kLaunchRegs) {
             note_error("tc GEMM compiled with fewer registers than its warpgroup split needs");
             return H32_ERR_UNSUPPORTED;
         }

@@ -511,3 +511,32 @@ def test_gemm_tc_many_tiles_per_cta_sampled(h32):
     ni = np.concatenate([r.integers(0, p.N, 4000), [p.N - 1, 0]])
     r32, _, _ = oracle.gemm_sampled(wq, wd, xq, xd, p.K, mi, ni)
     assert np.array_equal(y[mi, ni].view(np.uint32), r32.view(np.uint32))
+
+
+def test_back_to_back_launches_reuse_buffers(h32):
+    """Quantize, GEMM, quantize again into the same activation buffers, GEMM
+    again, eight rounds on one stream with no host synchronization: each kernel
+    may start under its predecessor's tail, so this fails if a kernel touched
+    memory before its predecessor finished (the second quantizer overwriting
+    codes the first GEMM still reads, or a GEMM reading codes not yet written)."""
+    import torch
+    M, N, K = 256, 1024, 2048
+    w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, 330)
+    wq, wd = oracle.quantize_weights_q4_0(w)
+    wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(wq), torch_of(wd.view(np.int16)))
+    xs = [wl.f32_to_bf16_bits(wl.act_normal_outliers(M, K, 0.01, 20.0, r, wl.CFG_TEST, 331))
+          for r in range(8)]
+    xdev = [torch_bf16(x) for x in xs]
+    xw = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    xdt = torch.zeros((K // 32, M), dtype=torch.float32, device="cuda")
+    ys = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in xs]
+    torch.cuda.synchronize()
+    for x, y in zip(xdev, ys):
+        h32.h32_quantize_act_q4_tc(x, xw=xw, xdt=xdt)
+        h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M, y=y)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    for x, y in zip(xs, ys):
+        xq, xd = oracle.quantize_act_q4(x)
+        r32, _, _ = oracle.gemm(wq, wd, xq, xd, K)
+        assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))

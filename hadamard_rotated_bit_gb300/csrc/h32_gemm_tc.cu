@@ -41,7 +41,10 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdint>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "h32_common.cuh"
 #include "h32_epilogue.cuh"
@@ -115,6 +118,9 @@ struct TcArgs {
     int64_t ldy, ldqnd;
     int32_t M, N, nb, bn, E;     // M: activation rows (all groups)
     int32_t qn_rot;              // 0 or 32: rotate the next projection's 32-blocks
+    // dense only: tiles from tail_first on (the last partial wave) are each cut
+    // into tail_k pieces along the tokens; tail_k = 1 cuts nothing
+    int32_t tail_first, tail_k;
     uint64_t wait_limit;
 };
 
@@ -204,8 +210,17 @@ __device__ __forceinline__ int group_chunks(const int *s_off, int e, int bn) {
     return hi > lo ? (hi - (lo & ~3) + bn - 1) / bn : 0;
 }
 
+template <bool kTail>
 __device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a, const int *s_off,
                                           const int *s_tpre) {
+    int sub = -1;   // the piece of a cut tail tile, or -1
+    if constexpr (kTail) {
+        if (t >= a.tail_first) {
+            const int p = t - a.tail_first;
+            t = a.tail_first + p / a.tail_k;
+            sub = p - (p / a.tail_k) * a.tail_k;
+        }
+    }
     int lo = 0, hi = a.E;   // the last group whose first tile is <= t
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -222,6 +237,14 @@ __device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a, const int *s_o
     ti.g0 = (s_off[e] & ~3) + ch * a.bn;
     ti.clo = max(0, s_off[e] - ti.g0);
     ti.chi = min(a.bn, s_off[e + 1] - ti.g0);
+    if (kTail && sub >= 0) {
+        // piece `sub` of the chunk's columns [0, chi) (dense: clo = 0), in widths
+        // that are multiples of 16 so every piece starts on a 16-byte boundary of
+        // the token scales; trailing pieces of a narrow chunk are empty
+        const int pw = ((ti.chi + a.tail_k - 1) / a.tail_k + 15) & ~15;
+        ti.g0 += sub * pw;
+        ti.chi = max(0, min(pw, ti.chi - sub * pw));
+    }
     ti.ncols = (ti.chi + 15) & ~15;
     return ti;
 }
@@ -230,7 +253,7 @@ __device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a, const int *s_o
 // positions of the shared-memory stages and TMEM buffers are carried as
 // counters and phase bits, arrivals come from one elected lane.  Returns false
 // when a wait gave up.
-template <int EPQ, int XB, bool kQN>
+template <int EPQ, int XB, bool kQN, bool kTail>
 __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const int *s_off,
                                                const int *s_tpre, uint64_t *bars, const float *s_sa,
                                                const float *s_sb, uint32_t tmem, int warp, int lane,
@@ -245,7 +268,8 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
     const uint64_t lim = a.wait_limit;
     uint32_t s = 0, sph = 0, gb = 0, gph = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const TcTile ti = tc_tile(t, a, s_off, s_tpre);
+        const TcTile ti = tc_tile<kTail>(t, a, s_off, s_tpre);
+        if (kTail && ti.ncols == 0) continue;   // an empty piece: no role touches it
         const int n16 = ti.ncols >> 4;
         const int base = n16 / EPQ, rem = n16 % EPQ;
         const int nch = base + (part < rem ? 1 : 0);
@@ -341,8 +365,9 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
 }
 
 // kEpi: 0 = y only, 1 = y and the block sums, 2 = y (optional) and the output
-// quantized for the next projection
-template <int EPQ, int XB, int kEpi>
+// quantized for the next projection.  kTail: the last partial wave's tiles are
+// cut into pieces (TcArgs::tail_first, tail_k).
+template <int EPQ, int XB, int kEpi, bool kTail = false>
 __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_sa,
@@ -424,7 +449,9 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
         }
         if (lane == 31) {
             s_tpre[E] = incl;
-            misc[kMiscTotal] = incl;
+            misc[kMiscTotal] = (kTail && incl > a.tail_first)
+                                   ? a.tail_first + (incl - a.tail_first) * a.tail_k
+                                   : incl;
         }
     }
     __syncthreads();
@@ -456,7 +483,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
             uint32_t ks = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TcTile ti = tc_tile(t, a, s_off, s_tpre);
+                const TcTile ti = tc_tile<kTail>(t, a, s_off, s_tpre);
+                if (kTail && ti.ncols == 0) continue;
                 for (int st = 0; st < nst; ++st, ++ks) {
                     const int s = ks % kStages;
                     if (!mbar_wait_bounded(&bars[kBarEmpty + s], ((ks / kStages) & 1) ^ 1, lim,
@@ -491,7 +519,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
             uint32_t ks = 0, kg = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TcTile ti = tc_tile(t, a, s_off, s_tpre);
+                const TcTile ti = tc_tile<kTail>(t, a, s_off, s_tpre);
+                if (kTail && ti.ncols == 0) continue;
                 const uint32_t idesc = idesc_e4m3_f32(kBM, ti.ncols);
                 for (int st = 0; st < nst && ok; ++st, ++ks) {
                     const int s = ks % kStages;
@@ -544,7 +573,7 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
     } else if constexpr (!kSums) {
         // ------------------------------------------------------- epilogue
         if constexpr (C::kRegSplit) reg_alloc<C::kEpiRegs>();
-        if (!epilogue_tiles<EPQ, XB, kEpi == 2>(a, total, s_off, s_tpre, bars, s_sa, s_sb, tmem,
+        if (!epilogue_tiles<EPQ, XB, kEpi == 2, kTail>(a, total, s_off, s_tpre, bars, s_sa, s_sb, tmem,
                                                 warp, lane,
                                      abort_flag))
             set_abort(misc);
@@ -559,7 +588,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
         uint32_t ks = 0, kg = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const TcTile ti = tc_tile(t, a, s_off, s_tpre);
+            const TcTile ti = tc_tile<kTail>(t, a, s_off, s_tpre);
+            if (kTail && ti.ncols == 0) continue;
             const int n16 = ti.ncols >> 4;
             const int base = n16 / EPQ, rem = n16 % EPQ;
             const int nch = base + (part < rem ? 1 : 0);
@@ -700,39 +730,99 @@ h32_status make_map(CUtensorMap *map, CUtensorMapDataType type, int esize, const
     return H32_OK;
 }
 
-// tokens per tile: simulate the static round-robin schedule (as the Q4_0 GEMM)
-int choose_bn_tc(int64_t M, int64_t N, int sms) {
-    const int64_t nt = (N + kBM - 1) / kBM;
-    int best = kBNMax;
-    double best_cost = 1e300;
-    for (int bn = kBNMax; bn >= 32; bn -= 16) {
-        const int64_t chunks = (M + bn - 1) / bn;
-        const int64_t tiles = nt * chunks;
-        const int64_t grid = tiles < sms ? tiles : sms;
-        double worst = 0.0;
-        for (int64_t c = 0; c < grid; ++c) {
-            double cost = 0.0;
-            for (int64_t t = c; t < tiles; t += grid) {
-                const int64_t ch = t % chunks;
-                const int64_t rows = (ch == chunks - 1) ? M - ch * bn : bn;
-                // a tile costs its MMA width plus a fixed part that, measured on
-                // GB300, is about the work of 64 more columns
-                cost += ((rows + 15) / 16) * 16 + 64;
+// The dense schedule: tokens per tile (bn), and how many pieces each tile of
+// the last partial wave is cut into along the tokens (tail_k), chosen by
+// simulating the kernel's static round-robin assignment of tiles to CTAs.
+struct TcPlan {
+    int bn, tail_k;
+    int64_t tail_first, total, grid;
+};
+
+// a tile costs its MMA width plus a fixed part that, measured on GB300, is
+// about the work of 64 more columns
+inline int64_t tile_cost(int64_t width) { return width > 0 ? ((width + 15) / 16) * 16 + 64 : 0; }
+
+inline int64_t plan_makespan(int64_t M, int64_t nt, int sms, int bn, int k, TcPlan *plan) {
+    const int64_t chunks = (M + bn - 1) / bn;
+    const int64_t T = nt * chunks;
+    const int64_t r = T % sms;   // tiles of the last partial wave
+    const int64_t tail_first = (k > 1 && r > 0) ? T - r : T;
+    const int64_t total = tail_first + (T - tail_first) * k;
+    const int64_t grid = total < sms ? total : sms;
+    auto width = [&](int64_t t) {
+        const int64_t ch = t % chunks;
+        return ch == chunks - 1 ? M - ch * bn : static_cast<int64_t>(bn);
+    };
+    int64_t worst = 0;
+    for (int64_t c = 0; c < grid; ++c) {
+        int64_t cost = 0;
+        for (int64_t t = c; t < total; t += grid) {
+            if (t < tail_first) {
+                cost += tile_cost(width(t));
+            } else {
+                const int64_t p = t - tail_first, sub = p % k;
+                const int64_t w = width(tail_first + p / k);
+                const int64_t pw = ((w + k - 1) / k + 15) / 16 * 16;
+                const int64_t wp = w - sub * pw < pw ? w - sub * pw : pw;
+                cost += tile_cost(wp > 0 ? wp : 0);
             }
-            if (cost > worst) worst = cost;
         }
-        if (worst < best_cost - 1e-9) {
-            best_cost = worst;
-            best = bn;
-        }
+        if (cost > worst) worst = cost;
     }
-    return best;
+    if (plan) *plan = TcPlan{bn, k, tail_first, total, grid};
+    return worst;
 }
 
-template <int EPQ, int XB, int kEpi>
+TcPlan plan_tc_uncached(int64_t M, int64_t N, int sms, bool allow_cut) {
+    const int64_t nt = (N + kBM - 1) / kBM;
+    int best_bn = kBNMax;
+    int64_t best = INT64_MAX;
+    for (int bn = kBNMax; bn >= 32; bn -= 16) {
+        const int64_t m = plan_makespan(M, nt, sms, bn, 1, nullptr);
+        if (m < best) {
+            best = m;
+            best_bn = bn;
+        }
+    }
+    // then the cut of the last partial wave, kept only where the simulation
+    // shortens the makespan by at least 4% (measured on GB300: smaller predicted
+    // gains do not survive the cut kernel's extra tile decoding)
+    TcPlan plan{};
+    plan_makespan(M, nt, sms, best_bn, 1, &plan);
+    const int64_t uncut = best;
+    for (int k = 2; allow_cut && k <= 8 && best_bn / k >= 16; k *= 2) {
+        TcPlan p{};
+        const int64_t m = plan_makespan(M, nt, sms, best_bn, k, &p);
+        if (m < best && m * 25 <= uncut * 24) {
+            best = m;
+            plan = p;
+        }
+    }
+    return plan;
+}
+
+// the simulation costs O(tiles) host time per candidate: remember the plan of
+// each shape (a bounded table, emptied when full)
+TcPlan plan_tc(int64_t M, int64_t N, int sms, bool allow_cut) {
+    static std::mutex mu;
+    static std::map<std::tuple<int64_t, int64_t, int, bool>, TcPlan> plans;
+    const auto key = std::make_tuple(M, N, sms, allow_cut);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const auto it = plans.find(key);
+        if (it != plans.end()) return it->second;
+    }
+    const TcPlan plan = plan_tc_uncached(M, N, sms, allow_cut);
+    std::lock_guard<std::mutex> lock(mu);
+    if (plans.size() >= 4096) plans.clear();
+    plans.emplace(key, plan);
+    return plan;
+}
+
+template <int EPQ, int XB, int kEpi, bool kTail = false>
 h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStream_t s) {
     using C = TcCfg<EPQ, XB>;
-    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi, kTail>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return launch_status(e);
     if constexpr (C::kRegSplit) {
@@ -741,7 +831,7 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
         // (read once per kernel; a failed read leaves -1 and refuses every launch)
         static const int regs = [] {
             cudaFuncAttributes fa{};
-            return cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi>) == cudaSuccess
+            return cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi, kTail>) == cudaSuccess
                        ? fa.numRegs
                        : -1;
         }();
@@ -750,7 +840,7 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
             return H32_ERR_UNSUPPORTED;
         }
     }
-    const cudaError_t el = launch_pdl(gemm_tc_kernel<EPQ, XB, kEpi>, dim3(grid), dim3(C::kThreads),
+    const cudaError_t el = launch_pdl(gemm_tc_kernel<EPQ, XB, kEpi, kTail>, dim3(grid), dim3(C::kThreads),
                                       C::kSmem, s, maps[0], maps[1], maps[2], maps[3], a);
     return launch_status(el != cudaSuccess ? el : cudaGetLastError());
 }
@@ -799,14 +889,15 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     if (M > 0x7FFFFFFFll || E * N > 0x7FFFFFFFll || K > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
     int sms = 0;
     H32_TRY(check_device(&sms));
-    // dense: the tile width from the schedule simulation; groups: full 128-row chunks
-    const int bn = expert_off ? kBNMax : choose_bn_tc(M, N, sms);
-    int64_t grid = sms;
+    // dense: the tile width and the cut of the last wave from the schedule
+    // simulation; groups: full 128-row chunks, nothing cut
+    TcPlan plan{kBNMax, 1, 0, 0, sms};
     if (!expert_off) {
-        const int64_t total = ((N + kBM - 1) / kBM) * ((M + bn - 1) / bn);
-        if (total > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
-        grid = total < sms ? total : sms;
+        if (((N + kBM - 1) / kBM) * ((M + 15) / 16) * 8 > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
+        plan = plan_tc(M, N, sms, xbits == 4 && !qn && !block_sums);
     }
+    const int bn = plan.bn;
+    const int64_t grid = plan.grid;
     CUtensorMap maps[4];
     H32_TRY(make_map(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wp, K, E * N, K, 128, kBM, true));
     const int64_t xrow = K * (xbits / 4);   // activation bytes per row
@@ -829,6 +920,8 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     a.nb = static_cast<int32_t>(K / 32);
     a.bn = bn;
     a.E = static_cast<int32_t>(E);
+    a.tail_first = static_cast<int32_t>(plan.tail_first);
+    a.tail_k = plan.tail_k;
     a.wait_limit = wait_limit();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int g = static_cast<int>(grid);
@@ -842,7 +935,11 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     // (5 or 6 chunks: measured 5-8% faster on the pp512 attention and FFN-down
     // shapes), 16 otherwise
     const int n16 = bn / 16;
-    if (n16 % 4 == 1 || n16 % 4 == 2) return launch_tc<3, 4, 0>(maps, a, g, s);
+    const bool narrow = n16 % 4 == 1 || n16 % 4 == 2;
+    if (plan.tail_k > 1)
+        return narrow ? launch_tc<3, 4, 0, true>(maps, a, g, s)
+                      : launch_tc<H32_TC_EPI_PER_QUAD, 4, 0, true>(maps, a, g, s);
+    if (narrow) return launch_tc<3, 4, 0>(maps, a, g, s);
     return launch_tc<H32_TC_EPI_PER_QUAD, 4, 0>(maps, a, g, s);
 }
 

@@ -75,7 +75,9 @@ def _tc_operands(h32, x, w, bf16=True):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 16, 128), (17, 144, 256), (64, 256, 512), (129, 128, 384),
-                                   (300, 384, 1024)])
+                                   (300, 384, 1024),
+                                   # last-wave tiles cut into pieces, some of them empty
+                                   (33, 1024, 256), (34, 2560, 128)])
 def test_gemm_tc_bit_exact(h32, M, N, K):
     import torch
     x = wl.f32_to_bf16_bits(wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, 220 + M))

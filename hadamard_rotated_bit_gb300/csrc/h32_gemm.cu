@@ -38,7 +38,9 @@
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "h32_common.cuh"
 #include "h32_epilogue.cuh"
@@ -812,7 +814,7 @@ h32_status make_weight_map(CUtensorMap *map, const uint8_t *wq, int64_t rows, in
 // assignment of tiles to SMs and keep the width with the shortest makespan
 // (a tile costs its 16-rounded width plus a fixed share for widening its
 // weight tile).
-int choose_bn(int64_t M, int64_t N, int sms) {
+int choose_bn_uncached(int64_t M, int64_t N, int sms) {
     const int64_t nt = (N + kBM - 1) / kBM;
     int best = kBNMax;
     double best_cost = 1e300;
@@ -836,6 +838,24 @@ int choose_bn(int64_t M, int64_t N, int sms) {
         }
     }
     return best;
+}
+
+// the simulation costs O(tiles) host time: remember each shape's width (a
+// bounded table, emptied when full)
+int choose_bn(int64_t M, int64_t N, int sms) {
+    static std::mutex mu;
+    static std::map<std::tuple<int64_t, int64_t, int>, int> widths;
+    const auto key = std::make_tuple(M, N, sms);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const auto it = widths.find(key);
+        if (it != widths.end()) return it->second;
+    }
+    const int bn = choose_bn_uncached(M, N, sms);
+    std::lock_guard<std::mutex> lock(mu);
+    if (widths.size() >= 4096) widths.clear();
+    widths.emplace(key, bn);
+    return bn;
 }
 
 template <int XB, bool kSums>

@@ -775,27 +775,29 @@ inline int64_t plan_makespan(int64_t M, int64_t nt, int sms, int bn, int k, TcPl
 
 TcPlan plan_tc_uncached(int64_t M, int64_t N, int sms, bool allow_cut) {
     const int64_t nt = (N + kBM - 1) / kBM;
-    int best_bn = kBNMax;
+    TcPlan plan{};
     int64_t best = INT64_MAX;
     for (int bn = kBNMax; bn >= 32; bn -= 16) {
-        const int64_t m = plan_makespan(M, nt, sms, bn, 1, nullptr);
+        TcPlan p{};
+        const int64_t m = plan_makespan(M, nt, sms, bn, 1, &p);
         if (m < best) {
             best = m;
-            best_bn = bn;
+            plan = p;
         }
     }
-    // then the cut of the last partial wave, kept only where the simulation
-    // shortens the makespan by at least 4% (measured on GB300: smaller predicted
-    // gains do not survive the cut kernel's extra tile decoding)
-    TcPlan plan{};
-    plan_makespan(M, nt, sms, best_bn, 1, &plan);
+    // then a cut of the last partial wave, at any width, kept only where the
+    // simulation shortens the best uncut makespan by at least 4% (measured on
+    // GB300: smaller predicted gains do not survive the cut kernel's extra
+    // tile decoding)
     const int64_t uncut = best;
-    for (int k = 2; allow_cut && k <= 8 && best_bn / k >= 16; k *= 2) {
-        TcPlan p{};
-        const int64_t m = plan_makespan(M, nt, sms, best_bn, k, &p);
-        if (m < best && m * 25 <= uncut * 24) {
-            best = m;
-            plan = p;
+    for (int bn = kBNMax; allow_cut && bn >= 32; bn -= 16) {
+        for (int k = 2; k <= 8 && bn / k >= 16; k *= 2) {
+            TcPlan p{};
+            const int64_t m = plan_makespan(M, nt, sms, bn, k, &p);
+            if (m < best && m * 25 <= uncut * 24) {
+                best = m;
+                plan = p;
+            }
         }
     }
     return plan;

@@ -28,6 +28,13 @@
 // The MMA and the epilogue hand off two blocks per synchronization; measured
 // on GB300, one block per hand-off (four buffers) is slower, as every hand-off
 // puts all epilogue warps in step.  Every wait is bounded.
+//
+// Schedule: one persistent CTA per SM takes tiles t = blockIdx.x, + gridDim.x,
+// ...  The host simulates that assignment once per shape to choose the token
+// width of a tile and, where it pays, a second kernel instance whose last
+// partial wave of tiles is cut into narrower pieces.  Kernels are launched with
+// programmatic dependent launch: nothing touches global memory before the
+// previous kernel of the stream has completed.
 
 // epilogue warps per TMEM lane quarter
 #ifndef H32_TC_EPI_PER_QUAD

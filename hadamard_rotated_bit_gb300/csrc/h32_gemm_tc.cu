@@ -912,7 +912,7 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     TcPlan plan{kBNMax, 1, 0, 0, sms};
     if (!expert_off) {
         if (((N + kBM - 1) / kBM) * ((M + 15) / 16) * 8 > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
-        plan = plan_tc(M, N, sms, xbits == 4 && !qn && !block_sums);
+        plan = plan_tc(M, N, sms, !qn && !block_sums);
     }
     const int bn = plan.bn;
     const int64_t grid = plan.grid;
@@ -943,9 +943,11 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     a.wait_limit = wait_limit();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int g = static_cast<int>(grid);
-    if (xbits == 8)
-        return block_sums ? launch_tc<H32_TC_EPI_PER_QUAD, 8, 1>(maps, a, g, s)
-                          : launch_tc<H32_TC_EPI_PER_QUAD, 8, 0>(maps, a, g, s);
+    if (xbits == 8) {
+        if (block_sums) return launch_tc<H32_TC_EPI_PER_QUAD, 8, 1>(maps, a, g, s);
+        return plan.tail_k > 1 ? launch_tc<H32_TC_EPI_PER_QUAD, 8, 0, true>(maps, a, g, s)
+                               : launch_tc<H32_TC_EPI_PER_QUAD, 8, 0>(maps, a, g, s);
+    }
     if (qn) return launch_tc<H32_TC_EPI_PER_QUAD, 4, 2>(maps, a, g, s);
     if (block_sums) return launch_tc<H32_TC_EPI_PER_QUAD, 4, 1>(maps, a, g, s);
     // the tile's 16-column chunks in even shares: 12 epilogue warps (3 per lane

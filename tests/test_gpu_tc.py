@@ -259,6 +259,29 @@ def test_tc_experts_identity_rows(h32):
     assert np.array_equal(y.reshape(-1).view(np.uint32), r32.view(np.uint32))
 
 
+def test_tc_experts_every_group_width(h32):
+    """Plain-output expert launches over groups of 1 .. 200 rows (every count
+    of 16-column chunks a 128-token chunk can have, ragged chunk widths,
+    groups longer than one chunk, empty groups) with group starts at every
+    residue mod 4; every output against the oracle's same-order fp32 value."""
+    counts = np.array([1, 7, 8, 9, 15, 16, 17, 23, 24, 25, 31, 33, 40, 47, 48, 49, 56, 63, 64,
+                       65, 72, 79, 80, 81, 88, 95, 96, 97, 104, 111, 112, 113, 120, 125, 127,
+                       128, 129, 0, 3, 200, 2, 41])
+    E, N, K, T = counts.size, 32, 128, 300
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    R = int(off[-1])
+    assert len({int(o) % 4 for o in off[:-1]}) == 4
+    ridx = np.random.default_rng(11).integers(0, T, R).astype(np.int32)
+    x = wl.act_normal_outliers(T, K, 0.02, 25.0, 0, wl.CFG_TEST, 270)
+    w = wl.weights_normal(E * N, K, 0.02, 0, wl.CFG_TEST, 271)
+    (wq, wd, xq, xd), y, _, st = _tc_experts(h32, x, w, E, N, ridx, off, block_sums=False)
+    assert st == 0
+    ri = np.repeat(np.arange(R), N)
+    ni = np.tile(np.arange(N), R)
+    r32, _, _ = oracle.gemm_experts_sampled(wq, wd, xq, xd, ridx, off, N, K, ri, ni)
+    assert np.array_equal(y.reshape(-1).view(np.uint32), r32.view(np.uint32))
+
+
 def test_tc_experts_bad_offsets_guarded(h32):
     import torch
     E, N, K = 2, 16, 128

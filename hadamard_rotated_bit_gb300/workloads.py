@@ -165,6 +165,11 @@ class MoEConfig:
 MOE = MoEConfig()
 
 
+def moe_logits(cfg: MoEConfig, seed: int = 0) -> np.ndarray:
+    """Router logits [T][E] fp32, U(0,1)."""
+    return rng(seed, cfg.config_id, 0).random((cfg.T, cfg.E), dtype=np.float32)
+
+
 def moe_routing(cfg: MoEConfig, seed: int = 0):
     """Top-k experts per token from U(0,1) logits, grouped by expert.
 
@@ -172,7 +177,7 @@ def moe_routing(cfg: MoEConfig, seed: int = 0):
     ties go to the lower expert id.  Returns (row_idx [T*k] int32: the token of
     each grouped row, expert_off [E+1] int32, expert_of_row [T*k] int32).
     Rows are grouped by expert, and within an expert kept in token order."""
-    logits = rng(seed, cfg.config_id, 0).random((cfg.T, cfg.E), dtype=np.float32)
+    logits = moe_logits(cfg, seed)
     # stable sort on -logit keeps the lower id first among equal logits
     order = np.argsort(-logits, axis=1, kind="stable")[:, :cfg.top_k]
     tok = np.repeat(np.arange(cfg.T, dtype=np.int64), cfg.top_k)

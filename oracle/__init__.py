@@ -66,6 +66,8 @@ def _load():
                 "o_gemm_sampled": [_P, _P, _P, _P, ctypes.c_int, _I64, _I64, _P, _P, _P, _P, _P],
                 "o_gemm_experts_sampled": [_P, _P, _I64, _P, _P, _P, _P, _I64, _I64, _I64,
                                            _P, _P, _P, _P, _P],
+                "o_moe_route": [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P],
+                "o_moe_combine": [_P, _I64, _P, _P, _I64, _I64, _I64, _P],
             }
             for name, args in sigs.items():
                 fn = getattr(lib, name)
@@ -298,3 +300,39 @@ def gemm_experts_sampled(wq, wd, xq, xd, row_idx, expert_off, N: int, K: int,
                                    _ptr(off), N, K, P, _ptr(r_idx), _ptr(n_idx),
                                    _ptr(y32), _ptr(y64), _ptr(S))
     return y32, y64, S
+
+
+# --------------------------------------------------------------------------
+# routing and the weighted combine around the expert GEMM ("Where the engine
+# is going: HRX and the NPU", section "4-bit activations reach the MoE experts")
+# --------------------------------------------------------------------------
+def moe_route(logits: np.ndarray, k: int):
+    """logits [T][E] fp32 -> (topk_id [T][k] int32, topk_w [T][k] fp32,
+    expert_off [E+1] int32, row_idx [T*k] int32, row_of [T][k] int32).
+
+    Top k by logit (ties: lower id), weights = softmax over the k chosen
+    logits (fp32, sum in choice order), rows grouped by expert then token."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    assert 1 <= k <= E
+    topk_id = np.empty((T, k), np.int32)
+    topk_w = np.empty((T, k), np.float32)
+    off = np.empty(E + 1, np.int32)
+    row_idx = np.empty(T * k, np.int32)
+    row_of = np.empty((T, k), np.int32)
+    _load().o_moe_route(_ptr(logits), T, E, k, _ptr(topk_id), _ptr(topk_w), _ptr(off),
+                        _ptr(row_idx), _ptr(row_of))
+    return topk_id, topk_w, off, row_idx, row_of
+
+
+def moe_combine(y: np.ndarray, row_of: np.ndarray, topk_w: np.ndarray) -> np.ndarray:
+    """y [R][H] fp32 (grouped rows) -> out [T][H]: sum over the token's k
+    choices in order of w_j * y[row_of[t][j]], fp32 fma from +0."""
+    y = _c(y, np.float32)
+    row_of, topk_w = _c(row_of, np.int32), _c(topk_w, np.float32)
+    T, k = row_of.shape
+    H = y.shape[1]
+    assert row_of.size == 0 or (row_of.min() >= 0 and row_of.max() < y.shape[0])
+    out = np.empty((T, H), np.float32)
+    _load().o_moe_combine(_ptr(y), H, _ptr(row_of), _ptr(topk_w), T, k, H, _ptr(out))
+    return out

@@ -468,3 +468,73 @@ void o_gemm_experts_sampled(const uint8_t *wq, const uint16_t *wd, int64_t E,
                    xd + xr * nb, 4, nb, &y32[i], &y64[i], S ? S + i * nb : 0);
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Expert routing and the weighted combine around the expert-batched GEMM    */
+/* ------------------------------------------------------------------------ */
+/* [MoE] "Where the engine is going: HRX and the NPU", section "4-bit
+ * activations reach the MoE experts": the route covers the expert matmuls of
+ * a mixture-of-experts model.  The pages do not spell out the router around
+ * them; the readings taken:
+ *   - a token takes the k experts of largest logit (the softmax is monotonic,
+ *     so these are its k most probable experts), ties to the lower expert id,
+ *     listed by decreasing logit;
+ *   - choice j weighs w_j = exp(l_j - l_max) / sum_i exp(l_i - l_max) over
+ *     the k chosen logits, which is the full softmax's top-k probabilities
+ *     renormalised to sum to 1; in fp32: one difference and one exp per
+ *     choice, the sum taken in choice order from +0, one IEEE divide each;
+ *   - rows are grouped by expert id, and within an expert by token;
+ *   - the combine adds the k expert rows of a token in choice order,
+ *     acc = fma(w_j, y_j, acc) from +0. */
+
+/* logits [T][E] -> topk_id [T][k], topk_w [T][k], expert_off [E+1],
+ * row_idx [T*k] (the token of grouped row r), row_of [T][k] (the grouped row
+ * of choice j of token t). */
+void o_moe_route(const float *logits, int64_t T, int64_t E, int64_t k, int32_t *topk_id,
+                 float *topk_w, int32_t *expert_off, int32_t *row_idx, int32_t *row_of)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = logits + t * E;
+        int32_t *id = topk_id + t * k;
+        for (int64_t j = 0; j < k; ++j) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e) {
+                int taken = 0;
+                for (int64_t i = 0; i < j; ++i)
+                    if (id[i] == e) taken = 1;
+                if (taken) continue;
+                if (best < 0 || l[e] > l[best]) best = e; /* strict: a tie keeps the lower id */
+            }
+            id[j] = (int32_t)best;
+        }
+        const float lmax = l[id[0]];
+        float s = 0.0f;
+        for (int64_t j = 0; j < k; ++j) s = s + expf(l[id[j]] - lmax);
+        for (int64_t j = 0; j < k; ++j) topk_w[t * k + j] = expf(l[id[j]] - lmax) / s;
+    }
+    int64_t r = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        expert_off[e] = (int32_t)r;
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t j = 0; j < k; ++j)
+                if (topk_id[t * k + j] == e) {
+                    row_idx[r] = (int32_t)t;
+                    row_of[t * k + j] = (int32_t)r;
+                    ++r;
+                }
+    }
+    expert_off[E] = (int32_t)r;
+}
+
+/* out [T][H] = sum over j < k of topk_w[t][j] * y[row_of[t][j]][:] (y [R][ldy]) */
+void o_moe_combine(const float *y, int64_t ldy, const int32_t *row_of, const float *topk_w,
+                   int64_t T, int64_t k, int64_t H, float *out)
+{
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int64_t j = 0; j < k; ++j)
+                acc = fmaf(topk_w[t * k + j], y[(int64_t)row_of[t * k + j] * ldy + h], acc);
+            out[t * H + h] = acc;
+        }
+}

@@ -806,6 +806,39 @@ def suite_moe(torch, h32, dev, stream, steps, warmup):
                 "value": round(cfg.T / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
                 "operand_form": "tc", "gemm_ms": {k: round(v, 4) for k, v in tt.items()},
                 "gemm_eff_TOPS": round(ops / ((tt["gate_up_ms"] + tt["down_ms"]) / 1e3) / 1e12, 1)})
+
+    # the whole expert layer on the GPU: the router (top 8 of the logits, their
+    # weights, the grouped order), the tc-form expert GEMMs on that order and the
+    # weighted combine back to token order (SwiGLU stays outside the path)
+    lg = torch.from_numpy(wl.moe_logits(cfg)).to(dev)
+    ids, tw, offs_r, ridx_r, row_of = h32.h32_moe_route(lg, cfg.top_k, stream=stream)
+    out_t = torch.empty((cfg.T, N_dn), dtype=torch.float32, device=dev)
+
+    def route():
+        h32.h32_moe_route(lg, cfg.top_k, topk_id=ids, topk_w=tw, expert_off=offs_r,
+                          row_idx=ridx_r, row_of=row_of, stream=stream)
+
+    def combine():
+        h32.h32_moe_combine(y_dn, row_of, tw, out=out_t, stream=stream)
+
+    def step_layer():
+        route()
+        h32.h32_quantize_act_q4_tc_gather(xg, ridx_r, xw=xw_gu, xdt=xt_gu, stream=stream)
+        h32.q4_0_x_q4_gemm_tc_experts(wp_gu, ws_gu, xw_gu, xt_gu, offs_r, N_gu, R=R, y=y_gu,
+                                      stream=stream)
+        h32.h32_quantize_act_q4_tc(xn, xw=xw_dn, xdt=xt_dn, stream=stream)
+        h32.q4_0_x_q4_gemm_tc_experts(wp_dn, ws_dn, xw_dn, xt_dn, offs_r, N_dn, R=R, y=y_dn,
+                                      stream=stream)
+        combine()
+    ms = _events_time(torch, step_layer, steps, warmup, stream)
+    t_route = _events_time(torch, route, steps, warmup, stream)
+    t_comb = _events_time(torch, combine, steps, warmup, stream)
+    comb_bytes = R * N_dn * 4 + cfg.T * N_dn * 4 + R * 8
+    out.append({"suite": "moe_layer_1024_tokens_route_experts_combine",
+                "value": round(cfg.T / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+                "operand_form": "tc", "route_ms": round(t_route, 4), "combine_ms": round(t_comb, 4),
+                "combine_GBps": round(comb_bytes / (t_comb / 1e3) / 1e9, 1),
+                "combine_note": "grouped rows L2-resident, as right after the down GEMM"})
     return out
 
 

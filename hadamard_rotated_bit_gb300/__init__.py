@@ -64,6 +64,8 @@ _SIGS = {
                                              _INT, _P]),
     "q4_0_x_q4_gemm_tc_experts": (_INT, [_P, _P, _I64, ctypes.c_int32, _P, _P, _I64, _P, _I64, _I64,
                                          _I64, _P, _I64, _P, _P]),
+    "h32_moe_route": (_INT, [_P, _I64, _I32, _I64, _I32, _P, _P, _P, _P, _P, _P]),
+    "h32_moe_combine": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I32, _I64, _P, _I64, _P]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -438,3 +440,53 @@ def q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=None, y=None, want_y=True, 
                                             _rot_arg(rotate_next), _stream(stream))
     _check("q4_0_x_q4_gemm_tc_quant_next", st)
     return y, xw_next, xdt_next
+
+
+def h32_moe_route(logits, k, topk_id=None, topk_w=None, expert_off=None, row_idx=None,
+                  row_of=None, stream=None):
+    """Router: logits [T][E] fp32 -> (topk_id [T][k] int32, topk_w [T][k] fp32,
+    expert_off [E+1] int32, row_idx [T*k] int32, row_of [T][k] int32).  The k
+    largest logits (ties: lower id), softmax weights over them, rows grouped by
+    expert then token."""
+    torch = _torch()
+    _cuda(logits, "logits")
+    if logits.dtype != torch.float32:
+        raise ValueError("logits must be fp32")
+    T, E = logits.shape
+    ldl = _rows(logits, "logits") if T > 0 else E
+    dev = logits.device
+    if topk_id is None:
+        topk_id = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if expert_off is None:
+        expert_off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    if row_idx is None:
+        row_idx = torch.empty(T * k, dtype=torch.int32, device=dev)
+    if row_of is None:
+        row_of = torch.empty((T, k), dtype=torch.int32, device=dev)
+    st = lib().h32_moe_route(_ptr(logits), T, E, ldl, k, _ptr(topk_id), _ptr(topk_w),
+                             _ptr(expert_off), _ptr(row_idx), _ptr(row_of), _stream(stream))
+    _check("h32_moe_route", st)
+    return topk_id, topk_w, expert_off, row_idx, row_of
+
+
+def h32_moe_combine(y, row_of, topk_w, out=None, stream=None):
+    """Weighted combine: y [R][H] fp32 (grouped rows), row_of [T][k], topk_w [T][k]
+    -> out [T][H] fp32, the token's k rows added in choice order (fp32 fma from 0)."""
+    torch = _torch()
+    _cuda(y, "y")
+    R, H = y.shape
+    T, k = row_of.shape
+    if row_of.dtype != torch.int32 or topk_w.dtype != torch.float32:
+        raise ValueError("row_of must be int32 and topk_w fp32")
+    if not (row_of.is_contiguous() and topk_w.is_contiguous()):
+        raise ValueError("row_of and topk_w must be contiguous")
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32, device=y.device)
+    ldy = _rows(y, "y") if R > 0 else H
+    ldo = _rows(out, "out") if T > 0 else H
+    st = lib().h32_moe_combine(_ptr(y), R, ldy, _ptr(row_of), _ptr(topk_w), T, k, H, _ptr(out),
+                               ldo, _stream(stream))
+    _check("h32_moe_combine", st)
+    return out

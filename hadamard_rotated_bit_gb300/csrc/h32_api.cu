@@ -66,9 +66,10 @@ extern "C" h32_status h32_device_status(void *stream) {
     H32_TRY(h32::check_device(nullptr));
     const cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return h32::launch_status(e);
-    const h32_status st[3] = {h32::quant_read_and_clear_status(s),
+    const h32_status st[4] = {h32::quant_read_and_clear_status(s),
                               h32::gemm_read_and_clear_status(s),
-                              h32::tc_read_and_clear_status(s)};
+                              h32::tc_read_and_clear_status(s),
+                              h32::moe_read_and_clear_status(s)};
     for (h32_status v : st)
         if (v == H32_ERR_CUDA) return H32_ERR_CUDA;
     for (h32_status v : st)

@@ -1,0 +1,281 @@
+// Routing and weighted combine around the expert-batched GEMM (sm_103a).
+//
+// "Where the engine is going: HRX and the NPU", section "4-bit activations
+// reach the MoE experts": the Hadamard route covers the expert matmuls of a
+// mixture-of-experts model.  These kernels are the layer around those
+// matmuls: pick each token's experts and weights from its router logits,
+// group the (token, expert) rows by expert for the grouped GEMM, and add a
+// token's expert outputs back together.  The pages leave the router open;
+// the reading taken here: the k largest logits (ties to the lower expert id),
+// listed by decreasing logit; weights = softmax over those k logits (the full
+// softmax's top-k probabilities renormalised to sum to 1); rows grouped by
+// expert, then by token; the combine sums a token's rows in choice order with
+// fp32 fma from +0.
+//
+// Every result is deterministic: no atomics decide an order.
+//   route_topk_kernel   one warp per token: k rounds of a warp-wide argmax
+//                       over the logits held in registers, then the weights
+//   route_group_kernel  one block per expert: its offset is the number of
+//                       choices of lower experts; its rows are the tokens
+//                       that chose it, in token order (ballot prefix sums)
+//   combine_kernel      one block per token (x) and column range (y): 16-byte loads
+//                       of the token's k rows, fma in choice order
+#include "h32_common.cuh"
+
+namespace h32 {
+namespace {
+
+__device__ uint32_t g_moe_status;   // kStatusGuard: a combine row index out of range
+
+constexpr int kMaxE = 1024;         // experts a router call handles
+constexpr int kMaxK = 32;           // choices per token (one lane each)
+constexpr int kTopkWarps = 8;       // tokens per block of route_topk_kernel
+constexpr int kGroupThreads = 256;
+constexpr int kCombineThreads = 128;
+constexpr int kCombineVec = 4;      // float4 columns per thread and block
+
+// (value, id) a beats b: larger value, or equal value and lower id; id < 0 = none
+__device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
+    if (ia < 0) return false;
+    if (ib < 0) return true;
+    return va > vb || (va == vb && ia < ib);
+}
+
+__global__ void __launch_bounds__(kTopkWarps * 32)
+    route_topk_kernel(const float *__restrict__ logits, int T, int E, int64_t ldl, int k,
+                      int32_t *__restrict__ topk_id, float *__restrict__ topk_w) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const float *row = logits + static_cast<int64_t>(t) * ldl;
+    const int nper = (E + 31) >> 5;   // logits per lane: expert lane + 32 i
+    float v[kMaxE / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = (i < nper && e < E) ? row[e] : 0.0f;
+    }
+    uint32_t taken = 0;   // bit i: expert lane + 32 i already chosen
+    int my_id = -1;       // lane j keeps choice j
+    float my_v = 0.0f;
+    for (int j = 0; j < k; ++j) {
+        float bv = 0.0f;
+        int bi = -1;
+#pragma unroll
+        for (int i = 0; i < kMaxE / 32; ++i) {
+            const int e = lane + 32 * i;
+            if (i < nper && e < E && !((taken >> i) & 1u) && beats(v[i], e, bv, bi)) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+            if (beats(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+            my_id = bi;
+            my_v = bv;
+        }
+    }
+    // weights: exp of each chosen logit minus the largest, their sum in choice
+    // order from +0, one IEEE divide each
+    const float lmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
+    const float ex = (lane < k) ? expf(__fsub_rn(my_v, lmax)) : 0.0f;
+    float s = 0.0f;
+    for (int j = 0; j < k; ++j) s = __fadd_rn(s, __shfl_sync(0xFFFFFFFFu, ex, j));
+    if (lane < k) {
+        topk_id[static_cast<int64_t>(t) * k + lane] = my_id;
+        topk_w[static_cast<int64_t>(t) * k + lane] = __fdiv_rn(ex, s);
+    }
+}
+
+// exclusive prefix of `flag` over the block's threads in thread order, and the
+// block's total (all threads get it); scratch holds one int per warp
+__device__ __forceinline__ int block_prefix(bool flag, int *warp_tot, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, flag);
+    if (lane == 0) warp_tot[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, all = 0;
+    for (int w = 0; w < kGroupThreads / 32; ++w) {
+        const int c = warp_tot[w];
+        if (w < warp) before += c;
+        all += c;
+    }
+    __syncthreads();
+    *total = all;
+    return before + __popc(bal & ((1u << lane) - 1u));
+}
+
+__global__ void __launch_bounds__(kGroupThreads)
+    route_group_kernel(const int32_t *__restrict__ topk_id, int T, int E, int k,
+                       int32_t *__restrict__ expert_off, int32_t *__restrict__ row_idx,
+                       int32_t *__restrict__ row_of) {
+    __shared__ int red[2][kGroupThreads / 32];
+    __shared__ int warp_tot[kGroupThreads / 32];
+    pdl_wait();
+    pdl_trigger();
+    const int e = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t n = static_cast<int64_t>(T) * k;
+    // choices of lower experts (this expert's first row) and of this expert
+    int lt = 0, eq = 0;
+    for (int64_t i = threadIdx.x; i < n; i += kGroupThreads) {
+        const int id = topk_id[i];
+        lt += id < e;
+        eq += id == e;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lt += __shfl_xor_sync(0xFFFFFFFFu, lt, o);
+        eq += __shfl_xor_sync(0xFFFFFFFFu, eq, o);
+    }
+    if (lane == 0) {
+        red[0][warp] = lt;
+        red[1][warp] = eq;
+    }
+    __syncthreads();
+    int first = 0, count = 0;
+    for (int w = 0; w < kGroupThreads / 32; ++w) {
+        first += red[0][w];
+        count += red[1][w];
+    }
+    if (threadIdx.x == 0) {
+        expert_off[e] = first;
+        if (e == E - 1) expert_off[E] = first + count;
+    }
+    // this expert's rows: the tokens that chose it, in token order
+    int base = first;
+    for (int t0 = 0; t0 < T; t0 += kGroupThreads) {
+        const int t = t0 + threadIdx.x;
+        int j = -1;
+        if (t < T)
+            for (int c = 0; c < k; ++c)
+                if (topk_id[static_cast<int64_t>(t) * k + c] == e) j = c;
+        int tot;
+        const int pos = block_prefix(j >= 0, warp_tot, &tot);
+        if (j >= 0) {
+            const int r = base + pos;
+            row_idx[r] = t;
+            row_of[static_cast<int64_t>(t) * k + j] = r;
+        }
+        base += tot;
+    }
+}
+
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const float *__restrict__ y, int64_t R, int64_t ldy,
+                   const int32_t *__restrict__ row_of, const float *__restrict__ topk_w, int k,
+                   int64_t H, float *__restrict__ out, int64_t ldo) {
+    __shared__ int64_t s_row[kMaxK];
+    __shared__ float s_w[kMaxK];
+    pdl_wait();
+    pdl_trigger();
+    const int64_t t = blockIdx.x;
+    if (threadIdx.x < k) {
+        int64_t r = row_of[t * k + threadIdx.x];
+        if (r < 0 || r >= R) {
+            atomicOr(&g_moe_status, kStatusGuard);
+            r = -1;
+        }
+        s_row[threadIdx.x] = r;
+        s_w[threadIdx.x] = topk_w[t * k + threadIdx.x];
+    }
+    __syncthreads();
+    const int64_t h4 = H / 4;
+#pragma unroll
+    for (int u = 0; u < kCombineVec; ++u) {
+        const int64_t c = (static_cast<int64_t>(blockIdx.y) * kCombineVec + u) * kCombineThreads +
+                          threadIdx.x;
+        if (c >= h4) break;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int j = 0; j < k; ++j) {
+            const int64_t r = s_row[j];
+            if (r < 0) continue;   // a guarded index adds nothing
+            const float w = s_w[j];
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(y + r * ldy) + c);
+            acc.x = __fmaf_rn(w, v.x, acc.x);
+            acc.y = __fmaf_rn(w, v.y, acc.y);
+            acc.z = __fmaf_rn(w, v.z, acc.z);
+            acc.w = __fmaf_rn(w, v.w, acc.w);
+        }
+        reinterpret_cast<float4 *>(out + t * ldo)[c] = acc;
+    }
+}
+
+}  // namespace
+
+h32_status moe_read_and_clear_status(cudaStream_t s) {
+    uint32_t v = 0;
+    const uint32_t z = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_moe_status, 4, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return H32_ERR_CUDA;
+    if (cudaMemcpyToSymbolAsync(g_moe_status, &z, 4, 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return H32_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return H32_ERR_CUDA;
+    return (v & kStatusGuard) ? H32_ERR_DEVICE_GUARD : H32_OK;
+}
+
+}  // namespace h32
+
+extern "C" h32_status h32_moe_route(const float *logits, int64_t T, int32_t E, int64_t ldl,
+                                    int32_t k, int32_t *topk_id, float *topk_w,
+                                    int32_t *expert_off, int32_t *row_idx, int32_t *row_of,
+                                    void *stream) {
+    using namespace h32;
+    if (T < 0 || E < 1 || E > kMaxE || k < 1 || k > kMaxK || k > E || ldl < E || !expert_off)
+        return H32_ERR_INVALID_ARG;
+    if (T * k > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
+    if (T > 0 && (!logits || !topk_id || !topk_w || !row_idx || !row_of))
+        return H32_ERR_INVALID_ARG;
+    if ((logits && (reinterpret_cast<uintptr_t>(logits) & 3u)) ||
+        (reinterpret_cast<uintptr_t>(expert_off) & 3u))
+        return H32_ERR_ALIGNMENT;
+    H32_TRY(check_device(nullptr));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int t32 = static_cast<int>(T);
+    if (T > 0) {
+        const dim3 grid(static_cast<unsigned>((T + kTopkWarps - 1) / kTopkWarps));
+        const cudaError_t e1 = launch_pdl(route_topk_kernel, grid, dim3(kTopkWarps * 32), 0, s,
+                                          logits, t32, static_cast<int>(E), ldl,
+                                          static_cast<int>(k), topk_id, topk_w);
+        if (e1 != cudaSuccess) return launch_status(e1);
+    }
+    // with T = 0 this writes all-zero offsets
+    const cudaError_t e2 = launch_pdl(route_group_kernel, dim3(E), dim3(kGroupThreads), 0, s,
+                                      static_cast<const int32_t *>(topk_id), t32,
+                                      static_cast<int>(E), static_cast<int>(k), expert_off,
+                                      row_idx, row_of);
+    return launch_status(e2 != cudaSuccess ? e2 : cudaGetLastError());
+}
+
+extern "C" h32_status h32_moe_combine(const float *y, int64_t R, int64_t ldy, const int32_t *row_of,
+                                      const float *topk_w, int64_t T, int32_t k, int64_t H,
+                                      float *out, int64_t ldo, void *stream) {
+    using namespace h32;
+    if (T < 0 || R < 0 || k < 1 || k > kMaxK || H <= 0 || (H % 4) != 0 || ldy < H || ldo < H)
+        return H32_ERR_INVALID_ARG;
+    if (T == 0) return H32_OK;
+    if (!y || !row_of || !topk_w || !out || T > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(out) || (ldy % 4) != 0 || (ldo % 4) != 0 ||
+        (reinterpret_cast<uintptr_t>(row_of) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
+        return H32_ERR_ALIGNMENT;
+    H32_TRY(check_device(nullptr));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t per_block = static_cast<int64_t>(kCombineThreads) * kCombineVec;   // float4s
+    const int64_t col_blocks = (H / 4 + per_block - 1) / per_block;
+    if (col_blocks > 65535) return H32_ERR_INVALID_ARG;
+    const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>(col_blocks));
+    const cudaError_t e = launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, s, y, R, ldy,
+                                     row_of, topk_w, static_cast<int>(k), H, out, ldo);
+    return launch_status(e != cudaSuccess ? e : cudaGetLastError());
+}

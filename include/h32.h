@@ -280,6 +280,51 @@ h32_status q4_0_x_q4_gemm_tc_experts(const uint8_t *wp, const float *wsc, int64_
                                      float *y, int64_t ldy, int32_t *block_sums, void *stream);
 
 /*
+ * Routing around the expert GEMMs ("Where the engine is going: HRX and the
+ * NPU", section "4-bit activations reach the MoE experts": the route covers
+ * the expert matmuls of a mixture-of-experts model; the pages do not spell
+ * out the router, so the reading taken is stated here).  Per token t:
+ *   - its k experts are those of largest logit, ties to the lower expert id,
+ *     listed by decreasing logit (the softmax is monotonic, so these are the
+ *     k most probable experts);
+ *   - choice j weighs w_j = e_j / s with e_j = exp(l_j - l_0) in fp32 and
+ *     s = the fp32 sum of e_0 .. e_{k-1} in that order (the full softmax's
+ *     top-k probabilities renormalised to sum to 1);
+ * then the (token, choice) pairs are grouped by expert id, and within an
+ * expert by token, which is the grouped order of h32_quantize_act_q4_tc_gather
+ * and q4_0_x_q4_gemm_tc_experts.  Deterministic; the ids, offsets and row maps
+ * are exact, the weights are within a few ulps of an IEEE fp32 evaluation
+ * (the exp is the CUDA libm expf).
+ *   logits     [T][ldl] fp32 device, ldl >= E (4-byte aligned)
+ *   topk_id    [T][k] int32 out: the chosen experts
+ *   topk_w     [T][k] fp32 out: their weights
+ *   expert_off [E+1] int32 out: group e holds grouped rows [off[e], off[e+1]); off[E] = T k
+ *   row_idx    [T k] int32 out: the token of grouped row r
+ *   row_of     [T][k] int32 out: the grouped row of choice j of token t
+ * Requires 1 <= E <= 1024, 1 <= k <= min(E, 32), T k < 2^31.  T = 0 writes
+ * all-zero offsets.  Non-finite logits are outside the contract.
+ */
+h32_status h32_moe_route(const float *logits, int64_t T, int32_t E, int64_t ldl, int32_t k,
+                         int32_t *topk_id, float *topk_w, int32_t *expert_off, int32_t *row_idx,
+                         int32_t *row_of, void *stream);
+
+/*
+ * The weighted combine after the expert GEMMs: the k expert outputs of each
+ * token, in grouped order, added back in token order:
+ *   out[t][h] = acc after acc = fma(topk_w[t][j], y[row_of[t][j]][h], acc)
+ *               for j = 0 .. k-1, from acc = +0 (fp32)
+ *   y       [R][ldy] fp32 device (grouped rows, e.g. the down projection of
+ *           q4_0_x_q4_gemm_tc_experts); row_of, topk_w as from h32_moe_route
+ *   out     [T][ldo] fp32 out
+ * Requires 1 <= k <= 32, H % 4 == 0, ldy, ldo >= H and multiples of 4, y and
+ * out 16-byte aligned.  A row index outside [0, R) records
+ * H32_ERR_DEVICE_GUARD (see h32_device_status) and adds nothing.
+ */
+h32_status h32_moe_combine(const float *y, int64_t R, int64_t ldy, const int32_t *row_of,
+                           const float *topk_w, int64_t T, int32_t k, int64_t H, float *out,
+                           int64_t ldo, void *stream);
+
+/*
  * Synchronize `stream`, then report and clear the device status word of every
  * kernel this library launched on the current device since the last call:
  * H32_OK, H32_ERR_TIMEOUT or H32_ERR_DEVICE_GUARD (or H32_ERR_CUDA when the

@@ -147,3 +147,25 @@ def test_quant_next_bad_arguments(lib):
                  s) == h32.H32_ERR_INVALID_ARG
     assert _call("q4_0_x_q4_gemm_tc_quant_next", p, p, 4, p, p, 8, 8, 64, 128, None, 64, p, p, 4, 1,
                  s) == h32.H32_ERR_INVALID_ARG
+
+
+def test_moe_route_and_combine_bad_arguments(lib):
+    p = ctypes.c_void_p(256)
+    s = ctypes.c_void_p(0)
+    # route: k > E, k > 32, E > 1024, ldl < E, missing offsets
+    assert _call("h32_moe_route", p, 4, 8, 8, 9, p, p, p, p, p, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_moe_route", p, 4, 64, 64, 33, p, p, p, p, p, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_moe_route", p, 4, 1025, 1025, 2, p, p, p, p, p, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_moe_route", p, 4, 16, 15, 2, p, p, p, p, p, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_moe_route", p, 4, 16, 16, 2, p, p, None, p, p, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_moe_route", None, 4, 16, 16, 2, p, p, p, p, p, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_moe_route", ctypes.c_void_p(258), 4, 16, 16, 2, p, p, p, p, p, s) == \
+        h32.H32_ERR_ALIGNMENT
+    # combine: H not a multiple of 4, ldy < H, misaligned y or pitch; T = 0 is a no-op
+    assert _call("h32_moe_combine", p, 8, 6, p, p, 2, 4, 6, p, 6, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_moe_combine", p, 8, 4, p, p, 2, 4, 8, p, 8, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_moe_combine", ctypes.c_void_p(260), 8, 8, p, p, 2, 4, 8, p, 8, s) == \
+        h32.H32_ERR_ALIGNMENT
+    assert _call("h32_moe_combine", p, 8, 10, p, p, 2, 4, 8, p, 8, s) == h32.H32_ERR_ALIGNMENT
+    assert _call("h32_moe_combine", p, 8, 8, p, p, 2, 33, 8, p, 8, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_moe_combine", p, 8, 8, p, p, 0, 4, 8, p, 8, s) == h32.H32_OK

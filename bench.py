@@ -831,8 +831,30 @@ def suite_moe(torch, h32, dev, stream, steps, warmup):
                                       stream=stream)
         combine()
     ms = _events_time(torch, step_layer, steps, warmup, stream)
-    t_route = _events_time(torch, route, steps, warmup, stream)
-    t_comb = _events_time(torch, combine, steps, warmup, stream)
+    # the router's and the combine's device time inside the layer: events around
+    # them on every step of a second pass (a call timed alone in a loop would
+    # measure the host's launch rate, not the kernels)
+    evs = []
+    with torch.cuda.stream(stream):
+        for i in range(warmup + steps):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record(stream)
+            route()
+            e[1].record(stream)
+            h32.h32_quantize_act_q4_tc_gather(xg, ridx_r, xw=xw_gu, xdt=xt_gu, stream=stream)
+            h32.q4_0_x_q4_gemm_tc_experts(wp_gu, ws_gu, xw_gu, xt_gu, offs_r, N_gu, R=R, y=y_gu,
+                                          stream=stream)
+            h32.h32_quantize_act_q4_tc(xn, xw=xw_dn, xdt=xt_dn, stream=stream)
+            h32.q4_0_x_q4_gemm_tc_experts(wp_dn, ws_dn, xw_dn, xt_dn, offs_r, N_dn, R=R, y=y_dn,
+                                          stream=stream)
+            e[2].record(stream)
+            combine()
+            e[3].record(stream)
+            if i >= warmup:
+                evs.append(e)
+    stream.synchronize()
+    t_route = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)
+    t_comb = sum(e[2].elapsed_time(e[3]) for e in evs) / len(evs)
     comb_bytes = R * N_dn * 4 + cfg.T * N_dn * 4 + R * 8
     out.append({"suite": "moe_layer_1024_tokens_route_experts_combine",
                 "value": round(cfg.T / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
@@ -903,7 +925,7 @@ def suite_quant_stream(torch, h32, dev, stream, steps, warmup, peaks):
     return out
 
 
-def run_suite(args):
+def run_suite(args, only_moe=False):
     import torch
     import hadamard_rotated_bit_gb300 as h32
     from hadamard_rotated_bit_gb300 import _build
@@ -913,6 +935,11 @@ def run_suite(args):
     peaks, _ = load_peaks()
     steps, warmup = args.steps, args.warmup
     lines = []
+    if only_moe:
+        lines += suite_moe(torch, h32, dev, stream, steps, warmup)
+        if h32.h32_device_status(stream) != 0:
+            raise RuntimeError("device status not OK after the MoE lines")
+        return lines
     lines += suite_quant_stream(torch, h32, dev, stream, steps, warmup, peaks)
     lines += suite_chain_routes(torch, h32, dev, stream, steps, warmup)
     lines += suite_rotations(torch, h32, dev, stream, steps, warmup)
@@ -943,11 +970,14 @@ def main(argv=None):
     ap.add_argument("--only-quant", choices=["q4", "q8", "q4_tc", "q8_tc"], default=None,
                     help="time the activation quantizer alone on a 16384 x 17408 bf16 matrix "
                          "(a streaming case for profilers)")
+    ap.add_argument("--only-moe", action="store_true",
+                    help="the MoE micro-batch lines of --suite alone (expert GEMMs, and the "
+                         "whole layer with the router and the combine)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.suite:
-        for ln in run_suite(args):
+    if args.suite or args.only_moe:
+        for ln in run_suite(args, only_moe=args.only_moe):
             print(json.dumps(ln), flush=True)
         return
     if args.only_gemm:

@@ -18,8 +18,8 @@
 //   route_group_kernel  one block per expert: its offset is the number of
 //                       choices of lower experts; its rows are the tokens
 //                       that chose it, in token order (ballot prefix sums)
-//   combine_kernel      one block per token (x) and column range (y): 16-byte loads
-//                       of the token's k rows, fma in choice order
+//   combine_kernel      one block per token (x) and 128 float4 columns (y): 16-byte
+//                       loads of the token's k rows, fma in choice order
 #include "h32_common.cuh"
 
 namespace h32 {
@@ -30,9 +30,8 @@ __device__ uint32_t g_moe_status;   // kStatusGuard: a combine row index out of 
 constexpr int kMaxE = 1024;         // experts a router call handles
 constexpr int kMaxK = 32;           // choices per token (one lane each)
 constexpr int kTopkWarps = 8;       // tokens per block of route_topk_kernel
-constexpr int kGroupThreads = 256;
-constexpr int kCombineThreads = 128;
-constexpr int kCombineVec = 4;      // float4 columns per thread and block
+constexpr int kGroupThreads = 1024;
+constexpr int kCombineThreads = 128;   // one float4 column each
 
 // (value, id) a beats b: larger value, or equal value and lower id; id < 0 = none
 __device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
@@ -41,6 +40,8 @@ __device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
 }
 
+// NPER: logits per lane (expert lane + 32 i, i < NPER), a power of two >= E / 32
+template <int NPER>
 __global__ void __launch_bounds__(kTopkWarps * 32)
     route_topk_kernel(const float *__restrict__ logits, int T, int E, int64_t ldl, int k,
                       int32_t *__restrict__ topk_id, float *__restrict__ topk_w) {
@@ -50,12 +51,11 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
     const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
     if (t >= T) return;
     const float *row = logits + static_cast<int64_t>(t) * ldl;
-    const int nper = (E + 31) >> 5;   // logits per lane: expert lane + 32 i
-    float v[kMaxE / 32];
+    float v[NPER];
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
+    for (int i = 0; i < NPER; ++i) {
         const int e = lane + 32 * i;
-        v[i] = (i < nper && e < E) ? row[e] : 0.0f;
+        v[i] = e < E ? row[e] : 0.0f;
     }
     uint32_t taken = 0;   // bit i: expert lane + 32 i already chosen
     int my_id = -1;       // lane j keeps choice j
@@ -64,9 +64,9 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
         float bv = 0.0f;
         int bi = -1;
 #pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i) {
+        for (int i = 0; i < NPER; ++i) {
             const int e = lane + 32 * i;
-            if (i < nper && e < E && !((taken >> i) & 1u) && beats(v[i], e, bv, bi)) {
+            if (e < E && !((taken >> i) & 1u) && beats(v[i], e, bv, bi)) {
                 bv = v[i];
                 bi = e;
             }
@@ -127,9 +127,18 @@ __global__ void __launch_bounds__(kGroupThreads)
     const int e = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t n = static_cast<int64_t>(T) * k;
-    // choices of lower experts (this expert's first row) and of this expert
+    // choices of lower experts (this expert's first row) and of this expert;
+    // 16-byte loads (topk_id is 16-byte aligned), independent within a thread
     int lt = 0, eq = 0;
-    for (int64_t i = threadIdx.x; i < n; i += kGroupThreads) {
+    const int64_t n4 = n / 4;
+    const int4 *id4 = reinterpret_cast<const int4 *>(topk_id);
+#pragma unroll 4
+    for (int64_t i = threadIdx.x; i < n4; i += kGroupThreads) {
+        const int4 q = id4[i];
+        lt += (q.x < e) + (q.y < e) + (q.z < e) + (q.w < e);
+        eq += (q.x == e) + (q.y == e) + (q.z == e) + (q.w == e);
+    }
+    for (int64_t i = 4 * n4 + threadIdx.x; i < n; i += kGroupThreads) {
         const int id = topk_id[i];
         lt += id < e;
         eq += id == e;
@@ -158,9 +167,12 @@ __global__ void __launch_bounds__(kGroupThreads)
     for (int t0 = 0; t0 < T; t0 += kGroupThreads) {
         const int t = t0 + threadIdx.x;
         int j = -1;
-        if (t < T)
+        if (t < T) {
+            const int32_t *ids = topk_id + static_cast<int64_t>(t) * k;
+#pragma unroll 8
             for (int c = 0; c < k; ++c)
-                if (topk_id[static_cast<int64_t>(t) * k + c] == e) j = c;
+                if (ids[c] == e) j = c;
+        }
         int tot;
         const int pos = block_prefix(j >= 0, warp_tot, &tot);
         if (j >= 0) {
@@ -191,25 +203,22 @@ __global__ void __launch_bounds__(kCombineThreads)
         s_w[threadIdx.x] = topk_w[t * k + threadIdx.x];
     }
     __syncthreads();
-    const int64_t h4 = H / 4;
-#pragma unroll
-    for (int u = 0; u < kCombineVec; ++u) {
-        const int64_t c = (static_cast<int64_t>(blockIdx.y) * kCombineVec + u) * kCombineThreads +
-                          threadIdx.x;
-        if (c >= h4) break;
-        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        for (int j = 0; j < k; ++j) {
-            const int64_t r = s_row[j];
-            if (r < 0) continue;   // a guarded index adds nothing
-            const float w = s_w[j];
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(y + r * ldy) + c);
-            acc.x = __fmaf_rn(w, v.x, acc.x);
-            acc.y = __fmaf_rn(w, v.y, acc.y);
-            acc.z = __fmaf_rn(w, v.z, acc.z);
-            acc.w = __fmaf_rn(w, v.w, acc.w);
-        }
-        reinterpret_cast<float4 *>(out + t * ldo)[c] = acc;
+    const int64_t c = static_cast<int64_t>(blockIdx.y) * kCombineThreads + threadIdx.x;
+    if (c >= H / 4) return;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    // the loads of several rows are in flight together; the fmas stay in order
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+        const int64_t r = s_row[j];
+        if (r < 0) continue;   // a guarded index adds nothing
+        const float w = s_w[j];
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(y + r * ldy) + c);
+        acc.x = __fmaf_rn(w, v.x, acc.x);
+        acc.y = __fmaf_rn(w, v.y, acc.y);
+        acc.z = __fmaf_rn(w, v.z, acc.z);
+        acc.w = __fmaf_rn(w, v.w, acc.w);
     }
+    reinterpret_cast<float4 *>(out + t * ldo)[c] = acc;
 }
 
 }  // namespace
@@ -238,16 +247,31 @@ extern "C" h32_status h32_moe_route(const float *logits, int64_t T, int32_t E, i
     if (T > 0 && (!logits || !topk_id || !topk_w || !row_idx || !row_of))
         return H32_ERR_INVALID_ARG;
     if ((logits && (reinterpret_cast<uintptr_t>(logits) & 3u)) ||
-        (reinterpret_cast<uintptr_t>(expert_off) & 3u))
+        (reinterpret_cast<uintptr_t>(expert_off) & 3u) || (topk_id && !aligned16(topk_id)) ||
+        (topk_w && (reinterpret_cast<uintptr_t>(topk_w) & 3u)) ||
+        (row_idx && (reinterpret_cast<uintptr_t>(row_idx) & 3u)) ||
+        (row_of && (reinterpret_cast<uintptr_t>(row_of) & 3u)))
         return H32_ERR_ALIGNMENT;
     H32_TRY(check_device(nullptr));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int t32 = static_cast<int>(T);
     if (T > 0) {
         const dim3 grid(static_cast<unsigned>((T + kTopkWarps - 1) / kTopkWarps));
-        const cudaError_t e1 = launch_pdl(route_topk_kernel, grid, dim3(kTopkWarps * 32), 0, s,
-                                          logits, t32, static_cast<int>(E), ldl,
-                                          static_cast<int>(k), topk_id, topk_w);
+        const dim3 block(kTopkWarps * 32);
+        const int ei = static_cast<int>(E), ki = static_cast<int>(k);
+        cudaError_t e1;
+        if (E <= 32)
+            e1 = launch_pdl(route_topk_kernel<1>, grid, block, 0, s, logits, t32, ei, ldl, ki, topk_id, topk_w);
+        else if (E <= 64)
+            e1 = launch_pdl(route_topk_kernel<2>, grid, block, 0, s, logits, t32, ei, ldl, ki, topk_id, topk_w);
+        else if (E <= 128)
+            e1 = launch_pdl(route_topk_kernel<4>, grid, block, 0, s, logits, t32, ei, ldl, ki, topk_id, topk_w);
+        else if (E <= 256)
+            e1 = launch_pdl(route_topk_kernel<8>, grid, block, 0, s, logits, t32, ei, ldl, ki, topk_id, topk_w);
+        else if (E <= 512)
+            e1 = launch_pdl(route_topk_kernel<16>, grid, block, 0, s, logits, t32, ei, ldl, ki, topk_id, topk_w);
+        else
+            e1 = launch_pdl(route_topk_kernel<32>, grid, block, 0, s, logits, t32, ei, ldl, ki, topk_id, topk_w);
         if (e1 != cudaSuccess) return launch_status(e1);
     }
     // with T = 0 this writes all-zero offsets
@@ -271,8 +295,7 @@ extern "C" h32_status h32_moe_combine(const float *y, int64_t R, int64_t ldy, co
         return H32_ERR_ALIGNMENT;
     H32_TRY(check_device(nullptr));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t per_block = static_cast<int64_t>(kCombineThreads) * kCombineVec;   // float4s
-    const int64_t col_blocks = (H / 4 + per_block - 1) / per_block;
+    const int64_t col_blocks = (H / 4 + kCombineThreads - 1) / kCombineThreads;
     if (col_blocks > 65535) return H32_ERR_INVALID_ARG;
     const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>(col_blocks));
     const cudaError_t e = launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, s, y, R, ldy,

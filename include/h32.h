@@ -296,7 +296,8 @@ h32_status q4_0_x_q4_gemm_tc_experts(const uint8_t *wp, const float *wsc, int64_
  * are exact, the weights are within a few ulps of an IEEE fp32 evaluation
  * (the exp is the CUDA libm expf).
  *   logits     [T][ldl] fp32 device, ldl >= E (4-byte aligned)
- *   topk_id    [T][k] int32 out: the chosen experts
+ *   topk_id    [T][k] int32 out: the chosen experts (16-byte aligned; the other
+ *              outputs 4-byte aligned)
  *   topk_w     [T][k] fp32 out: their weights
  *   expert_off [E+1] int32 out: group e holds grouped rows [off[e], off[e+1]); off[E] = T k
  *   row_idx    [T k] int32 out: the token of grouped row r

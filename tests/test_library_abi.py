@@ -161,6 +161,8 @@ def test_moe_route_and_combine_bad_arguments(lib):
     assert _call("h32_moe_route", None, 4, 16, 16, 2, p, p, p, p, p, s) == h32.H32_ERR_INVALID_ARG
     assert _call("h32_moe_route", ctypes.c_void_p(258), 4, 16, 16, 2, p, p, p, p, p, s) == \
         h32.H32_ERR_ALIGNMENT
+    assert _call("h32_moe_route", p, 4, 16, 16, 2, ctypes.c_void_p(264), p, p, p, p, s) == \
+        h32.H32_ERR_ALIGNMENT
     # combine: H not a multiple of 4, ldy < H, misaligned y or pitch; T = 0 is a no-op
     assert _call("h32_moe_combine", p, 8, 6, p, p, 2, 4, 6, p, 6, s) == h32.H32_ERR_INVALID_ARG
     assert _call("h32_moe_combine", p, 8, 4, p, p, 2, 4, 8, p, 8, s) == h32.H32_ERR_INVALID_ARG

@@ -5,6 +5,9 @@
 #include "h32_common.cuh"
 
 namespace h32 {
+// the status word of the router and combine kernels (h32_moe.cu)
+h32_status moe_read_and_clear_status(cudaStream_t s);
+
 namespace {
 
 std::atomic<uint64_t> g_wait_polls{kDefaultWaitPolls};

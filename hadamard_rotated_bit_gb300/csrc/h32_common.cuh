@@ -35,7 +35,6 @@ void note_error(const char *what);        // remember a non-CUDA failure text
 h32_status quant_read_and_clear_status(cudaStream_t s);
 h32_status gemm_read_and_clear_status(cudaStream_t s);
 h32_status tc_read_and_clear_status(cudaStream_t s);
-h32_status moe_read_and_clear_status(cudaStream_t s);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -24,6 +24,7 @@ __all__ = [
     "h32_last_cuda_error", "h32_quantize_act_q4_tc", "h32_prepack_weights_q4_0_tc",
     "q4_0_x_q4_gemm_tc", "h32_quantize_act_q4_tc_gather", "q4_0_x_q4_gemm_tc_experts",
     "h32_quantize_act_q8_tc", "q4_0_x_q8_gemm_tc", "q4_0_x_q4_gemm_tc_quant_next",
+    "h32_moe_route", "h32_moe_combine",
 ]
 
 
@@ -490,3 +491,21 @@ def h32_moe_combine(y, row_of, topk_w, out=None, stream=None):
                                ldo, _stream(stream))
     _check("h32_moe_combine", st)
     return out
+
+
+# --------------------------------------------------------------------------
+# optional per-call tracing (H32_TRACE=1: device time per call; H32_TRACE=hash:
+# also a hash of every output), off by default; see trace.py
+# --------------------------------------------------------------------------
+from . import trace as _trace  # noqa: E402
+
+_COMPUTE_CALLS = (
+    "h32_quantize_act_q4", "h32_quantize_act_q8", "h32_rotate_quantize_weights_q4_0",
+    "q4_0_x_q4_gemm", "q4_0_x_q8_gemm", "q4_0_x_q4_gemm_experts", "h32_quantize_act_q4_tc",
+    "h32_quantize_act_q8_tc", "h32_prepack_weights_q4_0_tc", "q4_0_x_q4_gemm_tc",
+    "q4_0_x_q8_gemm_tc", "h32_quantize_act_q4_tc_gather", "q4_0_x_q4_gemm_tc_experts",
+    "q4_0_x_q4_gemm_tc_quant_next", "h32_moe_route", "h32_moe_combine",
+)
+for _name in _COMPUTE_CALLS:
+    globals()[_name] = _trace.traced(_name)(globals()[_name])
+del _name

@@ -63,7 +63,9 @@ def _check_route(h32, l, k, ldl_pad=0):
     assert np.array_equal(np_of(ridx), rridx)
     assert np.array_equal(np_of(row_of), rrow)
     gw = np_of(w).astype(np.float64)
-    assert np.max(np.abs(gw - rw) / rw) <= _w_tol(k)
+    # relative bound, with the smallest normal fp32 as the floor where a weight
+    # underflows (subnormal or zero on both sides)
+    assert np.all(np.abs(gw - rw) <= _w_tol(k) * rw + 2.0 ** -126)
     return rid, rw, roff, rridx, rrow
 
 
@@ -79,6 +81,17 @@ def test_route_moe_config(h32):
                                    (33, 1000, 8), (257, 1024, 3), (9, 64, 1)])
 def test_route_ragged_and_ties(h32, T, E, k):
     _check_route(h32, _logits(T, E, T * 7 + E), k)
+
+
+def test_route_wide_logits_and_many_tokens(h32):
+    """Logits spread so far apart that weights underflow (exp of differences
+    below -87 is subnormal or zero), and a token count whose grouping walks
+    many chunks of tokens."""
+    r = np.random.default_rng(21)
+    wide = (r.standard_normal((300, 40)) * 60.0).astype(np.float32)
+    _, rw, _, _, _ = _check_route(h32, wide, 8)
+    assert np.any(rw == 0.0) and np.any((rw > 0) & (rw < 2.0 ** -126))
+    _check_route(h32, _logits(70000, 16, 22), 2)
 
 
 def test_route_row_pitch_and_equal_rows(h32):

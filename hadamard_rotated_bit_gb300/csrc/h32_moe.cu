@@ -48,9 +48,9 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kTopkWarps + (threadIdx.x >> 5);
     if (t >= T) return;
-    const float *row = logits + static_cast<int64_t>(t) * ldl;
+    const float *row = logits + t * ldl;
     float v[NPER];
 #pragma unroll
     for (int i = 0; i < NPER; ++i) {
@@ -93,13 +93,13 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
     float s = 0.0f;
     for (int j = 0; j < k; ++j) s = __fadd_rn(s, __shfl_sync(0xFFFFFFFFu, ex, j));
     if (lane < k) {
-        topk_id[static_cast<int64_t>(t) * k + lane] = my_id;
-        topk_w[static_cast<int64_t>(t) * k + lane] = __fdiv_rn(ex, s);
+        topk_id[t * k + lane] = my_id;
+        topk_w[t * k + lane] = __fdiv_rn(ex, s);
     }
 }
 
 // exclusive prefix of `flag` over the block's threads in thread order, and the
-// block's total (all threads get it); scratch holds one int per warp
+// block's total (all threads get it); warp_tot is shared memory, one int per warp
 __device__ __forceinline__ int block_prefix(bool flag, int *warp_tot, int *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t bal = __ballot_sync(0xFFFFFFFFu, flag);
@@ -164,11 +164,11 @@ __global__ void __launch_bounds__(kGroupThreads)
     }
     // this expert's rows: the tokens that chose it, in token order
     int base = first;
-    for (int t0 = 0; t0 < T; t0 += kGroupThreads) {
-        const int t = t0 + threadIdx.x;
+    for (int64_t t0 = 0; t0 < T; t0 += kGroupThreads) {
+        const int64_t t = t0 + threadIdx.x;
         int j = -1;
         if (t < T) {
-            const int32_t *ids = topk_id + static_cast<int64_t>(t) * k;
+            const int32_t *ids = topk_id + t * k;
 #pragma unroll 8
             for (int c = 0; c < k; ++c)
                 if (ids[c] == e) j = c;
@@ -177,8 +177,8 @@ __global__ void __launch_bounds__(kGroupThreads)
         const int pos = block_prefix(j >= 0, warp_tot, &tot);
         if (j >= 0) {
             const int r = base + pos;
-            row_idx[r] = t;
-            row_of[static_cast<int64_t>(t) * k + j] = r;
+            row_idx[r] = static_cast<int32_t>(t);
+            row_of[t * k + j] = r;
         }
         base += tot;
     }

@@ -146,12 +146,6 @@ def _check(fn: str, st: int):
         raise H32Error(fn, st)
 
 
-def _cuda(t, name):
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
-    return t
-
-
 def _rows(t, name):
     """2-D tensor with unit stride in its last dimension; returns its row pitch."""
     if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
@@ -159,25 +153,96 @@ def _rows(t, name):
     return t.stride(0) if t.shape[0] > 1 else t.shape[1]
 
 
+class _AtLeast(int):
+    """A shape entry the tensor may exceed (rows beyond those used, a row pitch)."""
+
+
+def _ge(n) -> _AtLeast:
+    return _AtLeast(int(n))
+
+
+def _fp16_bits():
+    torch = _torch()
+    return tuple(d for d in (torch.int16, getattr(torch, "uint16", None), torch.float16) if d)
+
+
+def _need(t, name, dtypes, shape, pitched=False):
+    """Check a tensor the library reaches only through a raw pointer, so that no
+    kernel reads or writes past it: dtype, shape (entries made with _ge may be
+    exceeded, the others must match) and layout (contiguous, or with `pitched`
+    2-D rows of unit stride that do not overlap).  Returns the tensor; the
+    device is checked by _same_gpu once all of a call's tensors are."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected " + " or ".join(map(str, dtypes)))
+    want = "(" + ", ".join((">=" if isinstance(d, _AtLeast) else "") + str(int(d))
+                           for d in shape) + ")"
+    if t.dim() != len(shape) or any(h < d or (not isinstance(d, _AtLeast) and h != d)
+                                    for h, d in zip(t.shape, shape)):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {want}")
+    if pitched:
+        if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1) or \
+                (t.shape[0] > 1 and t.stride(0) < t.shape[1]):
+            raise ValueError(f"{name} must be 2-D with contiguous, non-overlapping rows")
+    elif not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _same_gpu(*named):
+    """Every (name, tensor) given (None skipped) is on one CUDA device."""
+    dev = None
+    for name, t in named:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the call's other tensors on {dev}")
+
+
+def _act_dtype(x, name="x"):
+    torch = _torch()
+    if x.dtype == torch.bfloat16:
+        return H32_IN_BF16
+    if x.dtype == torch.float32:
+        return H32_IN_F32
+    raise ValueError(f"{name} must be bf16 or fp32")
+
+
+def _sums(block_sums, rows, N, nb, dev):
+    """The optional block-sum output: True allocates it, a tensor is checked."""
+    torch = _torch()
+    if block_sums is True:
+        return torch.empty((rows, N, nb), dtype=torch.int32, device=dev)
+    if block_sums is None or block_sums is False:
+        return None
+    return _need(block_sums, "block_sums", (torch.int32,), (_ge(rows), N, nb))
+
+
 # --------------------------------------------------------------------------
 # quantizers
 # --------------------------------------------------------------------------
 def _quantize_act(fn_name, bits, x, rotate, xq, xd, stream):
     torch = _torch()
-    _cuda(x, "x")
-    if x.dtype == torch.bfloat16:
-        dt = H32_IN_BF16
-    elif x.dtype == torch.float32:
-        dt = H32_IN_F32
-    else:
-        raise ValueError("x must be bf16 or fp32")
+    dt = _act_dtype(x)
+    _need(x, "x", (x.dtype,), (_ge(0), _ge(0)), pitched=True)
     ldx = _rows(x, "x")
     M, K = x.shape
+    dev = x.device
+    qcols, qtype = (K // 2, torch.uint8) if bits == 4 else (K, torch.int8)
     if xq is None:
-        xq = torch.empty((M, K // 2 if bits == 4 else K),
-                         dtype=torch.uint8 if bits == 4 else torch.int8, device=x.device)
+        xq = torch.empty((M, qcols), dtype=qtype, device=dev)
+    # code buffers are raw bytes: 8-bit codes may sit in an int8 or a uint8 tensor
+    _need(xq, "xq", (qtype,) if bits == 4 else (torch.int8, torch.uint8), (_ge(M), qcols))
     if xd is None:
-        xd = torch.empty((M, K // 32), dtype=torch.float32, device=x.device)
+        xd = torch.empty((M, K // 32), dtype=torch.float32, device=dev)
+    _need(xd, "xd", (torch.float32,), (_ge(M), K // 32))
+    _same_gpu(("x", x), ("xq", xq), ("xd", xd))
     st = getattr(lib(), fn_name)(_ptr(x), dt, M, K, ldx, _ptr(xq), _ptr(xd), _rot_arg(rotate),
                                  _stream(stream))
     _check(fn_name, st)
@@ -197,14 +262,17 @@ def h32_quantize_act_q8(x, rotate=True, xq=None, xd=None, stream=None):
 def h32_rotate_quantize_weights_q4_0(w, rotate=True, wq=None, wd=None, stream=None):
     """w [N][K] fp32 (contiguous) -> (wq [N][K/2] uint8, wd [N][K/32] int16 holding fp16 bits)."""
     torch = _torch()
-    _cuda(w, "w")
-    if w.dtype != torch.float32 or not w.is_contiguous() or w.dim() != 2:
+    if not isinstance(w, torch.Tensor) or w.dim() != 2:
         raise ValueError("w must be a contiguous 2-D fp32 tensor")
     N, K = w.shape
+    _need(w, "w", (torch.float32,), (N, K))
     if wq is None:
         wq = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    _need(wq, "wq", (torch.uint8,), (_ge(N), K // 2))
     if wd is None:
         wd = torch.empty((N, K // 32), dtype=torch.int16, device=w.device)
+    _need(wd, "wd", _fp16_bits(), (_ge(N), K // 32))
+    _same_gpu(("w", w), ("wq", wq), ("wd", wd))
     st = lib().h32_rotate_quantize_weights_q4_0(_ptr(w), N, K, _rot_arg(rotate), _ptr(wq),
                                                 _ptr(wd), _stream(stream))
     _check("h32_rotate_quantize_weights_q4_0", st)
@@ -216,21 +284,24 @@ def h32_rotate_quantize_weights_q4_0(w, rotate=True, wq=None, wd=None, stream=No
 # --------------------------------------------------------------------------
 def _gemm(fn_name, wq, wd, xq, xd, y, block_sums, stream):
     torch = _torch()
-    for t, n in ((wq, "wq"), (wd, "wd"), (xq, "xq"), (xd, "xd")):
-        _cuda(t, n)
-        if not t.is_contiguous():
-            raise ValueError(f"{n} must be contiguous")
-    N = wq.shape[0]
-    K = wq.shape[1] * 2
+    if wq.dim() != 2 or xq.dim() != 2:
+        raise ValueError("wq and xq must be 2-D")
+    N, K = wq.shape[0], wq.shape[1] * 2
     M = xq.shape[0]
+    dev = wq.device
+    _need(wq, "wq", (torch.uint8,), (N, K // 2))
+    _need(wd, "wd", _fp16_bits(), (_ge(N), K // 32))
+    if fn_name == "q4_0_x_q8_gemm":
+        _need(xq, "xq", (torch.int8, torch.uint8), (M, K))
+    else:
+        _need(xq, "xq", (torch.uint8,), (M, K // 2))
+    _need(xd, "xd", (torch.float32,), (_ge(M), K // 32))
     if y is None:
-        y = torch.empty((M, N), dtype=torch.float32, device=wq.device)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _need(y, "y", (torch.float32,), (_ge(M), _ge(N)), pitched=True)
     ldy = _rows(y, "y")
-    S = None
-    if block_sums is True:
-        S = torch.empty((M, N, K // 32), dtype=torch.int32, device=wq.device)
-    elif block_sums is not None and block_sums is not False:
-        S = block_sums
+    S = _sums(block_sums, M, N, K // 32, dev)
+    _same_gpu(("wq", wq), ("wd", wd), ("xq", xq), ("xd", xd), ("y", y), ("S", S))
     st = getattr(lib(), fn_name)(_ptr(wq), _ptr(wd), _ptr(xq), _ptr(xd), M, N, K, _ptr(y), ldy,
                                  _ptr(S), _stream(stream))
     _check(fn_name, st)
@@ -253,19 +324,27 @@ def q4_0_x_q4_gemm_experts(wq, wd, xq, xd, row_idx, expert_off, R, y=None, block
                            stream=None):
     """Expert-batched product: wq [E][N][K/2], wd [E][N][K/32]; rows grouped by expert."""
     torch = _torch()
-    for t, n in ((wq, "wq"), (wd, "wd"), (xq, "xq"), (xd, "xd"), (expert_off, "expert_off")):
-        _cuda(t, n)
-        if not t.is_contiguous():
-            raise ValueError(f"{n} must be contiguous")
+    if wq.dim() != 3 or xq.dim() != 2:
+        raise ValueError("wq must be 3-D [E][N][K/2] and xq 2-D")
     E, N, K = wq.shape[0], wq.shape[1], wq.shape[2] * 2
+    T = xq.shape[0]
+    dev = wq.device
+    _need(wq, "wq", (torch.uint8,), (E, N, K // 2))
+    _need(wd, "wd", _fp16_bits(), (E, N, K // 32))
+    _need(xq, "xq", (torch.uint8,), (T, K // 2))
+    _need(xd, "xd", (torch.float32,), (_ge(T), K // 32))
+    if row_idx is not None:
+        _need(row_idx, "row_idx", (torch.int32,), (_ge(R),))
+    elif T < R:
+        raise ValueError("without row_idx, xq must have at least R rows")
+    _need(expert_off, "expert_off", (torch.int32,), (_ge(E + 1),))
     if y is None:
-        y = torch.empty((R, N), dtype=torch.float32, device=wq.device)
+        y = torch.empty((R, N), dtype=torch.float32, device=dev)
+    _need(y, "y", (torch.float32,), (_ge(R), _ge(N)), pitched=True)
     ldy = _rows(y, "y")
-    S = None
-    if block_sums is True:
-        S = torch.empty((R, N, K // 32), dtype=torch.int32, device=wq.device)
-    elif block_sums is not None and block_sums is not False:
-        S = block_sums
+    S = _sums(block_sums, R, N, K // 32, dev)
+    _same_gpu(("wq", wq), ("wd", wd), ("xq", xq), ("xd", xd),
+              ("row_idx", row_idx), ("expert_off", expert_off), ("y", y), ("S", S))
     st = lib().q4_0_x_q4_gemm_experts(_ptr(wq), _ptr(wd), E, _ptr(xq), _ptr(xd), _ptr(row_idx),
                                       xq.shape[0], _ptr(expert_off), R, N, K, _ptr(y), ldy,
                                       _ptr(S), _stream(stream))
@@ -299,19 +378,18 @@ def h32_quantize_act_q8_tc(x, rotate=True, xw=None, xdt=None, stream=None):
 
 def _quantize_tc(fn, bytes_per_code, x, rotate, xw, xdt, stream):
     torch = _torch()
-    _cuda(x, "x")
-    if x.dtype == torch.bfloat16:
-        dt = H32_IN_BF16
-    elif x.dtype == torch.float32:
-        dt = H32_IN_F32
-    else:
-        raise ValueError("x must be bf16 or fp32")
+    dt = _act_dtype(x)
+    _need(x, "x", (x.dtype,), (_ge(0), _ge(0)), pitched=True)
     ldx = _rows(x, "x")
     M, K = x.shape
+    dev = x.device
     if xw is None:
-        xw = torch.empty((M, K * bytes_per_code), dtype=torch.uint8, device=x.device)
+        xw = torch.empty((M, K * bytes_per_code), dtype=torch.uint8, device=dev)
+    _need(xw, "xw", (torch.uint8,), (_ge(M), K * bytes_per_code))
     if xdt is None:
-        xdt = torch.zeros((K // 32, _round4(M)), dtype=torch.float32, device=x.device)
+        xdt = torch.zeros((K // 32, _round4(M)), dtype=torch.float32, device=dev)
+    _need(xdt, "xdt", (torch.float32,), (_ge(K // 32), _ge(M)))
+    _same_gpu(("x", x), ("xw", xw), ("xdt", xdt))
     st = getattr(lib(), fn)(_ptr(x), dt, M, K, ldx, _ptr(xw), _ptr(xdt), xdt.shape[1],
                             _rot_arg(rotate), _stream(stream))
     _check(fn, st)
@@ -322,13 +400,19 @@ def h32_prepack_weights_q4_0_tc(wq, wd, wp=None, wsc=None, stream=None):
     """Q4_0 planes (wq [N][K/2], wd [N][K/32] fp16 bits) -> tc form
     (wp [N][K] uint8, wsc [N][ldws] fp32 = d, ldws = K/32 rounded up to 4)."""
     torch = _torch()
-    _cuda(wq, "wq")
-    _cuda(wd, "wd")
+    if wq.dim() != 2:
+        raise ValueError("wq must be 2-D [N][K/2]")
     N, K = wq.shape[0], wq.shape[1] * 2
+    dev = wq.device
+    _need(wq, "wq", (torch.uint8,), (N, K // 2))
+    _need(wd, "wd", _fp16_bits(), (_ge(N), K // 32))
     if wp is None:
-        wp = torch.empty((N, K), dtype=torch.uint8, device=wq.device)
+        wp = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    _need(wp, "wp", (torch.uint8,), (_ge(N), K))
     if wsc is None:
-        wsc = torch.empty((N, _round4(K // 32)), dtype=torch.float32, device=wq.device)
+        wsc = torch.empty((N, _round4(K // 32)), dtype=torch.float32, device=dev)
+    _need(wsc, "wsc", (torch.float32,), (_ge(N), _ge(K // 32)))
+    _same_gpu(("wq", wq), ("wd", wd), ("wp", wp), ("wsc", wsc))
     st = lib().h32_prepack_weights_q4_0_tc(_ptr(wq), _ptr(wd), N, K, _ptr(wp), _ptr(wsc),
                                            wsc.shape[1], _stream(stream))
     _check("h32_prepack_weights_q4_0_tc", st)
@@ -345,19 +429,32 @@ def q4_0_x_q8_gemm_tc(wp, wsc, xw8, xdt, M=None, y=None, block_sums=None, stream
     return _gemm_tc("q4_0_x_q8_gemm_tc", wp, wsc, xw8, xdt, M, y, block_sums, stream)
 
 
+def _tc_operands(wp, wsc, xw, xdt, rows, bytes_per_code, weight_rows=None):
+    """Check the tc-form operands of a GEMM over `rows` activation rows; returns (N, K)."""
+    torch = _torch()
+    if wp.dim() != 2:
+        raise ValueError("wp must be 2-D [N][K]")
+    N, K = wp.shape
+    dev = wp.device
+    _need(wp, "wp", (torch.uint8,), (N, K))
+    _need(wsc, "wsc", (torch.float32,), (N, _ge(K // 32)))
+    _need(xw, "xw", (torch.uint8,), (_ge(rows), K * bytes_per_code))
+    _need(xdt, "xdt", (torch.float32,), (_ge(K // 32), _ge(rows)))
+    return N, K
+
+
 def _gemm_tc(fn, wp, wsc, xw, xdt, M, y, block_sums, stream):
     torch = _torch()
-    N, K = wp.shape
     if M is None:
         M = xw.shape[0]
+    N, K = _tc_operands(wp, wsc, xw, xdt, M, 2 if fn == "q4_0_x_q8_gemm_tc" else 1)
+    dev = wp.device
     if y is None:
-        y = torch.empty((M, N), dtype=torch.float32, device=wp.device)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _need(y, "y", (torch.float32,), (_ge(M), _ge(N)), pitched=True)
     ldy = _rows(y, "y")
-    S = None
-    if block_sums is True:
-        S = torch.empty((M, N, K // 32), dtype=torch.int32, device=wp.device)
-    elif block_sums is not None and block_sums is not False:
-        S = block_sums
+    S = _sums(block_sums, M, N, K // 32, dev)
+    _same_gpu(("wp", wp), ("wsc", wsc), ("xw", xw), ("xdt", xdt), ("y", y), ("S", S))
     st = getattr(lib(), fn)(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt), xdt.shape[1],
                             M, N, K, _ptr(y), ldy, _ptr(S), _stream(stream))
     _check(fn, st)
@@ -368,23 +465,22 @@ def h32_quantize_act_q4_tc_gather(x, row_idx, rotate=True, xw=None, xdt=None, st
     """x [T][K] bf16/fp32, row_idx [R] int32 -> (xw [R][K] uint8, xdt [K/32][ldxd] fp32):
     output row r is the tc-form quantization of x[row_idx[r]]."""
     torch = _torch()
-    _cuda(x, "x")
-    _cuda(row_idx, "row_idx")
-    if x.dtype == torch.bfloat16:
-        dt = H32_IN_BF16
-    elif x.dtype == torch.float32:
-        dt = H32_IN_F32
-    else:
-        raise ValueError("x must be bf16 or fp32")
-    if row_idx.dtype != torch.int32 or not row_idx.is_contiguous():
-        raise ValueError("row_idx must be a contiguous int32 tensor")
+    dt = _act_dtype(x)
+    _need(x, "x", (x.dtype,), (_ge(0), _ge(0)), pitched=True)
     ldx = _rows(x, "x")
     T, K = x.shape
+    dev = x.device
+    if row_idx.dim() != 1:
+        raise ValueError("row_idx must be 1-D")
     R = row_idx.shape[0]
+    _need(row_idx, "row_idx", (torch.int32,), (R,))
     if xw is None:
-        xw = torch.empty((R, K), dtype=torch.uint8, device=x.device)
+        xw = torch.empty((R, K), dtype=torch.uint8, device=dev)
+    _need(xw, "xw", (torch.uint8,), (_ge(R), K))
     if xdt is None:
-        xdt = torch.zeros((K // 32, _round4(R)), dtype=torch.float32, device=x.device)
+        xdt = torch.zeros((K // 32, _round4(R)), dtype=torch.float32, device=dev)
+    _need(xdt, "xdt", (torch.float32,), (_ge(K // 32), _ge(R)))
+    _same_gpu(("x", x), ("row_idx", row_idx), ("xw", xw), ("xdt", xdt))
     st = lib().h32_quantize_act_q4_tc_gather(_ptr(x), dt, T, K, ldx, _ptr(row_idx), R, _ptr(xw),
                                              _ptr(xdt), xdt.shape[1], _rot_arg(rotate),
                                              _stream(stream))
@@ -398,20 +494,21 @@ def q4_0_x_q4_gemm_tc_experts(wp, wsc, xw, xdt, expert_off, N, R=None, y=None, b
     repacked planes stacked), xw [R][K] / xdt [K/32][ldxd] in grouped order,
     expert_off [E+1] int32 -> y [R][N] fp32 in grouped order."""
     torch = _torch()
-    EN, K = wp.shape
-    if EN % N != 0:
-        raise ValueError("wp rows must be E * N")
-    E = EN // N
+    if wp.dim() != 2 or N <= 0 or wp.shape[0] % N != 0:
+        raise ValueError("wp must be 2-D with E * N rows")
+    E = wp.shape[0] // N
     if R is None:
         R = xw.shape[0]
+    EN, K = _tc_operands(wp, wsc, xw, xdt, R, 1)
+    dev = wp.device
+    _need(expert_off, "expert_off", (torch.int32,), (_ge(E + 1),))
     if y is None:
-        y = torch.empty((R, N), dtype=torch.float32, device=wp.device)
+        y = torch.empty((R, N), dtype=torch.float32, device=dev)
+    _need(y, "y", (torch.float32,), (_ge(R), _ge(N)), pitched=True)
     ldy = _rows(y, "y") if R > 0 else N
-    S = None
-    if block_sums is True:
-        S = torch.empty((R, N, K // 32), dtype=torch.int32, device=wp.device)
-    elif block_sums is not None and block_sums is not False:
-        S = block_sums
+    S = _sums(block_sums, R, N, K // 32, dev)
+    _same_gpu(("wp", wp), ("wsc", wsc), ("xw", xw), ("xdt", xdt),
+              ("expert_off", expert_off), ("y", y), ("S", S))
     st = lib().q4_0_x_q4_gemm_tc_experts(_ptr(wp), _ptr(wsc), wsc.shape[1], E, _ptr(xw), _ptr(xdt),
                                          xdt.shape[1], _ptr(expert_off), R, N, K, _ptr(y), ldy,
                                          _ptr(S), _stream(stream))
@@ -425,16 +522,23 @@ def q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=None, y=None, want_y=True, 
     in the same kernel.  Returns (y or None, xw_next [M][N] uint8, xdt_next
     [N/32][ldxd] fp32)."""
     torch = _torch()
-    N, K = wp.shape
     if M is None:
         M = xw.shape[0]
+    N, K = _tc_operands(wp, wsc, xw, xdt, M, 1)
+    dev = wp.device
     if y is None and want_y:
-        y = torch.empty((M, N), dtype=torch.float32, device=wp.device)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    if y is not None:
+        _need(y, "y", (torch.float32,), (_ge(M), _ge(N)), pitched=True)
     ldy = _rows(y, "y") if y is not None else N
     if xw_next is None:
-        xw_next = torch.empty((M, N), dtype=torch.uint8, device=wp.device)
+        xw_next = torch.empty((M, N), dtype=torch.uint8, device=dev)
+    _need(xw_next, "xw_next", (torch.uint8,), (_ge(M), N))
     if xdt_next is None:
-        xdt_next = torch.zeros((N // 32, _round4(M)), dtype=torch.float32, device=wp.device)
+        xdt_next = torch.zeros((N // 32, _round4(M)), dtype=torch.float32, device=dev)
+    _need(xdt_next, "xdt_next", (torch.float32,), (_ge(N // 32), _ge(M)))
+    _same_gpu(("wp", wp), ("wsc", wsc), ("xw", xw), ("xdt", xdt),
+              ("y", y), ("xw_next", xw_next), ("xdt_next", xdt_next))
     st = lib().q4_0_x_q4_gemm_tc_quant_next(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt),
                                             xdt.shape[1], M, N, K, _ptr(y), ldy, _ptr(xw_next),
                                             _ptr(xdt_next), xdt_next.shape[1],
@@ -450,22 +554,28 @@ def h32_moe_route(logits, k, topk_id=None, topk_w=None, expert_off=None, row_idx
     largest logits (ties: lower id), softmax weights over them, rows grouped by
     expert then token."""
     torch = _torch()
-    _cuda(logits, "logits")
-    if logits.dtype != torch.float32:
-        raise ValueError("logits must be fp32")
+    _need(logits, "logits", (torch.float32,), (_ge(0), _ge(0)), pitched=True)
     T, E = logits.shape
     ldl = _rows(logits, "logits") if T > 0 else E
     dev = logits.device
+    i32 = (torch.int32,)
     if topk_id is None:
         topk_id = torch.empty((T, k), dtype=torch.int32, device=dev)
+    _need(topk_id, "topk_id", i32, (_ge(T), k))
     if topk_w is None:
         topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    _need(topk_w, "topk_w", (torch.float32,), (_ge(T), k))
     if expert_off is None:
         expert_off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    _need(expert_off, "expert_off", i32, (_ge(E + 1),))
     if row_idx is None:
         row_idx = torch.empty(T * k, dtype=torch.int32, device=dev)
+    _need(row_idx, "row_idx", i32, (_ge(T * k),))
     if row_of is None:
         row_of = torch.empty((T, k), dtype=torch.int32, device=dev)
+    _need(row_of, "row_of", i32, (_ge(T), k))
+    _same_gpu(("logits", logits), ("topk_id", topk_id), ("topk_w", topk_w), ("expert_off", expert_off),
+              ("row_idx", row_idx), ("row_of", row_of))
     st = lib().h32_moe_route(_ptr(logits), T, E, ldl, k, _ptr(topk_id), _ptr(topk_w),
                              _ptr(expert_off), _ptr(row_idx), _ptr(row_of), _stream(stream))
     _check("h32_moe_route", st)
@@ -476,17 +586,20 @@ def h32_moe_combine(y, row_of, topk_w, out=None, stream=None):
     """Weighted combine: y [R][H] fp32 (grouped rows), row_of [T][k], topk_w [T][k]
     -> out [T][H] fp32, the token's k rows added in choice order (fp32 fma from 0)."""
     torch = _torch()
-    _cuda(y, "y")
+    _need(y, "y", (torch.float32,), (_ge(0), _ge(0)), pitched=True)
     R, H = y.shape
+    dev = y.device
+    if row_of.dim() != 2:
+        raise ValueError("row_of must be 2-D [T][k]")
     T, k = row_of.shape
-    if row_of.dtype != torch.int32 or topk_w.dtype != torch.float32:
-        raise ValueError("row_of must be int32 and topk_w fp32")
-    if not (row_of.is_contiguous() and topk_w.is_contiguous()):
-        raise ValueError("row_of and topk_w must be contiguous")
+    _need(row_of, "row_of", (torch.int32,), (T, k))
+    _need(topk_w, "topk_w", (torch.float32,), (T, k))
     if out is None:
-        out = torch.empty((T, H), dtype=torch.float32, device=y.device)
+        out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _need(out, "out", (torch.float32,), (_ge(T), _ge(H)), pitched=True)
     ldy = _rows(y, "y") if R > 0 else H
     ldo = _rows(out, "out") if T > 0 else H
+    _same_gpu(("y", y), ("row_of", row_of), ("topk_w", topk_w), ("out", out))
     st = lib().h32_moe_combine(_ptr(y), R, ldy, _ptr(row_of), _ptr(topk_w), T, k, H, _ptr(out),
                                ldo, _stream(stream))
     _check("h32_moe_combine", st)

@@ -1,0 +1,60 @@
+"""A plain C program calls the library through include/h32.h alone (no Python,
+no torch: its own cudaMalloc'd buffers and stream) and its result equals the
+oracle's same-order fp32 value bit for bit.  The build check runs on the CPU;
+the run needs a GPU."""
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from hadamard_rotated_bit_gb300 import _build
+from hadamard_rotated_bit_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "tests", "c", "h32_c_caller.c")
+CUDA = "/usr/local/cuda"
+
+
+def _compile(tmp_path):
+    if shutil.which("gcc") is None or not os.path.exists(os.path.join(CUDA, "include", "cuda_runtime.h")):
+        pytest.skip("gcc or the CUDA toolkit headers are missing")
+    lib = _build.build()
+    libdir = os.path.dirname(lib)
+    cudalib = os.path.join(CUDA, "lib64")
+    exe = str(tmp_path / "h32_c_caller")
+    cmd = ["gcc", "-std=c11", "-O2", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+           "-I", os.path.join(CUDA, "include"), SRC, "-o", exe, "-L", libdir, "-lh32",
+           "-L", cudalib, "-lcudart", f"-Wl,-rpath,{libdir}:{cudalib}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    return exe
+
+
+def test_c_caller_builds(tmp_path):
+    assert os.access(_compile(tmp_path), os.X_OK)
+
+
+@pytest.mark.gpu
+def test_c_caller_matches_the_oracle(tmp_path):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    exe = _compile(tmp_path)
+    M, N, K = 70, 144, 384
+    x = wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, 290)
+    w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, 291)
+    inp, out = tmp_path / "in.bin", tmp_path / "out.bin"
+    with open(inp, "wb") as f:
+        f.write(np.array([M, N, K], np.int64).tobytes())
+        f.write(np.ascontiguousarray(x, np.float32).tobytes())
+        f.write(np.ascontiguousarray(w, np.float32).tobytes())
+    r = subprocess.run([exe, str(inp), str(out)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    y = np.fromfile(out, np.float32).reshape(M, N)
+    wq, wd = oracle.quantize_weights_q4_0(w)
+    xq, xd = oracle.quantize_act_q4(x)
+    r32, _, _ = oracle.gemm(wq, wd, xq, xd, K)
+    assert np.array_equal(y.view(np.uint32), r32.view(np.uint32))

@@ -29,7 +29,10 @@
  *     rounded to fp32, then one fp32 multiply by that constant.
  *   - Activation scale d = amax / 7 (or / 127) in fp32; codes are the
  *     nearest-even integers of y * (1/d), clamped to [-8, 7] (or [-127, 127]).
- *     An all-zero block has d = 0 and all codes 0.
+ *     An all-zero block has d = 0 and all codes 0.  Where 1/d is not finite
+ *     (a block of subnormal size) or the rotation overflowed, the code is
+ *     y / d by an IEEE divide instead (zeros stay 0), inf / inf read as its
+ *     limit +-qmax; weights likewise.
  *   - 4-bit codes are packed in the Q4_0 nibble order: byte j of a block holds
  *     element j in its low nibble and element j + 16 in its high nibble.
  *   - Weight codes follow the ordinary Q4_0 rule without an importance matrix:
@@ -234,8 +237,20 @@ static void quantize_block_sym(const float y[32], int qmin, int qmax, int q[32],
     }
     float d = amax / (float)qmax;
     float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+    /* A degenerate block: 1/d overflows (d below 2^-128, a block of subnormal
+     * size) or the rotation itself overflowed (amax, and so d, infinite).
+     * There the code is y / d by an IEEE divide, so exact zeros stay 0 and
+     * the element of largest magnitude gets +-qmax; an infinite element of an
+     * overflowed block (inf / inf) takes the limit of y / d, +-qmax. */
+    int degenerate = isinf(id) || isinf(amax);
     for (int i = 0; i < 32; ++i) {
-        float t = y[i] * id;
+        float t;
+        if (!degenerate) {
+            t = y[i] * id;
+        } else {
+            t = y[i] / d;
+            if (isnan(t)) t = copysignf((float)qmax, y[i]);
+        }
         /* clamp first (max then min), then round to nearest even */
         t = fmaxf(t, (float)qmin);
         t = fminf(t, (float)qmax);
@@ -304,11 +319,23 @@ static void q4_0_block(const float y[32], uint8_t qs[16], uint16_t *d16)
     }
     float d = mx / -8.0f;
     float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+    /* degenerate blocks as for the activations: where 1/d overflows or the
+     * rotation overflowed, y / d by an IEEE divide (a zero stays at code 8,
+     * the signed maximum gets code 0); inf / inf takes its limit, -8 when y
+     * has the sign of the signed maximum, else +8 */
+    int degenerate = isinf(id) || isinf(amax);
     int c[32];
     for (int i = 0; i < 32; ++i) {
         /* two roundings, the product then the sum: -ffp-contract=off keeps
          * the compiler from fusing them */
-        float u = y[i] * id + 8.5f;
+        float u;
+        if (!degenerate) {
+            u = y[i] * id + 8.5f;
+        } else {
+            float t = y[i] / d;
+            if (isnan(t)) t = ((signbit(y[i]) != 0) == (signbit(mx) != 0)) ? -8.0f : 8.0f;
+            u = t + 8.5f;
+        }
         u = fmaxf(u, 0.0f);
         u = fminf(u, 15.0f);
         c[i] = (int)u; /* truncation; u >= 0 here */
@@ -487,6 +514,31 @@ void o_gemm_experts_sampled(const uint8_t *wq, const uint16_t *wd, int64_t E,
  *   - the combine adds the k expert rows of a token in choice order,
  *     acc = fma(w_j, y_j, acc) from +0. */
 
+/* Logits that are not finite (masked experts, a broken router) follow the
+ * limits of the same rule: a NaN ranks below every number, -inf included
+ * (NaNs among themselves by id); the unnormalised weight e_j of a choice is
+ * exp(l_j - l_max) when the largest chosen logit l_max is finite (0 for a
+ * chosen -inf or NaN), 1 for the choices equal to +inf (0 for the others)
+ * when l_max = +inf, and 1 for every choice when l_max is -inf or NaN (all
+ * logits masked: equal weights). */
+
+/* does logit a (expert ia) rank before logit b (expert ib)? */
+static int ranks_before(float a, int64_t ia, float b, int64_t ib)
+{
+    if (isnan(a) || isnan(b)) {
+        if (isnan(a) && isnan(b)) return ia < ib;
+        return isnan(b);
+    }
+    return a > b || (a == b && ia < ib);
+}
+
+static float unnormalised_weight(float l, float lmax)
+{
+    if (isfinite(lmax)) return isnan(l) ? 0.0f : expf(l - lmax);
+    if (lmax > 0.0f) return (l == lmax) ? 1.0f : 0.0f; /* lmax = +inf */
+    return 1.0f;                                         /* -inf or NaN */
+}
+
 /* logits [T][E] -> topk_id [T][k], topk_w [T][k], expert_off [E+1],
  * row_idx [T*k] (the token of grouped row r), row_of [T][k] (the grouped row
  * of choice j of token t). */
@@ -503,14 +555,15 @@ void o_moe_route(const float *logits, int64_t T, int64_t E, int64_t k, int32_t *
                 for (int64_t i = 0; i < j; ++i)
                     if (id[i] == e) taken = 1;
                 if (taken) continue;
-                if (best < 0 || l[e] > l[best]) best = e; /* strict: a tie keeps the lower id */
+                if (best < 0 || ranks_before(l[e], e, l[best], best)) best = e;
             }
             id[j] = (int32_t)best;
         }
         const float lmax = l[id[0]];
         float s = 0.0f;
-        for (int64_t j = 0; j < k; ++j) s = s + expf(l[id[j]] - lmax);
-        for (int64_t j = 0; j < k; ++j) topk_w[t * k + j] = expf(l[id[j]] - lmax) / s;
+        for (int64_t j = 0; j < k; ++j) s = s + unnormalised_weight(l[id[j]], lmax);
+        for (int64_t j = 0; j < k; ++j)
+            topk_w[t * k + j] = unnormalised_weight(l[id[j]], lmax) / s;
     }
     int64_t r = 0;
     for (int64_t e = 0; e < E; ++e) {

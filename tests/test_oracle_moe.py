@@ -119,3 +119,33 @@ def test_combine_within_the_fp32_bound():
     ref = terms.sum(axis=1)
     bound = (k + 1) * 2.0 ** -24 * np.abs(terms).sum(axis=1)
     assert np.all(np.abs(out - ref) <= bound)
+
+
+def test_non_finite_logits_closed_forms():
+    """Masked (-inf), infinite and NaN logits follow the limits of the rule: a
+    NaN ranks below every number (-inf included); weights are the softmax over
+    the finite chosen logits (0 for a chosen -inf or NaN), shared equally by
+    the +inf choices when the largest is +inf, and equal when every chosen
+    logit is -inf or NaN."""
+    ninf, nan, inf = -np.inf, np.nan, np.inf
+    l = np.array([[1.0, ninf, 2.0, ninf, nan, 0.5]], np.float32)
+    ids, w, _, _, _ = oracle.moe_route(l, 4)
+    assert ids.tolist() == [[2, 0, 5, 1]]
+    e = np.exp(np.array([0.0, -1.0, -1.5], np.float64))
+    assert np.allclose(w[0, :3], e / e.sum(), rtol=1e-6, atol=0)
+    assert w[0, 3] == 0.0
+    ids, w, _, _, _ = oracle.moe_route(l, 6)
+    assert ids.tolist() == [[2, 0, 5, 1, 3, 4]] and w[0, 3:].tolist() == [0.0, 0.0, 0.0]
+    third = np.float32(1) / np.float32(3)
+    for row in ([ninf] * 5, [nan] * 5, [nan, ninf, ninf, nan, nan]):
+        ids, w, _, _, _ = oracle.moe_route(np.array([row], np.float32), 3)
+        assert np.array_equal(w, np.full((1, 3), third))
+    ids, _, _, _, _ = oracle.moe_route(np.array([[nan, ninf, ninf, nan, nan]], np.float32), 3)
+    assert ids.tolist() == [[1, 2, 0]]
+    ids, w, _, _, _ = oracle.moe_route(np.array([[0.0, inf, 3.0, inf]], np.float32), 3)
+    assert ids.tolist() == [[1, 3, 2]] and w.tolist() == [[0.5, 0.5, 0.0]]
+    # masked experts are never grouped ahead of a finite choice of the same token
+    l = np.array([[ninf, 0.0, ninf, 1.0], [2.0, ninf, ninf, ninf]], np.float32)
+    ids, w, off, ridx, row_of = oracle.moe_route(l, 2)
+    assert ids.tolist() == [[3, 1], [0, 1]]
+    assert w[1].tolist() == [1.0, 0.0]

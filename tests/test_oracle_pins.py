@@ -188,12 +188,77 @@ def test_tie_block_golden(golden):
 
 
 def test_tiny_block_edge_golden(golden):
+    """Blocks whose 1/d overflows: zeros stay 0, the largest element gets +-qmax."""
     g = golden("tiny_block.txt")
+    u = np.float32(2.0 ** -149)
     x = np.zeros((1, 32), np.float32)
     x[0, 0] = np.float32(2.0 ** -130)
     xq, xd = oracle.quantize_act_q4(x, rotate=False)
-    assert xd[0, 0] == np.float32(np.float32(2.0 ** -130) / np.float32(7))
-    assert np.array_equal(oracle.decode_act4(xq, 32)[0].astype(np.int64), _ints(g["q4_codes"]))
+    assert xd[0, 0] == np.float32(int(g["case_a_d_units"]) * u)
+    assert np.array_equal(oracle.decode_act4(xq, 32)[0].astype(np.int64), _ints(g["case_a_q4_codes"]))
+    xq, xd = oracle.quantize_act_q8(x, rotate=False)
+    assert xd[0, 0] == np.float32(int(g["case_b_d_units"]) * u)
+    assert np.array_equal(xq[0].astype(np.int64), _ints(g["case_b_q8_codes"]))
+    xq, xd = oracle.quantize_act_q4(x, rotate=True)
+    assert xd[0, 0] == np.float32(int(g["case_c_d_units"]) * u)
+    assert np.array_equal(oracle.decode_act4(xq, 32)[0].astype(np.int64), _ints(g["case_c_q4_codes"]))
+    w = np.zeros((1, 32), np.float32)
+    w[0, 0] = np.float32(2.0 ** -140)
+    wq, wd = oracle.quantize_weights_q4_0(w, rotate=False)
+    assert np.array_equal(oracle.decode_w4(wq, 32)[0].astype(np.int64) + 8, _ints(g["case_d_codes"]))
+    assert int(wd[0, 0]) == int(g["case_d_d16"], 16)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("rotate", [True, False])
+def test_degenerate_blocks_reconstruction_bound(bits, rotate):
+    """Blocks of subnormal size (1/d overflows) keep the half-step bound of the
+    ordinary blocks, |y - q d| <= d/2 up to the rounding of y / d, wherever
+    y / d is inside the code range (a subnormal d can be far from amax/qmax,
+    and then the clamp decides); an exact zero keeps code 0."""
+    r = np.random.default_rng(11)
+    x = (r.standard_normal((64, 64)) * 2.0 ** -131).astype(np.float32)
+    x[:, 5] = 0.0                      # exact zeros (unrotated: they stay zero)
+    x[0] = 0.0
+    x[0, 7] = np.float32(2.0 ** -140)  # one nonzero element: the rest of the block is zero
+    if bits == 4:
+        xq, xd = oracle.quantize_act_q4(x, rotate)
+        q = oracle.decode_act4(xq, 64).astype(np.float64)
+        qmax = 7
+    else:
+        xq, xd = oracle.quantize_act_q8(x, rotate)
+        q = xq.astype(np.float64)
+        qmax = 127
+    y = (oracle.fwht32(x.reshape(-1)).reshape(x.shape) if rotate else x).astype(np.float64)
+    d = np.repeat(xd.astype(np.float64), 32, axis=1)
+    assert np.all(np.isinf(np.float32(1.0) / xd[xd > 0].astype(np.float32)))   # degenerate indeed
+    assert np.abs(q).max() <= qmax
+    ratio = np.divide(y, d, out=np.zeros_like(y), where=d > 0)
+    inside = np.abs(ratio) <= qmax + 0.5
+    assert np.all((np.abs(y - q * d) <= 0.5 * d + 2.0 ** -23 * np.abs(y))[inside])
+    assert np.all((q == np.sign(y) * qmax)[~inside])
+    assert np.all(q[y == 0] == 0)
+    # the element of largest magnitude gets the largest code magnitude
+    yb, qb = y.reshape(64, 2, 32), q.reshape(64, 2, 32)
+    pos = np.abs(yb).argmax(axis=2)
+    top = np.take_along_axis(qb, pos[..., None], axis=2)[..., 0]
+    assert np.array_equal(np.abs(top), np.abs(qb).max(axis=2))
+    assert (np.abs(top) == qmax).mean() > 0.9
+
+
+def test_overflowed_rotation_block():
+    """A block whose rotation overflows to +-inf: finite elements get 0, the
+    infinite ones +-qmax (the limit of y / d), d = inf."""
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0], x[0, 1] = np.float32(3e38), np.float32(-3e38)
+    y = oracle.fwht32(x.reshape(-1))
+    assert np.isinf(y).any() and np.isfinite(y).any()
+    xq, xd = oracle.quantize_act_q4(x, rotate=True)
+    q = oracle.decode_act4(xq, 32)[0]
+    assert np.isinf(xd[0, 0])
+    assert np.array_equal(q, np.where(np.isinf(y), np.sign(y) * 7, 0).astype(q.dtype))
+    xq, xd = oracle.quantize_act_q8(x, rotate=True)
+    assert np.array_equal(xq[0], np.where(np.isinf(y), np.sign(y) * 127, 0).astype(xq.dtype))
 
 
 @pytest.mark.parametrize("bits", [4, 8])

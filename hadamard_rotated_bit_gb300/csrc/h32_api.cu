@@ -69,6 +69,9 @@ extern "C" h32_status h32_device_status(void *stream) {
     H32_TRY(h32::check_device(nullptr));
     const cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return h32::launch_status(e);
+    // one caller at a time: each status word is taken through one device word
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
     const h32_status st[4] = {h32::quant_read_and_clear_status(s),
                               h32::gemm_read_and_clear_status(s),
                               h32::tc_read_and_clear_status(s),

@@ -58,6 +58,25 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 #endif
 
+#if defined(__CUDACC__)
+// Read and clear a kernel status word in one atomic step: `take` is a
+// one-thread kernel that swaps the word with 0 and leaves the old value in the
+// device word `taken`, which is then copied out.  A bit that a kernel on
+// another stream sets meanwhile is reported by this call or by the next one,
+// never lost.  `*ok` is false when a launch, copy or synchronization failed.
+// Not reentrant (one `taken` word per status word): h32_device_status
+// serializes its callers.
+template <typename T>
+uint32_t take_status(void (*take)(), const T &taken, cudaStream_t s, bool *ok) {
+    uint32_t v = 0;
+    take<<<1, 1, 0, s>>>();
+    *ok = cudaGetLastError() == cudaSuccess &&
+          cudaMemcpyFromSymbolAsync(&v, taken, 4, 0, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
+          cudaStreamSynchronize(s) == cudaSuccess;
+    return v;
+}
+#endif
+
 #define H32_TRY(expr)                  \
     do {                               \
         h32_status _st = (expr);       \
@@ -225,6 +244,28 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// two 16-lane halves of the warp's lane quarter: threads 0..15 read lanes
+// base + t, columns [c, c + 8); threads 16..31 read lanes base + t - 16,
+// columns [c + 8, c + 16)
+__device__ __forceinline__ void tmem_ld_16x32bx2_x8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], 8;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr));
+}
+
+// 16 lanes x 256 bit, twice along the columns: thread t holds lanes base + t/4
+// (r[0], r[1]) and base + t/4 + 8 (r[2], r[3]) at columns c + 2 (t%4) and + 1,
+// then the same 8 columns further (r[4..7])
+__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
         : "r"(taddr));
 }
 

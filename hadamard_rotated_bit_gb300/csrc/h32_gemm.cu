@@ -917,14 +917,13 @@ h32_status gemm_dense(const uint8_t *wq, const uint16_t *wd, const void *xq, con
 
 }  // namespace
 
+__device__ uint32_t g_gemm_status_taken;
+__global__ void take_g_gemm_status() { g_gemm_status_taken = atomicExch(&g_gemm_status, 0u); }
+
 h32_status gemm_read_and_clear_status(cudaStream_t s) {
-    uint32_t v = 0;
-    const uint32_t z = 0;
-    if (cudaMemcpyFromSymbolAsync(&v, g_gemm_status, 4, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return H32_ERR_CUDA;
-    if (cudaMemcpyToSymbolAsync(g_gemm_status, &z, 4, 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return H32_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return H32_ERR_CUDA;
+    bool ok = false;
+    const uint32_t v = take_status(take_g_gemm_status, g_gemm_status_taken, s, &ok);
+    if (!ok) return H32_ERR_CUDA;
     if (v & kStatusTimeout) return H32_ERR_TIMEOUT;
     if (v & kStatusGuard) return H32_ERR_DEVICE_GUARD;
     return H32_OK;
@@ -989,6 +988,9 @@ extern "C" h32_status q4_0_x_q4_gemm_experts(const uint8_t *wq, const uint16_t *
     // SM, each walks the tile list it computes from expert_off
     const int64_t nt = (N + kBM - 1) / kBM;
     const int64_t bound = nt * (E + (R + kBNMax - 1) / kBNMax);
+    // the kernel counts tiles in int (at most R / 128 + 2 E chunks per weight tile)
+    if (nt * (R / kBNMax + 2 * static_cast<int64_t>(E) + 1) > 0x7FFFFFFFll)
+        return H32_ERR_INVALID_ARG;
     const int grid = static_cast<int>(bound < sms ? bound : sms);
     return launch<4>(map, a, grid, reinterpret_cast<cudaStream_t>(stream));
 }

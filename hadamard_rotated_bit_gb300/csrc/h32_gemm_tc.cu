@@ -36,6 +36,11 @@
 // programmatic dependent launch: nothing touches global memory before the
 // previous kernel of the stream has completed.
 
+// how the epilogue's TMEM fragment maps to threads (rows a thread holds: 0 -> 1,
+// 1 -> 2, 2 -> 4); see epilogue_tiles
+#ifndef H32_TC_LAYOUT
+#define H32_TC_LAYOUT 0
+#endif
 // epilogue warps per TMEM lane quarter
 #ifndef H32_TC_EPI_PER_QUAD
 #define H32_TC_EPI_PER_QUAD 4
@@ -150,8 +155,8 @@ __device__ __forceinline__ uint32_t quant_lane_block(float v, int lane, bool rot
     for (int h = 1; h < 32; h <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, h));
     const float dd = __fdiv_rn(amax, 7.0f);
     const float id = (dd != 0.0f) ? __frcp_rn(dd) : 0.0f;
-    float t = __fmul_rn(v, id);
-    if (!(amax < INFINITY) || isinf(id)) t = fminf(fmaxf(t, -8.0f), 7.0f);
+    const float t = (!(amax < INFINITY) || isinf(id)) ? degenerate_code(v, dd, -8.0f, 7.0f)
+                                                       : __fmul_rn(v, id);
     *d = dd;
     return tc_bytes(__float_as_uint(__fadd_rn(t, kRoundMagic)) & 0xFFu) & 0xFFu;
 }
@@ -260,16 +265,31 @@ __device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a, const int *s_o
 // positions of the shared-memory stages and TMEM buffers are carried as
 // counters and phase bits, arrivals come from one elected lane.  Returns false
 // when a wait gave up.
-template <int EPQ, int XB, bool kQN, bool kTail>
+//
+// LAY picks how a warp's TMEM fragment maps to its threads (the warp always
+// covers its lane quarter's 32 weight rows x its share of the columns):
+//   0  32x32b: a thread holds one row; every token scale of a chunk is a
+//      broadcast shared-memory load (4 per 16 columns and block)
+//   1  16x32bx2: a thread holds two rows (t % 16 and t % 16 + 16) and 8 of a
+//      chunk's 16 columns: 2 token-scale loads per 16 columns and block
+//   2  16x256b: a thread holds four rows (t / 4 + 8 k) and 4 of a chunk's
+//      columns, two column pairs: 2 narrow token-scale loads per 16 columns
+// The fused producer (kQN) needs 0: its warp's 32 lanes are one 32-block of
+// the next projection's input.
+template <int EPQ, int XB, bool kQN, bool kTail, int LAY = 0>
 __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const int *s_off,
                                                const int *s_tpre, uint64_t *bars, const float *s_sa,
                                                const float *s_sb, uint32_t tmem, int warp, int lane,
                                                volatile int *abort_flag) {
     using C = TcCfg<EPQ, XB>;
+    static_assert(!kQN || LAY == 0, "the fused producer takes one row a thread");
     const int ew = warp - C::kProdWarps;
     const int quad = warp & 3;                 // TMEM lanes 32 quad .. 32 quad + 31
     const int part = ew >> 2;                  // share of the columns
-    const int row = quad * 32 + lane;
+    // the rows this thread holds (quarter-relative), by layout
+    const int row = quad * 32 + lane;                                    // LAY 0
+    const int row2 = quad * 32 + (lane & 15), half = lane >> 4;          // LAY 1: row2, row2 + 16
+    const int row4 = quad * 32 + (lane >> 2), g4 = lane & 3;             // LAY 2: row4 + 8 k
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const int nst = a.nb / 4;
     const uint64_t lim = a.wait_limit;
@@ -287,9 +307,26 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
         for (int i = 0; i < 8 * C::kMaxChunks; ++i) acc[i] = 0ull;
         for (int st = 0; st < nst; ++st) {
             if (!warp_wait(&bars[kBarFull + s], sph, lim, abort_flag)) return false;
-            const float4 dw4 = *reinterpret_cast<const float4 *>(s_sa + s * (kScaleBytes / 4) + 4 * row);
-            const float dws[4] = {dw4.x, dw4.y, dw4.z, dw4.w};
+            const float *sa = s_sa + s * (kScaleBytes / 4);        // [128 rows][4 blocks]
             const float *sb = s_sb + s * (kScaleBytes / 4) + c0;   // [4 blocks][bn tokens]
+            // the weight scales of the thread's rows for the stage's 4 blocks
+            float dws[4][4];
+            if constexpr (LAY == 0) {
+                const float4 v = *reinterpret_cast<const float4 *>(sa + 4 * row);
+                dws[0][0] = v.x, dws[0][1] = v.y, dws[0][2] = v.z, dws[0][3] = v.w;
+            } else if constexpr (LAY == 1) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float4 v = *reinterpret_cast<const float4 *>(sa + 4 * (row2 + 16 * k));
+                    dws[k][0] = v.x, dws[k][1] = v.y, dws[k][2] = v.z, dws[k][3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float4 v = *reinterpret_cast<const float4 *>(sa + 4 * (row4 + 8 * k));
+                    dws[k][0] = v.x, dws[k][1] = v.y, dws[k][2] = v.z, dws[k][3] = v.w;
+                }
+            }
 #pragma unroll
             for (int j0 = 0; j0 < 4; j0 += kGroup) {
                 if (!warp_wait(&bars[kBarSFull + gb], gph, lim, abort_flag)) return false;
@@ -303,10 +340,35 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
                     if (c < nch) {
 #pragma unroll
                         for (int i = 0; i < kGroup; ++i) {
-                            uint32_t v[16];
-                            tmem_ld_x16(tcol0 + i * 128 + c * 16, v);
-                            tmem_ld_wait();
-                            fold16(acc + 8 * c, dws[j0 + i], sb + (j0 + i) * a.bn + 16 * c, v);
+                            const int j = j0 + i;
+                            const uint32_t tc = tcol0 + i * 128 + c * 16;
+                            const float *dx = sb + j * a.bn + 16 * c;
+                            if constexpr (LAY == 0) {
+                                uint32_t v[16];
+                                tmem_ld_x16(tc, v);
+                                tmem_ld_wait();
+                                fold16(acc + 8 * c, dws[0][j], dx, v);
+                            } else if constexpr (LAY == 1) {
+                                uint32_t va[8], vb[8];
+                                tmem_ld_16x32bx2_x8(tc, va);
+                                tmem_ld_16x32bx2_x8(tc + (16u << 16), vb);
+                                tmem_ld_wait();
+                                fold8x2(acc + 8 * c, dws[0][j], dws[1][j], dx + 8 * half, va, vb);
+                            } else {
+                                uint32_t va[8], vb[8];
+                                tmem_ld_16x256b_x2(tc, va);
+                                tmem_ld_16x256b_x2(tc + (16u << 16), vb);
+                                tmem_ld_wait();
+                                uint64_t dw2[4];
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    dw2[k] = pair_of(__float_as_uint(dws[k][j]),
+                                                     __float_as_uint(dws[k][j]));
+                                const uint64_t p0 = *reinterpret_cast<const uint64_t *>(dx + 2 * g4);
+                                const uint64_t p1 =
+                                    *reinterpret_cast<const uint64_t *>(dx + 8 + 2 * g4);
+                                fold4x4(acc + 8 * c, dw2, p0, p1, va, vb);
+                            }
                         }
                     }
                 }
@@ -325,20 +387,35 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
                 sph ^= 1;
             }
         }
-        const int64_t n = ti.n0 + row;
-        if (n < a.N && (!kQN || a.y)) {
+        if (!kQN || a.y) {
+            // acc[8 c + q] holds two adjacent columns of one row: (row, first column)
+            // by layout
 #pragma unroll
             for (int c = 0; c < C::kMaxChunks; ++c) {
                 if (c < nch) {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        const int col = c0 + c * 16 + 2 * q;
-                        const uint64_t pr = acc[8 * c + q];
-                        if (col >= ti.clo && col < ti.chi)
-                            a.y[(ti.g0 + col) * a.ldy + n] = __uint_as_float(static_cast<uint32_t>(pr));
-                        if (col + 1 >= ti.clo && col + 1 < ti.chi)
-                            a.y[(ti.g0 + col + 1) * a.ldy + n] =
-                                __uint_as_float(static_cast<uint32_t>(pr >> 32));
+                        int r, col;
+                        if constexpr (LAY == 0) {
+                            r = row;
+                            col = c0 + c * 16 + 2 * q;
+                        } else if constexpr (LAY == 1) {
+                            r = row2 + 16 * (q >> 2);
+                            col = c0 + c * 16 + 8 * half + 2 * (q & 3);
+                        } else {
+                            r = row4 + 8 * (q >> 1);
+                            col = c0 + c * 16 + 8 * (q & 1) + 2 * g4;
+                        }
+                        const int64_t n = ti.n0 + r;
+                        if (n < a.N) {
+                            const uint64_t pr = acc[8 * c + q];
+                            if (col >= ti.clo && col < ti.chi)
+                                a.y[(ti.g0 + col) * a.ldy + n] =
+                                    __uint_as_float(static_cast<uint32_t>(pr));
+                            if (col + 1 >= ti.clo && col + 1 < ti.chi)
+                                a.y[(ti.g0 + col + 1) * a.ldy + n] =
+                                    __uint_as_float(static_cast<uint32_t>(pr >> 32));
+                        }
                     }
                 }
             }
@@ -346,22 +423,26 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
         // the output quantized for the next projection: this warp's 32 lanes are
         // one 32-block of it for every token column (N % 32 == 0, so a block is
         // all inside or all outside the N rows)
-        if (kQN && ti.n0 + quad * 32 < a.N) {
-            const int nb0 = (ti.n0 + quad * 32) >> 5;
+        if constexpr (kQN) {
+            if (ti.n0 + quad * 32 < a.N) {
+                const int64_t n = ti.n0 + row;
+                const int nb0 = (ti.n0 + quad * 32) >> 5;
 #pragma unroll
-            for (int c = 0; c < C::kMaxChunks; ++c) {
-                if (c < nch) {
+                for (int c = 0; c < C::kMaxChunks; ++c) {
+                    if (c < nch) {
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const int col = c0 + c * 16 + q;
-                        const uint64_t pr = acc[8 * c + (q >> 1)];
-                        const float v = __uint_as_float(static_cast<uint32_t>(pr >> (32 * (q & 1))));
-                        float d;
-                        const uint32_t byte = quant_lane_block(v, lane, a.qn_rot != 0, &d);
-                        if (col >= ti.clo && col < ti.chi) {
-                            const int64_t g = ti.g0 + col;
-                            a.qn[g * a.N + n] = static_cast<uint8_t>(byte);
-                            if (lane == 0) a.qnd[nb0 * a.ldqnd + g] = d;
+                        for (int q = 0; q < 16; ++q) {
+                            const int col = c0 + c * 16 + q;
+                            const uint64_t pr = acc[8 * c + (q >> 1)];
+                            const float v =
+                                __uint_as_float(static_cast<uint32_t>(pr >> (32 * (q & 1))));
+                            float d;
+                            const uint32_t byte = quant_lane_block(v, lane, a.qn_rot != 0, &d);
+                            if (col >= ti.clo && col < ti.chi) {
+                                const int64_t g = ti.g0 + col;
+                                a.qn[g * a.N + n] = static_cast<uint8_t>(byte);
+                                if (lane == 0) a.qnd[nb0 * a.ldqnd + g] = d;
+                            }
                         }
                     }
                 }
@@ -374,7 +455,7 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
 // kEpi: 0 = y only, 1 = y and the block sums, 2 = y (optional) and the output
 // quantized for the next projection.  kTail: the last partial wave's tiles are
 // cut into pieces (TcArgs::tail_first, tail_k).
-template <int EPQ, int XB, int kEpi, bool kTail = false>
+template <int EPQ, int XB, int kEpi, bool kTail = false, int LAY = 0>
 __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_sa,
@@ -580,9 +661,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
     } else if constexpr (!kSums) {
         // ------------------------------------------------------- epilogue
         if constexpr (C::kRegSplit) reg_alloc<C::kEpiRegs>();
-        if (!epilogue_tiles<EPQ, XB, kEpi == 2, kTail>(a, total, s_off, s_tpre, bars, s_sa, s_sb, tmem,
-                                                warp, lane,
-                                     abort_flag))
+        if (!epilogue_tiles<EPQ, XB, kEpi == 2, kTail, kEpi == 2 ? 0 : LAY>(
+                a, total, s_off, s_tpre, bars, s_sa, s_sb, tmem, warp, lane, abort_flag))
             set_abort(misc);
     } else {
         // ------------------------------------ epilogue with block sums
@@ -837,10 +917,10 @@ TcPlan plan_tc(int64_t M, int64_t N, int sms, bool allow_cut) {
     return plan;
 }
 
-template <int EPQ, int XB, int kEpi, bool kTail = false>
+template <int EPQ, int XB, int kEpi, bool kTail = false, int LAY = H32_TC_LAYOUT>
 h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStream_t s) {
     using C = TcCfg<EPQ, XB>;
-    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi, kTail>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi, kTail, LAY>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return launch_status(e);
     if constexpr (C::kRegSplit) {
@@ -849,7 +929,7 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
         // (read once per kernel; a failed read leaves -1 and refuses every launch)
         static const int regs = [] {
             cudaFuncAttributes fa{};
-            return cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi, kTail>) == cudaSuccess
+            return cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi, kTail, LAY>) == cudaSuccess
                        ? fa.numRegs
                        : -1;
         }();
@@ -858,21 +938,20 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
             return H32_ERR_UNSUPPORTED;
         }
     }
-    const cudaError_t el = launch_pdl(gemm_tc_kernel<EPQ, XB, kEpi, kTail>, dim3(grid), dim3(C::kThreads),
+    const cudaError_t el = launch_pdl(gemm_tc_kernel<EPQ, XB, kEpi, kTail, LAY>, dim3(grid), dim3(C::kThreads),
                                       C::kSmem, s, maps[0], maps[1], maps[2], maps[3], a);
     return launch_status(el != cudaSuccess ? el : cudaGetLastError());
 }
 
 }  // namespace
 
+__device__ uint32_t g_tc_status_taken;
+__global__ void take_g_tc_status() { g_tc_status_taken = atomicExch(&g_tc_status, 0u); }
+
 h32_status tc_read_and_clear_status(cudaStream_t s) {
-    uint32_t v = 0;
-    const uint32_t z = 0;
-    if (cudaMemcpyFromSymbolAsync(&v, g_tc_status, 4, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return H32_ERR_CUDA;
-    if (cudaMemcpyToSymbolAsync(g_tc_status, &z, 4, 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return H32_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return H32_ERR_CUDA;
+    bool ok = false;
+    const uint32_t v = take_status(take_g_tc_status, g_tc_status_taken, s, &ok);
+    if (!ok) return H32_ERR_CUDA;
     if (v & kStatusTimeout) return H32_ERR_TIMEOUT;
     if (v & kStatusGuard) return H32_ERR_DEVICE_GUARD;
     return H32_OK;
@@ -910,7 +989,12 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     // dense: the tile width and the cut of the last wave from the schedule
     // simulation; groups: full 128-row chunks, nothing cut
     TcPlan plan{kBNMax, 1, 0, 0, sms};
-    if (!expert_off) {
+    if (expert_off) {
+        // the kernel numbers tiles in int: group e has at most
+        // ceil((size_e + 3) / 128) chunks, so at most R / 128 + 2 E chunks in all
+        if (((N + kBM - 1) / kBM) * (M / kBNMax + 2 * E + 1) > 0x7FFFFFFFll)
+            return H32_ERR_INVALID_ARG;
+    } else {
         if (((N + kBM - 1) / kBM) * ((M + 15) / 16) * 8 > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
         plan = plan_tc(M, N, sms, !qn && !block_sums);
     }

@@ -33,11 +33,26 @@ constexpr int kTopkWarps = 8;       // tokens per block of route_topk_kernel
 constexpr int kGroupThreads = 1024;
 constexpr int kCombineThreads = 128;   // one float4 column each
 
-// (value, id) a beats b: larger value, or equal value and lower id; id < 0 = none
+// (value, id) a beats b: larger value, or equal value and lower id; a NaN
+// ranks below every number (-inf included), NaNs among themselves by id;
+// id < 0 = none
 __device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
     if (ia < 0) return false;
     if (ib < 0) return true;
+    const bool na = isnan(va), nb = isnan(vb);
+    if (na || nb) return (na && nb) ? ia < ib : nb;
     return va > vb || (va == vb && ia < ib);
+}
+
+// Unnormalised weight of a chosen logit l given the largest chosen logit
+// lmax: exp(l - lmax) when lmax is finite (0 for a chosen -inf or NaN); when
+// lmax = +inf, 1 for the +inf choices and 0 for the others; when lmax is -inf
+// or NaN (every logit masked), 1: equal weights.  These are the limits of the
+// softmax over the chosen logits.
+__device__ __forceinline__ float unnormalised_weight(float l, float lmax) {
+    if (isfinite(lmax)) return isnan(l) ? 0.0f : expf(__fsub_rn(l, lmax));
+    if (lmax > 0.0f) return l == lmax ? 1.0f : 0.0f;
+    return 1.0f;
 }
 
 // NPER: logits per lane (expert lane + 32 i, i < NPER), a power of two >= E / 32
@@ -89,7 +104,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
     // weights: exp of each chosen logit minus the largest, their sum in choice
     // order from +0, one IEEE divide each
     const float lmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
-    const float ex = (lane < k) ? expf(__fsub_rn(my_v, lmax)) : 0.0f;
+    const float ex = (lane < k) ? unnormalised_weight(my_v, lmax) : 0.0f;
     float s = 0.0f;
     for (int j = 0; j < k; ++j) s = __fadd_rn(s, __shfl_sync(0xFFFFFFFFu, ex, j));
     if (lane < k) {
@@ -223,14 +238,13 @@ __global__ void __launch_bounds__(kCombineThreads)
 
 }  // namespace
 
+__device__ uint32_t g_moe_status_taken;
+__global__ void take_g_moe_status() { g_moe_status_taken = atomicExch(&g_moe_status, 0u); }
+
 h32_status moe_read_and_clear_status(cudaStream_t s) {
-    uint32_t v = 0;
-    const uint32_t z = 0;
-    if (cudaMemcpyFromSymbolAsync(&v, g_moe_status, 4, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return H32_ERR_CUDA;
-    if (cudaMemcpyToSymbolAsync(g_moe_status, &z, 4, 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return H32_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return H32_ERR_CUDA;
+    bool ok = false;
+    const uint32_t v = take_status(take_g_moe_status, g_moe_status_taken, s, &ok);
+    if (!ok) return H32_ERR_CUDA;
     return (v & kStatusGuard) ? H32_ERR_DEVICE_GUARD : H32_OK;
 }
 

@@ -162,18 +162,16 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const void *__restrict__
         const float d = __fdiv_rn(amax, kQmax);
         const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
 
-        // codes: round-half-even(clamp(y * id)).  With a finite amax and a
-        // finite id every product lies in [-qmax, qmax] up to rounding, so the
-        // clamp only matters when 1/d overflowed (a block of subnormal size) or
-        // the rotation itself overflowed to +-inf (products inf * 0 = NaN)
+        // codes: round-half-even(y * id).  With a finite amax and a finite id
+        // every product lies in [-qmax, qmax] up to rounding; when 1/d
+        // overflowed (a block of subnormal size) or the rotation itself
+        // overflowed to +-inf, the code is the clamped y / d instead
         uint32_t bits[32];
         if (!(amax < INFINITY) || isinf(id)) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float t = __fmul_rn(v[i], id);
-                t = fminf(fmaxf(t, kQmin), kQmax);
-                bits[i] = __float_as_uint(__fadd_rn(t, kRoundMagic));
-            }
+            for (int i = 0; i < 32; ++i)
+                bits[i] = __float_as_uint(__fadd_rn(degenerate_code(v[i], d, kQmin, kQmax),
+                                                    kRoundMagic));
         } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -236,10 +234,21 @@ __global__ void __launch_bounds__(256) quant_w_kernel(const float *__restrict__ 
         }
         const float d = __fdiv_rn(mx, -8.0f);
         const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+        // a degenerate block (1/d overflows, or the rotation overflowed): the
+        // code from y / d by an IEEE divide, inf / inf read as its limit
+        // (-8 where y has the sign of the signed maximum, else +8)
+        const bool degen = isinf(id) || !(amax < INFINITY);
         uint32_t c[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            float u = __fadd_rn(__fmul_rn(v[i], id), 8.5f);
+            float u;
+            if (!degen) {
+                u = __fadd_rn(__fmul_rn(v[i], id), 8.5f);
+            } else {
+                float t = __fdiv_rn(v[i], d);
+                if (isnan(t)) t = ((__float_as_uint(v[i]) ^ __float_as_uint(mx)) >> 31) ? 8.0f : -8.0f;
+                u = __fadd_rn(t, 8.5f);
+            }
             u = fminf(fmaxf(u, 0.0f), 15.0f);
             c[i] = static_cast<uint32_t>(__float2int_rz(u));
         }
@@ -317,13 +326,11 @@ __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restric
         const float d = __fdiv_rn(amax, kQmax);
         const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
         uint32_t bits[32];
-        if (!(amax < INFINITY) || isinf(id)) {
+        if (!(amax < INFINITY) || isinf(id)) {   // degenerate block: the clamped y / d
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float t = __fmul_rn(v[i], id);
-                t = fminf(fmaxf(t, kQmin), kQmax);
-                bits[i] = __float_as_uint(__fadd_rn(t, kRoundMagic));
-            }
+            for (int i = 0; i < 32; ++i)
+                bits[i] = __float_as_uint(__fadd_rn(degenerate_code(v[i], d, kQmin, kQmax),
+                                                    kRoundMagic));
         } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -439,14 +446,13 @@ h32_status quantize_act(const void *x, h32_in_dtype dt, int64_t M, int64_t K, in
 
 }  // namespace
 
+__device__ uint32_t g_quant_status_taken;
+__global__ void take_g_quant_status() { g_quant_status_taken = atomicExch(&g_quant_status, 0u); }
+
 h32_status quant_read_and_clear_status(cudaStream_t s) {
-    uint32_t v = 0;
-    const uint32_t z = 0;
-    if (cudaMemcpyFromSymbolAsync(&v, g_quant_status, 4, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return H32_ERR_CUDA;
-    if (cudaMemcpyToSymbolAsync(g_quant_status, &z, 4, 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return H32_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return H32_ERR_CUDA;
+    bool ok = false;
+    const uint32_t v = take_status(take_g_quant_status, g_quant_status_taken, s, &ok);
+    if (!ok) return H32_ERR_CUDA;
     if (v & kStatusGuard) return H32_ERR_DEVICE_GUARD;
     return H32_OK;
 }

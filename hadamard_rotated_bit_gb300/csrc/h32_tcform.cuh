@@ -14,6 +14,18 @@ constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;   // half of kInvSqrt32: the fp32 
 // mantissa bits as a two's-complement integer
 constexpr float kRoundMagic = 12582912.0f;
 
+// The code value of y in a degenerate block, where 1/d is not finite (d below
+// 2^-128: a block of subnormal size) or d is infinite (the rotation
+// overflowed): y / d by an IEEE divide, so an exact zero stays 0 and the
+// element of largest magnitude gets +-qmax; inf / inf (an infinite element of
+// an overflowed block) reads as its limit, +-qmax.  Clamped to [qmin, qmax],
+// not yet rounded.
+__device__ __forceinline__ float degenerate_code(float y, float d, float qmin, float qmax) {
+    float t = __fdiv_rn(y, d);
+    if (isnan(t)) t = copysignf(qmax, y);
+    return fminf(fmaxf(t, qmin), qmax);
+}
+
 // tensor-core form: one byte per code, the e4m3 encoding of the integer code
 __device__ __forceinline__ uint32_t byte_sign_mask(uint32_t x) {
     uint32_t r;

@@ -65,7 +65,10 @@ typedef enum h32_in_dtype {
  * For each row m and block b: y = H x_block / sqrt(32) (fp32 butterfly,
  * strides 1, 2, 4, 8, 16, then one multiply by the fp32 nearest 1/sqrt(32));
  * d = amax(|y|) / 7 in fp32; codes = round-half-even(clamp(y * (1/d), -8, 7)),
- * all codes 0 when d = 0.
+ * all codes 0 when d = 0.  In a degenerate block, where 1/d is not finite (a
+ * block of subnormal size, d below 2^-128) or the rotation overflowed to
+ * +-inf, the code is round-half-even(clamp(y / d)) by an IEEE divide instead:
+ * exact zeros stay 0 and an infinite element gets +-7 (the limit of y / d).
  *   x      [M][ldx] activations of type `dt`, ldx >= K
  *   xq     [M][K/2] out: two's-complement 4-bit codes, Q4_0 nibble order
  *   xd     [M][K/32] out: fp32 scales d
@@ -98,7 +101,10 @@ h32_status h32_quantize_act_q8(const void *x, h32_in_dtype dt, int64_t M, int64_
  * h32_quantize_act_q4: 0, 1/32, 64 or 128 points), then
  * rounded by the Q4_0 rule: the signed value of largest magnitude (first on
  * ties) maps to code 0, d = max / -8, code = min(15, trunc(y * (1/d) + 8.5)),
- * d stored as fp16 rounded to nearest even.
+ * d stored as fp16 rounded to nearest even.  Degenerate blocks as for the
+ * activations: where 1/d is not finite or the rotation overflowed, y / d by an
+ * IEEE divide replaces y * (1/d) (a zero gets code 8); inf / inf reads as -8
+ * where y has the sign of the signed maximum, else +8.
  *   w      [N][K] fp32 weights (rows are output features)
  *   wq     [N][K/2] out: codes 0..15 in Q4_0 nibble order
  *   wd     [N][K/32] out: fp16 scales (bit patterns)
@@ -302,8 +308,13 @@ h32_status q4_0_x_q4_gemm_tc_experts(const uint8_t *wp, const float *wsc, int64_
  *   expert_off [E+1] int32 out: group e holds grouped rows [off[e], off[e+1]); off[E] = T k
  *   row_idx    [T k] int32 out: the token of grouped row r
  *   row_of     [T][k] int32 out: the grouped row of choice j of token t
+ * Logits that are not finite (masked experts) follow the limits of the same
+ * rule: a NaN ranks below every number, -inf included (NaNs among themselves
+ * by id); a chosen -inf or NaN weighs 0 when the largest chosen logit l_0 is
+ * finite; when l_0 = +inf the +inf choices share the weight equally; when
+ * l_0 is -inf or NaN (every logit masked) the k weights are equal.
  * Requires 1 <= E <= 1024, 1 <= k <= min(E, 32), T k < 2^31.  T = 0 writes
- * all-zero offsets.  Non-finite logits are outside the contract.
+ * all-zero offsets.
  */
 h32_status h32_moe_route(const float *logits, int64_t T, int32_t E, int64_t ldl, int32_t k,
                          int32_t *topk_id, float *topk_w, int32_t *expert_off, int32_t *row_idx,
@@ -326,10 +337,14 @@ h32_status h32_moe_combine(const float *y, int64_t R, int64_t ldy, const int32_t
                            int64_t ldo, void *stream);
 
 /*
- * Synchronize `stream`, then report and clear the device status word of every
- * kernel this library launched on the current device since the last call:
- * H32_OK, H32_ERR_TIMEOUT or H32_ERR_DEVICE_GUARD (or H32_ERR_CUDA when the
- * synchronization itself fails).
+ * Synchronize `stream`, then report and clear the device status words that
+ * this library's kernels on the current device write: H32_OK, H32_ERR_TIMEOUT
+ * or H32_ERR_DEVICE_GUARD (or H32_ERR_CUDA when the synchronization, or a
+ * copy, fails).  The words are shared by every stream of the device.  Each is
+ * read and cleared in one atomic step on the device, so a problem recorded
+ * by a kernel that is still running on another stream is reported by this
+ * call or by a later one, never lost.  Calls from several host threads are
+ * serialized.
  */
 h32_status h32_device_status(void *stream);
 

@@ -8,7 +8,7 @@
  * Input file: int64 M, N, K, then x and w as fp32, row-major.
  * Usage: h32_c_caller <input> <output>.  Exit status 0 = success, 1 = a
  * library status that is not H32_OK (printed), 2 = I/O or CUDA runtime error.
- * Test infrastructure: built and run by tests/test_gpu_c_caller.py.
+ * Test infrastructure: built and run by tests/test_c_caller.py.
  */
 #include <stdint.h>
 #include <stdio.h>

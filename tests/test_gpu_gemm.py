@@ -203,14 +203,15 @@ def test_pp512_attention_projection(h32, xbits):
     sampled_check(h32, wq, wd, xq, xd, p.K, xbits)
 
 
+@pytest.mark.parametrize("xbits", [4, 8])
 @pytest.mark.parametrize("proj", ["gate_up", "down"])
-def test_pp512_ffn(h32, proj):
+def test_pp512_ffn(h32, proj, xbits):
     p = wl.FFN_GATE_UP if proj == "gate_up" else wl.FFN_DOWN
     x = p.activations(512, 0, wl.CFG_FFN)
     w = p.weights(0, wl.CFG_FFN)
     wq, wd = oracle.quantize_weights_q4_0(w)
-    xq, xd = oracle.quantize_act_q4(x)
-    sampled_check(h32, wq, wd, xq, xd, p.K, 4)
+    xq, xd = (oracle.quantize_act_q4 if xbits == 4 else oracle.quantize_act_q8)(x)
+    sampled_check(h32, wq, wd, xq, xd, p.K, xbits)
 
 
 # --------------------------------------------------------------------------

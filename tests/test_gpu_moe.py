@@ -101,6 +101,27 @@ def test_route_row_pitch_and_equal_rows(h32):
     assert rid[3].tolist() == list(range(6))
 
 
+def test_route_non_finite_logits(h32):
+    """Masked experts (-inf), +inf and NaN logits, placed so that a NaN or a
+    -inf sits ahead of finite logits in every lane position: ids, offsets and
+    row maps exact, weights as the oracle's limits of the softmax."""
+    r = np.random.default_rng(23)
+    T, E = 96, 70
+    l = r.standard_normal((T, E)).astype(np.float32)
+    for t in range(T):
+        m = r.random(E)
+        l[t, m < 0.3] = -np.inf
+        l[t, (m >= 0.3) & (m < 0.4)] = np.nan
+    l[0, :] = -np.inf                       # every expert masked: equal weights
+    l[1, :] = np.nan
+    l[2, :5] = np.inf                       # several +inf: they share the weight
+    l[3, 0] = np.nan                        # a NaN in the first lane position
+    l[4, ::2] = -np.inf
+    for k in (1, 4, 8, 32):
+        rid, rw, _, _, _ = _check_route(h32, l, k)
+    assert np.all(rw[0] == np.float32(1) / np.float32(32))
+
+
 def test_route_empty_and_bad_args(h32):
     import torch
     l = torch.zeros((0, 16), dtype=torch.float32, device="cuda")

@@ -65,6 +65,38 @@ def test_quantize_tc_matches_oracle(h32, M, K):
     assert np.array_equal(xdt[:, :M].T.view(np.uint32), rd.view(np.uint32))
 
 
+EDGE_ROWS = [np.zeros(32), np.r_[2.0 ** -130, np.zeros(31)], np.arange(32.0),
+             np.r_[7, 2.5, -0.5, 1.5, 3.5, -2.5, np.zeros(26)], np.full(32, -3.0),
+             np.r_[3e38, -3e38, np.zeros(30)], np.eye(32)[5],
+             np.r_[2.0 ** 24, 1.0, np.zeros(14), -(2.0 ** 24), np.zeros(15)],
+             np.r_[np.zeros(7), -(2.0 ** -131), np.zeros(12), 2.0 ** -133, np.zeros(11)]]
+
+
+@pytest.mark.parametrize("rotate", [True, False])
+def test_quantize_tc_edge_blocks(h32, rotate):
+    """Zero, subnormal-size (1/d overflows: zeros stay code 0), ramp, tie,
+    constant, overflowing, one-hot and wide-range blocks through the tc
+    quantizers (4-bit, 8-bit and the gathered form) against the oracle."""
+    import torch
+    x = np.stack(EDGE_ROWS).astype(np.float32)
+    M, K = x.shape[0], 32
+    rq, rd = oracle.quantize_act_q4(x, rotate)
+    xw, xdt = h32.h32_quantize_act_q4_tc(torch_of(x), rotate=rotate)
+    assert np.array_equal(e4m3_value(np_of(xw)), oracle.decode_act4(rq, K).astype(np.float64))
+    assert np.array_equal(np_of(xdt)[:, :M].T.view(np.uint32), rd.view(np.uint32))
+    rq8, rd8 = oracle.quantize_act_q8(x, rotate)
+    xw8, xdt8 = h32.h32_quantize_act_q8_tc(torch_of(x), rotate=rotate)
+    assert np.array_equal(_q8_codes_from_tc(np_of(xw8), K)[0], rq8.astype(np.float64))
+    assert np.array_equal(np_of(xdt8)[:, :M].T.view(np.uint32), rd8.view(np.uint32))
+    idx = np.array([8, 1, 1, 5, 0, 7], np.int32)
+    xg, xgd = h32.h32_quantize_act_q4_tc_gather(torch_of(x), torch_of(idx), rotate=rotate)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    assert np.array_equal(e4m3_value(np_of(xg)),
+                          oracle.decode_act4(rq, K).astype(np.float64)[idx])
+    assert np.array_equal(np_of(xgd)[:, :idx.size].T.view(np.uint32), rd[idx].view(np.uint32))
+
+
 def _tc_operands(h32, x, w, bf16=True):
     """x: bf16 bits (uint16) when bf16, else fp32."""
     wq, wd = oracle.quantize_weights_q4_0(w)
@@ -429,6 +461,33 @@ def test_gemm_q8_tc_pp512_sampled(h32):
     assert np.array_equal(y[mi, ni].view(np.uint32), r32.view(np.uint32))
 
 
+@pytest.mark.parametrize("proj", ["gate_up", "down"])
+def test_gemm_q8_tc_pp512_ffn_sampled(h32, proj):
+    """The exact 8-bit route at the pp512 FFN shapes (gate/up 512 x 34816 x 5120,
+    down 512 x 5120 x 17408), sampled outputs against the oracle bit for bit."""
+    import torch
+    p = wl.FFN_GATE_UP if proj == "gate_up" else wl.FFN_DOWN
+    x = p.activations(512, 0, wl.CFG_FFN)
+    w = p.weights(0, wl.CFG_FFN)
+    wq, wd = oracle.quantize_weights_q4_0(w)
+    xq, xd = oracle.quantize_act_q8(x)
+    wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(wq), torch_of(wd.view(np.int16)))
+    xw8, xdt = h32.h32_quantize_act_q8_tc(torch_bf16(x))
+    # the quantizer at this size: every code and scale
+    codes, _ = _q8_codes_from_tc(np_of(xw8), p.K)
+    assert np.array_equal(codes, xq.astype(np.float64))
+    assert np.array_equal(np_of(xdt)[:, :512].T.view(np.uint32), xd.view(np.uint32))
+    y = np_of(h32.q4_0_x_q8_gemm_tc(wp, wsc, xw8, xdt, M=512))
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r = np.random.default_rng(3)
+    mi = np.concatenate([r.integers(0, 512, 3000), [0, 511, 511, 0]])
+    ni = np.concatenate([r.integers(0, p.N, 3000), [0, p.N - 1, 0, p.N - 1]])
+    r32, _, _ = oracle.gemm_sampled(wq, wd, xq, xd, p.K, mi, ni)
+    assert np.array_equal(y[mi, ni].view(np.uint32), r32.view(np.uint32))
+    assert np.isfinite(y).all()
+
+
 # --------------------------------------------------------------------------
 # the fused producer: the product quantized for the next projection in the
 # GEMM's own epilogue
@@ -453,6 +512,32 @@ def test_gemm_tc_quant_next_pp512_sampled_rows(h32):
     assert np.array_equal(e4m3_value(np_of(xn)[rows]),
                           oracle.decode_act4(nq, p.N).astype(np.float64))
     assert np.array_equal(np_of(xnd)[:, rows].T.view(np.uint32), nd.view(np.uint32))
+
+
+@pytest.mark.parametrize("rot", [True, False])
+def test_gemm_tc_quant_next_degenerate_blocks(h32, rot):
+    """Output blocks of the fused producer that are all zero (a zero token row)
+    or of subnormal size (token rows scaled by 2^-131 and 2^-140, so the output
+    blocks' 1/d overflows): the codes must equal the oracle's quantizer on the
+    oracle's output, zeros staying code 0."""
+    import torch
+    M, N, K = 40, 128, 256
+    x = wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, 296).astype(np.float32)
+    x[3] = 0.0
+    x[5] *= np.float32(2.0 ** -131)
+    x[6, :128] *= np.float32(2.0 ** -131)
+    x[7] *= np.float32(2.0 ** -140)
+    w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, 297)
+    (wq, wd, xq, xd), (wp, wsc, xw, xdt) = _tc_operands(h32, x, w, bf16=False)
+    y, xn, xnd = h32.q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=M, rotate_next=rot)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r32, _, _ = oracle.gemm(wq, wd, xq, xd, K)
+    assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
+    nq, nd = oracle.quantize_act_q4(r32, rot)
+    assert np.any(np.isinf(np.float32(1.0) / nd[nd > 0]))   # some block is degenerate
+    assert np.array_equal(e4m3_value(np_of(xn)), oracle.decode_act4(nq, N).astype(np.float64))
+    assert np.array_equal(np_of(xnd)[:, :M].T.view(np.uint32), nd.view(np.uint32))
 
 
 @pytest.mark.parametrize("M,N,K,rot", [(70, 160, 256, True), (17, 96, 128, False),

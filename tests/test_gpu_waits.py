@@ -51,3 +51,61 @@ def test_one_poll_wait_bound_reports_timeout_and_recovers(h32):
     assert h32.h32_device_status() == 0
     r32, _, _ = oracle.gemm(rwq, rwd, rxq, rxd, 256)
     assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
+
+
+def _tc_ones(h32, rows, K, scale=1.0):
+    """tc-form operands whose every code is 1 (e4m3 0x38), scales `scale`."""
+    import torch
+    w = torch.full((rows, K), 0x38, dtype=torch.uint8, device="cuda")
+    sc = torch.full((rows, (K // 32 + 3) // 4 * 4), scale, dtype=torch.float32, device="cuda")
+    return w, sc
+
+
+def _exact_small_case(h32):
+    """A small tc product after the timeouts, against the oracle bit for bit."""
+    x = wl.f32_to_bf16_bits(wl.act_normal_outliers(70, 256, 0.01, 20.0, 0, wl.CFG_TEST, 122))
+    w = wl.weights_normal(160, 256, 0.02, 0, wl.CFG_TEST, 123)
+    rwq, rwd = oracle.quantize_weights_q4_0(w)
+    rxq, rxd = oracle.quantize_act_q4(x)
+    from tests._gpu import torch_bf16
+    wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(rwq), torch_of(rwd.view(np.int16)))
+    xw, xdt = h32.h32_quantize_act_q4_tc(torch_bf16(x))
+    y = h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=70)
+    assert h32.h32_device_status() == 0
+    r32, _, _ = oracle.gemm(rwq, rwd, rxq, rxd, 256)
+    assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
+
+
+@pytest.mark.parametrize("kind", ["q4_tc", "q8_tc", "experts_tc"])
+def test_tc_gemm_one_poll_wait_bound(h32, kind):
+    """The tensor-core-form GEMM (the chain's kernel, its 8-bit and its expert
+    instances) under a one-poll wait bound: the TMA, MMA and epilogue roles that
+    give up record H32_ERR_TIMEOUT, drain their copies and MMAs, free TMEM and
+    return; the status is reported once and the same context then computes
+    exact results."""
+    import torch
+    M, N, K = 512, 4096, 2048
+    wp, wsc = _tc_ones(h32, N, K, 0.0625)
+    xb = 2 if kind == "q8_tc" else 1
+    xw = torch.full((M, K * xb), 0x38, dtype=torch.uint8, device="cuda")
+    xdt = torch.ones((K // 32, M), dtype=torch.float32, device="cuda")
+    E = 8
+    off = torch.tensor([i * M // E for i in range(E + 1)], dtype=torch.int32, device="cuda")
+    wpe, wsce = _tc_ones(h32, E * 512, K, 0.0625)
+    assert h32.h32_device_status() == 0
+    h32.h32_set_wait_limit(1)
+    try:
+        for _ in range(3):
+            if kind == "q4_tc":
+                h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M)
+            elif kind == "q8_tc":
+                h32.q4_0_x_q8_gemm_tc(wp, wsc, xw, xdt, M=M)
+            else:
+                h32.q4_0_x_q4_gemm_tc_experts(wpe, wsce, xw, xdt, off, 512, R=M)
+        st = h32.h32_device_status()
+    finally:
+        h32.h32_set_wait_limit(0)
+    assert st == h32.H32_ERR_TIMEOUT
+    assert h32.h32_device_status() == 0
+    torch.cuda.synchronize()
+    _exact_small_case(h32)

@@ -54,12 +54,16 @@ GEMM_SOURCES = {"tc": [os.path.join(_CSRC, f) for f in ("h32_gemm_tc.cu", "h32_c
                                                         "h32_epilogue.cuh", "h32_tcform.cuh")],
                 "q4_0": [os.path.join(_CSRC, f) for f in ("h32_gemm.cu", "h32_common.cuh",
                                                           "h32_epilogue.cuh")]}
-SMS = 152
-EVENT_EVERY = 8           # per-kernel events on one timed step in this many
-FP32_LANES_PER_SM = 128   # FP32 FMA/FMUL lanes per SM per clock
-# measured on GB300: interleaved mul.f32x2 / fma.f32x2 issue at 0.89 packed operations per
-# clock per sub-partition, 57 fp32 lane operations, 1.78x the 32 lanes of the unit count
-FP32_MIX_OVER_UNITS = 1.78
+PEAKS_SUMMARY = os.path.join(ROOT, "profiles", "peaks_gb300.md")
+PEAKS_SOURCE = os.path.join(ROOT, "hadamard_rotated_bit_gb300", "peaks", "h32_peaks.cu")
+FP32_LANES_PER_SM = 128   # fp32 lanes per SM per clock (the unit count)
+# per-SM rates measured on GB300 by the probes of hadamard_rotated_bit_gb300/peaks
+# (`bench.py --peaks`), as committed in profiles/peaks_gb300.md; used when that file
+# cannot be read
+FALLBACK_RATES = {"fp32_mix_lane_ops_per_clock_per_sm": 168.5,
+                  "tcgen05_f8f6f4_macs_per_clock_per_sm": 7826.0,
+                  "mma_sync_s8_macs_per_clock_per_sm": 252.0}
+ISOLATED_REPS = 25        # launches a kernel is timed alone (median), L2 flushed before each
 
 
 # --------------------------------------------------------------------------
@@ -110,6 +114,23 @@ def load_peaks():
     except (OSError, ValueError):
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                 "sm_max_mhz": 2070.0}, "fallback"
+
+
+def load_rates():
+    """The per-SM rates the rooflines divide by: fp32 lane operations per clock of
+    the epilogue's mul.f32x2 + fma.f32x2 mix, and the MACs per clock of the FP8
+    tensor cores (tcgen05) and of the legacy int8 path (mma.sync s8), read from the
+    committed probe summary."""
+    rates = dict(FALLBACK_RATES)
+    try:
+        text = open(PEAKS_SUMMARY).read()
+    except OSError:
+        return rates, "fallback constants in bench.py"
+    for k in rates:
+        m = re.search(rf"{k}:\s*([0-9.]+)", text)
+        if m:
+            rates[k] = float(m.group(1))
+    return rates, "profiles/peaks_gb300.md (measured with bench.py --peaks)"
 
 
 def source_sha(paths) -> str:
@@ -221,6 +242,23 @@ class Chain:
             self.sets.append(projs)
         torch.cuda.synchronize()
 
+    def kernel_fn(self, s, k, stream):
+        """Kernel k of the chain (2 i = projection i's quantizer, 2 i + 1 its GEMM)
+        on input set s, as a callable."""
+        h = self.h32
+        p = self.sets[s % len(self.sets)][k // 2]
+        tc = self.form == "tc"
+        if k % 2 == 0:
+            if tc:
+                return lambda: h.h32_quantize_act_q4_tc(p["x"], xw=p["xq"], xdt=p["xd"],
+                                                        stream=stream)
+            return lambda: h.h32_quantize_act_q4(p["x"], xq=p["xq"], xd=p["xd"], stream=stream)
+        if tc:
+            return lambda: h.q4_0_x_q4_gemm_tc(p["wq"], p["wd"], p["xq"], p["xd"], M=M_TOKENS,
+                                               y=p["y"], stream=stream)
+        return lambda: h.q4_0_x_q4_gemm(p["wq"], p["wd"], p["xq"], p["xd"], y=p["y"],
+                                        stream=stream)
+
     def step(self, s, stream, events=None):
         """Enqueue one chain pass on `stream`; optionally bracket each kernel with events."""
         h = self.h32
@@ -252,18 +290,41 @@ def kernel_names(form):
     return names
 
 
-def algorithmic(p, form="tc"):
-    """Per-launch algorithmic work of one projection (M = 512)."""
-    M, N, K = M_TOKENS, p.N, p.K
+def algorithmic(p, form="tc", M=M_TOKENS):
+    """Per-launch algorithmic work of one projection.  Bytes are the scope table's:
+    bf16 in, 4-bit codes (0.5 B) and fp32 scales out for the quantizer (2.625 B an
+    element); Q4_0 weights (0.5 B a code, fp16 scales), 4-bit activations and the
+    fp32 output for the GEMM.  The tc form stores a code in a byte: its actual
+    bytes are the `*_traffic_bytes`."""
+    N, K = p.N, p.K
     nb = K // 32
     code = 1 if form == "tc" else 0.5          # bytes per stored 4-bit code
     wscale = 4 if form == "tc" else 2          # fp32 (tc) or fp16 (Q4_0) weight scales
     return {
-        "quant_bytes": int(M * K * 2 + M * K * code + M * nb * 4),   # bf16 in, codes + scales out
+        "quant_bytes": int(M * K * 2 + M * K * 0.5 + M * nb * 4),
+        "quant_traffic_bytes": int(M * K * 2 + M * K * code + M * nb * 4),
         "gemm_alu_ops": 2 * M * N * nb,                            # d_w*d_x and one fma per block
         "gemm_int_ops": 2 * M * N * K,                             # 2 MNK (multiply + add)
-        "gemm_bytes": int(N * K * code + N * nb * wscale + M * K * code + M * nb * 4 + M * N * 4),
+        "gemm_bytes": int(N * K * 0.5 + N * nb * 2 + M * K * 0.5 + M * nb * 4 + M * N * 4),
+        "gemm_traffic_bytes": int(N * K * code + N * nb * wscale + M * K * code + M * nb * 4
+                                  + M * N * 4),
     }
+
+
+def isolated_median_ms(torch, fn, stream, flush, reps=ISOLATED_REPS):
+    """Median device time of `fn` over `reps` launches, each after writing a buffer
+    of twice the L2 size (so every launch reads its inputs from HBM)."""
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+    stream.synchronize()
+    return float(np.median([a.elapsed_time(b) for a, b in evs]))
 
 
 def run_gpu(args):
@@ -291,13 +352,9 @@ def run_gpu(args):
     if h32.h32_device_status(stream) != 0:
         raise RuntimeError("device status not OK after warm-up")
 
-    # timed region: device-resident inputs, per-kernel events on the launch stream
-    # on every EVENT_EVERY-th step (events between kernels keep a kernel from
-    # starting under its predecessor's tail, so the other steps run without them)
+    # timed region: device-resident inputs, no events between the kernels (they
+    # would keep each kernel from starting under its predecessor's tail)
     nk = 2 * len(CHAIN)
-    ev_steps = list(range(0, args.steps, EVENT_EVERY))
-    evs = {i: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(nk)] for i in ev_steps}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     barrier(dist, device)
@@ -307,7 +364,7 @@ def run_gpu(args):
     with torch.cuda.stream(stream):
         t0.record(stream)
         for i in range(args.steps):
-            chain.step(i, stream, evs.get(i))
+            chain.step(i, stream)
         t1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
@@ -319,60 +376,91 @@ def run_gpu(args):
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
 
-    per_kernel = np.zeros(nk)
-    for i in ev_steps:
-        for k in range(nk):
-            per_kernel[k] += evs[i][k][0].elapsed_time(evs[i][k][1])
-    per_kernel /= len(ev_steps)  # ms per launch
-
     tokens = M_TOKENS * args.steps * world
     value = tokens / (elapsed_ms / 1e3)
     ms_per_step = elapsed_ms / args.steps
+
+    # per-kernel device time in the chain: events around every kernel of every step
+    # of a second pass of the same chain (same buffers, stream and input sets)
+    ev_steps = max(20, min(args.steps, 400))
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(nk)] for _ in range(ev_steps)]
+    with torch.cuda.stream(stream):
+        for i in range(ev_steps):
+            chain.step(i, stream, evs[i])
+    stream.synchronize()
+    per_kernel = np.array([np.mean([evs[i][k][0].elapsed_time(evs[i][k][1])
+                                    for i in range(ev_steps)]) for k in range(nk)])
+
+    # each kernel alone: median of ISOLATED_REPS launches, L2 flushed before each
+    props = torch.cuda.get_device_properties(device)
+    flush = torch.empty(max(2 * int(getattr(props, "L2_cache_size", 0)), 256 << 20),
+                        dtype=torch.uint8, device=device)
+    isolated = np.array([isolated_median_ms(torch, chain.kernel_fn(0, k, stream), stream, flush)
+                         for k in range(nk)])
+    del flush
+    if h32.h32_device_status(stream) != 0:
+        raise RuntimeError("device status not OK after the per-kernel timing")
 
     # end to end through host buffers: H2D of the step's activations, the
     # chain, D2H of the step's outputs, all inside the timed region
     e2e = time_e2e(torch, h32, chain, stream, args, dist, device, world)
 
-    # roofline of the dominant kernel
+    # rooflines: the SM count from the device, the per-SM rates measured by the
+    # committed probes, the maximum SM clock of the measured peaks
+    sms = int(props.multi_processor_count)
+    rates, rate_src = load_rates()
+    clock_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    ghz = clock_mhz / 1e3
+    fp32_peak = sms * rates["fp32_mix_lane_ops_per_clock_per_sm"] * ghz / 1e3   # T lane-ops/s
+    fp32_units = sms * FP32_LANES_PER_SM * ghz / 1e3
+    fp8_peak = 2 * sms * rates["tcgen05_f8f6f4_macs_per_clock_per_sm"] * ghz / 1e3   # T ops/s
+    int8_peak = 2 * sms * rates["mma_sync_s8_macs_per_clock_per_sm"] * ghz / 1e3
+
     names = kernel_names(args.form)
     dom = int(np.argmax(per_kernel))
     p = CHAIN[dom // 2]
     alg = algorithmic(p, args.form)
-    clock_mhz = float(peaks.get("sm_max_mhz", 2070.0))
     if dom % 2 == 1:
-        alu_peak = SMS * FP32_LANES_PER_SM * clock_mhz * 1e6 / 1e12  # T lane-ops/s
         achieved = alg["gemm_alu_ops"] / (per_kernel[dom] / 1e3) / 1e12
         roofline = {"kernel": names[dom], "bound": "alu", "achieved": round(achieved, 3),
-                    "peak": round(alu_peak, 3), "unit": "Tops/s (fp32 lane ops)",
-                    "frac": round(achieved / alu_peak, 4), "traffic": profiled_traffic(args.form),
-                    "peak_source": f"{SMS} SMs x {FP32_LANES_PER_SM} FP32 lanes x "
-                                   f"{clock_mhz:.0f} MHz ({peak_src} max SM clock)",
+                    "peak": round(fp32_peak, 3), "unit": "T fp32 lane ops/s",
+                    "frac": round(achieved / fp32_peak, 4),
+                    "traffic": profiled_traffic(args.form),
+                    "peak_source": f"{sms} SMs x {rates['fp32_mix_lane_ops_per_clock_per_sm']:.1f} "
+                                   f"fp32 lane ops per clock (mul.f32x2 + fma.f32x2, measured, "
+                                   f"{rate_src}) x {clock_mhz:.0f} MHz ({peak_src} max SM clock)",
                     "algorithmic_per_launch": alg["gemm_alu_ops"],
                     "ms_per_launch": round(per_kernel[dom], 5),
-                    "frac_of_measured_fp32_mix": round(achieved / (alu_peak * FP32_MIX_OVER_UNITS), 4)}
+                    "frac_of_fp32_unit_count": round(achieved / fp32_units, 4),
+                    "frac_of_fp8_tensor_measured": round(
+                        alg["gemm_int_ops"] / (per_kernel[dom] / 1e3) / 1e12 / fp8_peak, 4)}
     else:
         achieved = alg["quant_bytes"] / (per_kernel[dom] / 1e3) / 1e9
         roofline = {"kernel": names[dom], "bound": "hbm", "achieved": round(achieved, 1),
                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None}
 
-    # secondary views of the same timed launches
-    int8_peak = 252 * 2 * SMS * clock_mhz * 1e6 / 1e12    # measured mma.sync s8 MAC/clk/SM
-    fp8_peak = 2.0 * float(peaks["bf16_tflops"])           # nominal fp8 : bf16 ratio 2
+    # every kernel of the chain, in the chain and alone
     kernels = {}
     for i, p in enumerate(CHAIN):
         alg = algorithmic(p, args.form)
         tq, tg = per_kernel[2 * i], per_kernel[2 * i + 1]
+        iq, ig = isolated[2 * i], isolated[2 * i + 1]
         kernels[p.name] = {
-            "quant_ms": round(tq, 5),
-            "quant_GBps": round(alg["quant_bytes"] / (tq / 1e3) / 1e9, 1),
-            "quant_hbm_frac": round(alg["quant_bytes"] / (tq / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-            "gemm_ms": round(tg, 5),
+            "quant_ms_in_chain": round(tq, 5),
+            "quant_ms_alone": round(iq, 5),
+            "quant_GBps_alone": round(alg["quant_bytes"] / (iq / 1e3) / 1e9, 1),
+            "quant_hbm_frac_alone": round(alg["quant_bytes"] / (iq / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "quant_algorithmic_bytes": alg["quant_bytes"],
+            "quant_traffic_bytes": alg["quant_traffic_bytes"],
+            "gemm_ms_in_chain": round(tg, 5),
+            "gemm_ms_alone": round(ig, 5),
             "gemm_eff_TOPS": round(alg["gemm_int_ops"] / (tg / 1e3) / 1e12, 1),
-            "gemm_frac_of_int8_mma_peak": round(alg["gemm_int_ops"] / (tg / 1e3) / 1e12 / int8_peak, 3),
-            "gemm_frac_of_fp8_tensor_peak": round(alg["gemm_int_ops"] / (tg / 1e3) / 1e12 / fp8_peak, 4),
-            "gemm_alu_frac": round(alg["gemm_alu_ops"] / (tg / 1e3) / 1e12 /
-                                   (SMS * FP32_LANES_PER_SM * clock_mhz * 1e6 / 1e12), 4),
+            "gemm_frac_of_fp32_measured": round(alg["gemm_alu_ops"] / (tg / 1e3) / 1e12 / fp32_peak, 4),
+            "gemm_frac_of_fp32_unit_count": round(alg["gemm_alu_ops"] / (tg / 1e3) / 1e12 / fp32_units, 4),
+            "gemm_frac_of_fp8_tensor_measured": round(alg["gemm_int_ops"] / (tg / 1e3) / 1e12 / fp8_peak, 4),
+            "gemm_x_int8_mma_sync_measured": round(alg["gemm_int_ops"] / (tg / 1e3) / 1e12 / int8_peak, 3),
         }
 
     line = {
@@ -389,8 +477,13 @@ def run_gpu(args):
         "gpu_launches": nk * args.steps,
         "clocks": clocks,
         "kernels": kernels,
-        "peaks": {"int8_mma_sync_TOPS": round(int8_peak, 1), "fp8_tensor_TFLOPS": fp8_peak,
-                  "hbm_GBps": peaks["hbm_gbs"], "source": peak_src},
+        "kernel_timing": (f"in_chain: mean over {ev_steps} chain steps with events around every "
+                          f"kernel (after the timed region); alone: median of {ISOLATED_REPS} "
+                          "launches, L2 flushed before each"),
+        "peaks": {"fp32_T_lane_ops": round(fp32_peak, 2), "fp32_unit_count_T_lane_ops": round(fp32_units, 2),
+                  "fp8_tensor_TOPS": round(fp8_peak, 1), "int8_mma_sync_TOPS": round(int8_peak, 1),
+                  "hbm_GBps": peaks["hbm_gbs"], "sms": sms, "hbm_source": peak_src,
+                  "rates_source": rate_src},
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_tokens)
@@ -477,40 +570,69 @@ def oracle_prepare(sample_tokens: int):
     return prepared
 
 
-def oracle_step(prepared) -> float:
-    """One timed pass of the oracle over the sample: quantize + full GEMM per projection."""
+def oracle_step(prepared, pool=None, threads=1) -> float:
+    """One timed pass of the oracle over the sample: quantize + full GEMM per
+    projection.  With `threads` > 1 each GEMM's output columns are split among
+    the pool's threads (the C oracle releases the GIL; every output is computed
+    by the same function in the same order)."""
     import oracle
     t = time.perf_counter()
     for wq, wd, x, K in prepared:
         xq, xd = oracle.quantize_act_q4(x)
-        oracle.gemm(wq, wd, xq, xd, K)
+        if threads <= 1:
+            oracle.gemm(wq, wd, xq, xd, K)
+        else:
+            N = wq.shape[0]
+            cuts = np.linspace(0, N, threads + 1).astype(int)
+            list(pool.map(lambda ab: oracle.gemm(wq[ab[0]:ab[1]], wd[ab[0]:ab[1]], xq, xd, K),
+                          [(a, b) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]))
     return time.perf_counter() - t
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 def cpu_baseline(sample_tokens: int):
     """Time the CPU oracle, as it stands, on a bounded sample of the same
     workload: `sample_tokens` of the 512 tokens through the whole chain
-    (quantize + GEMM for all three projections), single threaded."""
-    dt = oracle_step(oracle_prepare(sample_tokens))
-    return {"value": round(sample_tokens / dt, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "seconds": round(dt, 2),
+    (quantize + GEMM for all three projections), on one core and on every core
+    this process may run on."""
+    from concurrent.futures import ThreadPoolExecutor
+    prepared = oracle_prepare(sample_tokens)
+    cores = host_cores()
+    dt1 = oracle_step(prepared)
+    with ThreadPoolExecutor(cores) as pool:
+        dtn = oracle_step(prepared, pool, cores)
+    return {"value": round(sample_tokens / dtn, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "seconds": round(dtn, 2), "value_one_core": round(sample_tokens / dt1, 4),
+            "seconds_one_core": round(dt1, 2),
             "sample": f"{sample_tokens} of the 512 tokens through the whole chain "
-                      f"(3 quantizations + 3 full GEMMs), single-threaded C oracle"}
+                      f"(3 quantizations + 3 full GEMMs), C oracle; `value` with each GEMM's "
+                      f"output columns split over {cores} threads (all granted cores), "
+                      f"`value_one_core` single-threaded"}
 
 
 def run_reference(args):
-    """The reference arm: the CPU oracle on the host cores, each step a bounded
-    sample (`--ref-tokens` tokens) of the pp512 chain."""
+    """The reference arm: the CPU oracle on the host cores (every granted core),
+    each step a bounded sample (`--ref-tokens` tokens) of the pp512 chain."""
+    from concurrent.futures import ThreadPoolExecutor
     rank, world, local = dist_env()
     if rank != 0:
         return None
     prepared = oracle_prepare(args.ref_tokens)
-    for _ in range(args.warmup):
-        oracle_step(prepared)
-    secs = sum(oracle_step(prepared) for _ in range(args.steps))
+    cores = host_cores()
+    with ThreadPoolExecutor(cores) as pool:
+        for _ in range(args.warmup):
+            oracle_step(prepared, pool, cores)
+        secs = sum(oracle_step(prepared, pool, cores) for _ in range(args.steps))
     value = args.ref_tokens * args.steps / secs
     sample = (f"{args.ref_tokens} of the 512 tokens per step through the whole chain "
-              f"(3 quantizations + 3 full GEMMs), single-threaded C oracle")
+              f"(3 quantizations + 3 full GEMMs), C oracle, each GEMM's output columns split "
+              f"over {cores} threads")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * secs / args.steps, 2), "higher_is_better": True,
@@ -518,10 +640,25 @@ def run_reference(args):
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "tokens_per_step": args.ref_tokens,
                        "note": "each step is a bounded sample of the pp512 chain"},
-            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+def run_peaks(args):
+    """Build and run the rate microbenchmarks (hadamard_rotated_bit_gb300/peaks):
+    their JSON lines, as committed in profiles/peaks_gb300.md."""
+    out_dir = os.path.join(ROOT, "hadamard_rotated_bit_gb300", "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    exe = os.path.join(out_dir, "h32_peaks")
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe,
+                    PEAKS_SOURCE], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=600)
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    if r.returncode != 0:
+        raise RuntimeError(f"peak probes failed: {r.stdout}{r.stderr}")
+    return lines
 
 
 def run_only_gemm(args):
@@ -960,7 +1097,7 @@ def main(argv=None):
     ap.add_argument("--form", choices=list(FORMS), default="tc",
                     help="operand form of the chain (default: tensor-core form)")
     ap.add_argument("--cpu-tokens", type=int, default=24)
-    ap.add_argument("--ref-tokens", type=int, default=1)
+    ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true",
                     help="measure the other configurations (8-bit and unrotated routes, MoE, "
@@ -970,12 +1107,19 @@ def main(argv=None):
     ap.add_argument("--only-quant", choices=["q4", "q8", "q4_tc", "q8_tc"], default=None,
                     help="time the activation quantizer alone on a 16384 x 17408 bf16 matrix "
                          "(a streaming case for profilers)")
+    ap.add_argument("--peaks", action="store_true",
+                    help="run the rate microbenchmarks behind the rooflines (fp32 pipe, tensor "
+                         "cores, TMEM, shared memory, mbarrier), one JSON line each")
     ap.add_argument("--only-moe", action="store_true",
                     help="the MoE micro-batch lines of --suite alone (expert GEMMs, and the "
                          "whole layer with the router and the combine)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.peaks:
+        for ln in run_peaks(args):
+            print(json.dumps(ln), flush=True)
+        return
     if args.suite or args.only_moe:
         for ln in run_suite(args, only_moe=args.only_moe):
             print(json.dumps(ln), flush=True)

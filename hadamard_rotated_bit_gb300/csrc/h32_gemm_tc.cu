@@ -36,11 +36,6 @@
 // programmatic dependent launch: nothing touches global memory before the
 // previous kernel of the stream has completed.
 
-// how the epilogue's TMEM fragment maps to threads (rows a thread holds: 0 -> 1,
-// 1 -> 2, 2 -> 4); see epilogue_tiles
-#ifndef H32_TC_LAYOUT
-#define H32_TC_LAYOUT 0
-#endif
 // epilogue warps per TMEM lane quarter
 #ifndef H32_TC_EPI_PER_QUAD
 #define H32_TC_EPI_PER_QUAD 4
@@ -264,32 +259,18 @@ __device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a, const int *s_o
 // The epilogue of one warp over all of its tiles, without block sums: ring
 // positions of the shared-memory stages and TMEM buffers are carried as
 // counters and phase bits, arrivals come from one elected lane.  Returns false
-// when a wait gave up.
-//
-// LAY picks how a warp's TMEM fragment maps to its threads (the warp always
-// covers its lane quarter's 32 weight rows x its share of the columns):
-//   0  32x32b: a thread holds one row; every token scale of a chunk is a
-//      broadcast shared-memory load (4 per 16 columns and block)
-//   1  16x32bx2: a thread holds two rows (t % 16 and t % 16 + 16) and 8 of a
-//      chunk's 16 columns: 2 token-scale loads per 16 columns and block
-//   2  16x256b: a thread holds four rows (t / 4 + 8 k) and 4 of a chunk's
-//      columns, two column pairs: 2 narrow token-scale loads per 16 columns
-// The fused producer (kQN) needs 0: its warp's 32 lanes are one 32-block of
-// the next projection's input.
-template <int EPQ, int XB, bool kQN, bool kTail, int LAY = 0>
+// when a wait gave up.  A warp holds its lane quarter's 32 weight rows (one a
+// thread, the 32x32b TMEM fragment) times its share of the tile's columns.
+template <int EPQ, int XB, bool kQN, bool kTail>
 __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const int *s_off,
                                                const int *s_tpre, uint64_t *bars, const float *s_sa,
                                                const float *s_sb, uint32_t tmem, int warp, int lane,
                                                volatile int *abort_flag) {
     using C = TcCfg<EPQ, XB>;
-    static_assert(!kQN || LAY == 0, "the fused producer takes one row a thread");
     const int ew = warp - C::kProdWarps;
     const int quad = warp & 3;                 // TMEM lanes 32 quad .. 32 quad + 31
     const int part = ew >> 2;                  // share of the columns
-    // the rows this thread holds (quarter-relative), by layout
-    const int row = quad * 32 + lane;                                    // LAY 0
-    const int row2 = quad * 32 + (lane & 15), half = lane >> 4;          // LAY 1: row2, row2 + 16
-    const int row4 = quad * 32 + (lane >> 2), g4 = lane & 3;             // LAY 2: row4 + 8 k
+    const int row = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const int nst = a.nb / 4;
     const uint64_t lim = a.wait_limit;
@@ -307,68 +288,27 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
         for (int i = 0; i < 8 * C::kMaxChunks; ++i) acc[i] = 0ull;
         for (int st = 0; st < nst; ++st) {
             if (!warp_wait(&bars[kBarFull + s], sph, lim, abort_flag)) return false;
-            const float *sa = s_sa + s * (kScaleBytes / 4);        // [128 rows][4 blocks]
+            const float4 dw4 = *reinterpret_cast<const float4 *>(s_sa + s * (kScaleBytes / 4) + 4 * row);
+            const float dws[4] = {dw4.x, dw4.y, dw4.z, dw4.w};
             const float *sb = s_sb + s * (kScaleBytes / 4) + c0;   // [4 blocks][bn tokens]
-            // the weight scales of the thread's rows for the stage's 4 blocks
-            float dws[4][4];
-            if constexpr (LAY == 0) {
-                const float4 v = *reinterpret_cast<const float4 *>(sa + 4 * row);
-                dws[0][0] = v.x, dws[0][1] = v.y, dws[0][2] = v.z, dws[0][3] = v.w;
-            } else if constexpr (LAY == 1) {
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const float4 v = *reinterpret_cast<const float4 *>(sa + 4 * (row2 + 16 * k));
-                    dws[k][0] = v.x, dws[k][1] = v.y, dws[k][2] = v.z, dws[k][3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float4 v = *reinterpret_cast<const float4 *>(sa + 4 * (row4 + 8 * k));
-                    dws[k][0] = v.x, dws[k][1] = v.y, dws[k][2] = v.z, dws[k][3] = v.w;
-                }
-            }
 #pragma unroll
             for (int j0 = 0; j0 < 4; j0 += kGroup) {
                 if (!warp_wait(&bars[kBarSFull + gb], gph, lim, abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t tcol0 = tcol_base + gb * (kGroup * 128);
                 // one 16-column chunk of one block per TMEM wait (measured: fewer
-                // live load registers beat fewer waits); every accumulator takes
-                // the blocks in order
+                // live load registers beat fewer waits, and every reordering that
+                // overlaps loads with folds measured slower); every accumulator
+                // takes the blocks in order
 #pragma unroll
                 for (int c = 0; c < C::kMaxChunks; ++c) {
                     if (c < nch) {
 #pragma unroll
                         for (int i = 0; i < kGroup; ++i) {
-                            const int j = j0 + i;
-                            const uint32_t tc = tcol0 + i * 128 + c * 16;
-                            const float *dx = sb + j * a.bn + 16 * c;
-                            if constexpr (LAY == 0) {
-                                uint32_t v[16];
-                                tmem_ld_x16(tc, v);
-                                tmem_ld_wait();
-                                fold16(acc + 8 * c, dws[0][j], dx, v);
-                            } else if constexpr (LAY == 1) {
-                                uint32_t va[8], vb[8];
-                                tmem_ld_16x32bx2_x8(tc, va);
-                                tmem_ld_16x32bx2_x8(tc + (16u << 16), vb);
-                                tmem_ld_wait();
-                                fold8x2(acc + 8 * c, dws[0][j], dws[1][j], dx + 8 * half, va, vb);
-                            } else {
-                                uint32_t va[8], vb[8];
-                                tmem_ld_16x256b_x2(tc, va);
-                                tmem_ld_16x256b_x2(tc + (16u << 16), vb);
-                                tmem_ld_wait();
-                                uint64_t dw2[4];
-#pragma unroll
-                                for (int k = 0; k < 4; ++k)
-                                    dw2[k] = pair_of(__float_as_uint(dws[k][j]),
-                                                     __float_as_uint(dws[k][j]));
-                                const uint64_t p0 = *reinterpret_cast<const uint64_t *>(dx + 2 * g4);
-                                const uint64_t p1 =
-                                    *reinterpret_cast<const uint64_t *>(dx + 8 + 2 * g4);
-                                fold4x4(acc + 8 * c, dw2, p0, p1, va, vb);
-                            }
+                            uint32_t v[16];
+                            tmem_ld_x16(tcol0 + i * 128 + c * 16, v);
+                            tmem_ld_wait();
+                            fold16(acc + 8 * c, dws[j0 + i], sb + (j0 + i) * a.bn + 16 * c, v);
                         }
                     }
                 }
@@ -387,35 +327,20 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
                 sph ^= 1;
             }
         }
-        if (!kQN || a.y) {
-            // acc[8 c + q] holds two adjacent columns of one row: (row, first column)
-            // by layout
+        const int64_t n = ti.n0 + row;
+        if (n < a.N && (!kQN || a.y)) {
 #pragma unroll
             for (int c = 0; c < C::kMaxChunks; ++c) {
                 if (c < nch) {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        int r, col;
-                        if constexpr (LAY == 0) {
-                            r = row;
-                            col = c0 + c * 16 + 2 * q;
-                        } else if constexpr (LAY == 1) {
-                            r = row2 + 16 * (q >> 2);
-                            col = c0 + c * 16 + 8 * half + 2 * (q & 3);
-                        } else {
-                            r = row4 + 8 * (q >> 1);
-                            col = c0 + c * 16 + 8 * (q & 1) + 2 * g4;
-                        }
-                        const int64_t n = ti.n0 + r;
-                        if (n < a.N) {
-                            const uint64_t pr = acc[8 * c + q];
-                            if (col >= ti.clo && col < ti.chi)
-                                a.y[(ti.g0 + col) * a.ldy + n] =
-                                    __uint_as_float(static_cast<uint32_t>(pr));
-                            if (col + 1 >= ti.clo && col + 1 < ti.chi)
-                                a.y[(ti.g0 + col + 1) * a.ldy + n] =
-                                    __uint_as_float(static_cast<uint32_t>(pr >> 32));
-                        }
+                        const int col = c0 + c * 16 + 2 * q;
+                        const uint64_t pr = acc[8 * c + q];
+                        if (col >= ti.clo && col < ti.chi)
+                            a.y[(ti.g0 + col) * a.ldy + n] = __uint_as_float(static_cast<uint32_t>(pr));
+                        if (col + 1 >= ti.clo && col + 1 < ti.chi)
+                            a.y[(ti.g0 + col + 1) * a.ldy + n] =
+                                __uint_as_float(static_cast<uint32_t>(pr >> 32));
                     }
                 }
             }
@@ -423,26 +348,22 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
         // the output quantized for the next projection: this warp's 32 lanes are
         // one 32-block of it for every token column (N % 32 == 0, so a block is
         // all inside or all outside the N rows)
-        if constexpr (kQN) {
-            if (ti.n0 + quad * 32 < a.N) {
-                const int64_t n = ti.n0 + row;
-                const int nb0 = (ti.n0 + quad * 32) >> 5;
+        if (kQN && ti.n0 + quad * 32 < a.N) {
+            const int nb0 = (ti.n0 + quad * 32) >> 5;
 #pragma unroll
-                for (int c = 0; c < C::kMaxChunks; ++c) {
-                    if (c < nch) {
+            for (int c = 0; c < C::kMaxChunks; ++c) {
+                if (c < nch) {
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) {
-                            const int col = c0 + c * 16 + q;
-                            const uint64_t pr = acc[8 * c + (q >> 1)];
-                            const float v =
-                                __uint_as_float(static_cast<uint32_t>(pr >> (32 * (q & 1))));
-                            float d;
-                            const uint32_t byte = quant_lane_block(v, lane, a.qn_rot != 0, &d);
-                            if (col >= ti.clo && col < ti.chi) {
-                                const int64_t g = ti.g0 + col;
-                                a.qn[g * a.N + n] = static_cast<uint8_t>(byte);
-                                if (lane == 0) a.qnd[nb0 * a.ldqnd + g] = d;
-                            }
+                    for (int q = 0; q < 16; ++q) {
+                        const int col = c0 + c * 16 + q;
+                        const uint64_t pr = acc[8 * c + (q >> 1)];
+                        const float v = __uint_as_float(static_cast<uint32_t>(pr >> (32 * (q & 1))));
+                        float d;
+                        const uint32_t byte = quant_lane_block(v, lane, a.qn_rot != 0, &d);
+                        if (col >= ti.clo && col < ti.chi) {
+                            const int64_t g = ti.g0 + col;
+                            a.qn[g * a.N + n] = static_cast<uint8_t>(byte);
+                            if (lane == 0) a.qnd[nb0 * a.ldqnd + g] = d;
                         }
                     }
                 }
@@ -455,7 +376,7 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
 // kEpi: 0 = y only, 1 = y and the block sums, 2 = y (optional) and the output
 // quantized for the next projection.  kTail: the last partial wave's tiles are
 // cut into pieces (TcArgs::tail_first, tail_k).
-template <int EPQ, int XB, int kEpi, bool kTail = false, int LAY = 0>
+template <int EPQ, int XB, int kEpi, bool kTail = false>
 __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_sa,
@@ -661,8 +582,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
     } else if constexpr (!kSums) {
         // ------------------------------------------------------- epilogue
         if constexpr (C::kRegSplit) reg_alloc<C::kEpiRegs>();
-        if (!epilogue_tiles<EPQ, XB, kEpi == 2, kTail, kEpi == 2 ? 0 : LAY>(
-                a, total, s_off, s_tpre, bars, s_sa, s_sb, tmem, warp, lane, abort_flag))
+        if (!epilogue_tiles<EPQ, XB, kEpi == 2, kTail>(a, total, s_off, s_tpre, bars, s_sa, s_sb,
+                                                       tmem, warp, lane, abort_flag))
             set_abort(misc);
     } else {
         // ------------------------------------ epilogue with block sums
@@ -917,11 +838,12 @@ TcPlan plan_tc(int64_t M, int64_t N, int sms, bool allow_cut) {
     return plan;
 }
 
-template <int EPQ, int XB, int kEpi, bool kTail = false, int LAY = H32_TC_LAYOUT>
+template <int EPQ, int XB, int kEpi, bool kTail = false>
 h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStream_t s) {
     using C = TcCfg<EPQ, XB>;
-    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi, kTail, LAY>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    constexpr int kSmem = C::kSmem;
+    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi, kTail>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return launch_status(e);
     if constexpr (C::kRegSplit) {
         // the epilogue's setmaxnreg.inc waits until the pool holds its registers:
@@ -929,7 +851,7 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
         // (read once per kernel; a failed read leaves -1 and refuses every launch)
         static const int regs = [] {
             cudaFuncAttributes fa{};
-            return cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi, kTail, LAY>) == cudaSuccess
+            return cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi, kTail>) == cudaSuccess
                        ? fa.numRegs
                        : -1;
         }();
@@ -938,8 +860,8 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
             return H32_ERR_UNSUPPORTED;
         }
     }
-    const cudaError_t el = launch_pdl(gemm_tc_kernel<EPQ, XB, kEpi, kTail, LAY>, dim3(grid), dim3(C::kThreads),
-                                      C::kSmem, s, maps[0], maps[1], maps[2], maps[3], a);
+    const cudaError_t el = launch_pdl(gemm_tc_kernel<EPQ, XB, kEpi, kTail>, dim3(grid), dim3(C::kThreads),
+                                      kSmem, s, maps[0], maps[1], maps[2], maps[3], a);
     return launch_status(el != cudaSuccess ? el : cudaGetLastError());
 }
 

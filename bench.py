@@ -762,7 +762,79 @@ def _events_time(torch, fn, steps, warmup, stream):
     return e0.elapsed_time(e1) / steps  # ms per call
 
 
-def suite_chain_routes(torch, h32, dev, stream, steps, warmup):
+class Peaks:
+    """The roofline denominators of one run: measured HBM copy rate, and the fp32,
+    FP8-tensor and mma.sync rates of the committed probes times the SM count and
+    the maximum SM clock."""
+
+    def __init__(self, torch, dev):
+        hbm, self.hbm_source = load_peaks()
+        self.hbm_gbs = float(hbm["hbm_gbs"])
+        rates, self.rate_source = load_rates()
+        self.sms = int(torch.cuda.get_device_properties(dev).multi_processor_count)
+        ghz = float(hbm.get("sm_max_mhz", 2070.0)) / 1e3
+        self.fp32 = self.sms * rates["fp32_mix_lane_ops_per_clock_per_sm"] * ghz / 1e3   # T/s
+        self.fp8 = 2 * self.sms * rates["tcgen05_f8f6f4_macs_per_clock_per_sm"] * ghz / 1e3
+
+    def fields(self, ms, int_ops=0, alu_ops=0, nbytes=0):
+        """Effective rates of `ms` of work and their fractions of the peaks."""
+        s = ms / 1e3
+        out = {}
+        if int_ops:
+            out["eff_TOPS"] = round(int_ops / s / 1e12, 1)
+            out["frac_of_fp8_tensor"] = round(int_ops / s / 1e12 / self.fp8, 4)
+        if alu_ops:
+            out["epilogue_T_lane_ops"] = round(alu_ops / s / 1e12, 2)
+            out["frac_of_fp32"] = round(alu_ops / s / 1e12 / self.fp32, 4)
+        if nbytes:
+            out["HBM_GBps"] = round(nbytes / s / 1e9, 1)
+            out["frac_of_hbm"] = round(nbytes / s / 1e9 / self.hbm_gbs, 4)
+        return out
+
+
+def chain_work(projs, M, xbits=4):
+    """Algorithmic work of one pass of quantize + GEMM over `projs` at M tokens:
+    2MNK integer ops, 2MN(K/32) epilogue lane ops, and the scope table's bytes
+    (bf16 in, codes + scales out, Q4_0 weights, activation codes, fp32 output)."""
+    ints = alu = nbytes = 0
+    for p in projs:
+        N, K = p.N, p.K
+        nb = K // 32
+        ints += 2 * M * N * K
+        alu += 2 * M * N * nb
+        code = 0.5 if xbits == 4 else 1.0
+        nbytes += (M * K * 2 + M * K * code + M * nb * 4                      # quantizer
+                   + N * K * 0.5 + N * nb * 2 + M * K * code + M * nb * 4 + M * N * 4)   # GEMM
+    return int(ints), int(alu), int(nbytes)
+
+
+def suite_tiny(torch, h32, dev, stream, steps, warmup, pk):
+    """The tiny configuration (64 tokens, K = N = 256, fp32 activations with 1% of
+    channels x20): quantize + GEMM on the 4-bit and the exact 8-bit routes."""
+    p = wl.TINY.chain[0]
+    x = torch.from_numpy(p.activations(64, 0, wl.CFG_TINY, bf16=False)).to(dev)
+    wq, wd = h32.h32_rotate_quantize_weights_q4_0(torch.from_numpy(p.weights(0, wl.CFG_TINY)).to(dev))
+    wp, wsc = h32.h32_prepack_weights_q4_0_tc(wq, wd)
+    y = torch.empty((64, p.N), device=dev)
+    out = []
+    for bits in (4, 8):
+        q = h32.h32_quantize_act_q4_tc if bits == 4 else h32.h32_quantize_act_q8_tc
+        g = h32.q4_0_x_q4_gemm_tc if bits == 4 else h32.q4_0_x_q8_gemm_tc
+
+        def step():
+            xw, xdt = q(x, stream=stream)
+            g(wp, wsc, xw, xdt, M=64, y=y, stream=stream)
+        ms = _events_time(torch, step, steps, warmup, stream)
+        ints, alu, nbytes = chain_work([p], 64, bits)
+        nbytes += 64 * p.K * 2   # fp32 activations: twice the bf16 bytes counted
+        out.append({"suite": f"tiny_64x256x256_q{bits}", "value": round(64 / (ms / 1e3), 1),
+                    "unit": UNIT, "ms_per_step": round(ms, 5),
+                    **pk.fields(ms, ints, alu, nbytes),
+                    "note": "two launches of a few microseconds each: launch-bound"})
+    return out
+
+
+def suite_chain_routes(torch, h32, dev, stream, steps, warmup, pk):
     """The pp512 chain on the exact 8-bit route (tensor-core form and Q4_0-direct),
     on the unrotated 4-bit route (tensor-core form) and on the rotated 4-bit route
     with the Q4_0-direct GEMM."""
@@ -797,8 +869,9 @@ def suite_chain_routes(torch, h32, dev, stream, steps, warmup):
                     xq, xd = h32.h32_quantize_act_q4(x, rotate=rot, stream=stream)
                     h32.q4_0_x_q4_gemm(wq, wd, xq, xd, y=y, stream=stream)
         ms = _events_time(torch, step, steps, warmup, stream)
+        ints, alu, nbytes = chain_work(CHAIN, M_TOKENS, 8 if route.startswith("q8") else 4)
         out.append({"suite": f"pp512_chain_{route}", "value": round(M_TOKENS / (ms / 1e3), 1),
-                    "unit": UNIT, "ms_per_step": round(ms, 4)})
+                    "unit": UNIT, "ms_per_step": round(ms, 4), **pk.fields(ms, ints, alu, nbytes)})
         del bufs
     return out
 
@@ -872,7 +945,7 @@ def suite_fused_producer(torch, h32, dev, stream, steps, warmup):
              "value": out["fused"]}]
 
 
-def suite_moe(torch, h32, dev, stream, steps, warmup):
+def suite_moe(torch, h32, dev, stream, steps, warmup, pk):
     """One 1024-token MoE micro-batch: quantize, expert gate/up GEMM, quantize the
     down input, expert down GEMM (routing, SwiGLU and combine are outside the path)."""
     cfg = wl.MOE
@@ -939,10 +1012,17 @@ def suite_moe(torch, h32, dev, stream, steps, warmup):
           "down_ms": _events_time(torch, lambda: h32.q4_0_x_q4_gemm_tc_experts(
               wp_dn, ws_dn, xw_dn, xt_dn, offs, N_dn, R=R, y=y_dn, stream=stream), steps, warmup,
               stream)}
+    E = cfg.E
+    moe_alu = 2 * R * (N_gu * (cfg.hidden // 32) + N_dn * (cfg.ffn // 32))
+    moe_bytes = int(E * (N_gu * cfg.hidden + N_dn * cfg.ffn) * 0.5625        # Q4_0 experts
+                    + cfg.T * cfg.hidden * 2 + R * cfg.ffn * 2                # bf16 inputs
+                    + 2 * R * (cfg.hidden + cfg.ffn) * 0.625                  # codes + scales, out and in
+                    + R * (N_gu + N_dn) * 4)                                  # fp32 outputs
     out.append({"suite": "moe_1024_tokens_top8_128_experts",
                 "value": round(cfg.T / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
                 "operand_form": "tc", "gemm_ms": {k: round(v, 4) for k, v in tt.items()},
-                "gemm_eff_TOPS": round(ops / ((tt["gate_up_ms"] + tt["down_ms"]) / 1e3) / 1e12, 1)})
+                "gemm_eff_TOPS": round(ops / ((tt["gate_up_ms"] + tt["down_ms"]) / 1e3) / 1e12, 1),
+                **pk.fields(ms, ops, moe_alu, moe_bytes)})
 
     # the whole expert layer on the GPU: the router (top 8 of the logits, their
     # weights, the grouped order), the tc-form expert GEMMs on that order and the
@@ -1001,7 +1081,7 @@ def suite_moe(torch, h32, dev, stream, steps, warmup):
     return out
 
 
-def suite_long(torch, h32, dev, stream, steps, warmup):
+def suite_long(torch, h32, dev, stream, steps, warmup, pk):
     """The chain on long prompts, in 1024-token micro-batches."""
     out = []
     projs = [wl.LONG_ATTN, wl.LONG_GATE_UP, wl.LONG_DOWN]
@@ -1025,8 +1105,13 @@ def suite_long(torch, h32, dev, stream, steps, warmup):
                     h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=m, y=y[:m], stream=stream)
         ms = _events_time(torch, step, max(1, steps // max(1, M // 1024)), max(1, warmup // 4),
                           stream)
+        ints, alu, nbytes = 0, 0, 0
+        for s0 in range(0, M, mb):
+            i_, a_, b_ = chain_work(projs, min(mb, M - s0))
+            ints, alu, nbytes = ints + i_, alu + a_, nbytes + b_
         out.append({"suite": f"long_prompt_{M}_tokens_1024_microbatches",
-                    "value": round(M / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 3)})
+                    "value": round(M / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
+                    **pk.fields(ms, ints, alu, nbytes)})
         del xs, ys
     return out
 
@@ -1070,19 +1155,23 @@ def run_suite(args, only_moe=False):
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(dev)
     peaks, _ = load_peaks()
+    pk = Peaks(torch, dev)
     steps, warmup = args.steps, args.warmup
-    lines = []
+    lines = [{"suite": "peaks", "fp32_T_lane_ops": round(pk.fp32, 2), "fp8_tensor_TOPS": round(pk.fp8, 1),
+              "hbm_GBps": pk.hbm_gbs, "sms": pk.sms, "hbm_source": pk.hbm_source,
+              "rates_source": pk.rate_source}]
     if only_moe:
-        lines += suite_moe(torch, h32, dev, stream, steps, warmup)
+        lines += suite_moe(torch, h32, dev, stream, steps, warmup, pk)
         if h32.h32_device_status(stream) != 0:
             raise RuntimeError("device status not OK after the MoE lines")
         return lines
+    lines += suite_tiny(torch, h32, dev, stream, steps, warmup, pk)
     lines += suite_quant_stream(torch, h32, dev, stream, steps, warmup, peaks)
-    lines += suite_chain_routes(torch, h32, dev, stream, steps, warmup)
+    lines += suite_chain_routes(torch, h32, dev, stream, steps, warmup, pk)
     lines += suite_rotations(torch, h32, dev, stream, steps, warmup)
     lines += suite_fused_producer(torch, h32, dev, stream, steps, warmup)
-    lines += suite_moe(torch, h32, dev, stream, steps, warmup)
-    lines += suite_long(torch, h32, dev, stream, steps, warmup)
+    lines += suite_moe(torch, h32, dev, stream, steps, warmup, pk)
+    lines += suite_long(torch, h32, dev, stream, steps, warmup, pk)
     if h32.h32_device_status(stream) != 0:
         raise RuntimeError("device status not OK after the suite")
     return lines

@@ -10,6 +10,9 @@
 //   lds       ld.shared.v4 with one address for the whole warp (a broadcast),
 //             16 warps: clocks per instruction per SM
 //   mbarrier  arrive on one warp -> observed by another: clocks per hop
+//   quantizer_launch_floor  an empty kernel and a copy with the activation
+//             quantizer's access pattern on its grid at the pp512 sizes
+//             (512 x 5120 and 512 x 17408 bf16), L2 flushed before each launch
 // Every wait is bounded; nothing here depends on another kernel or rank.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -260,6 +263,29 @@ __global__ void __launch_bounds__(512, 1) k_sm(int iters, long long *cyc, uint32
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tm) : "memory");
 }
 
+// ---------------------------------------- launch floor of the pp512 quantizer sizes
+__global__ void k_empty() {}
+
+// the activation quantizer's access pattern without its arithmetic: a warp takes
+// 4 rows x 8 blocks of 32 bf16 values, a thread loads its block (64 bytes) and
+// stores 32 code bytes and one scale (block-major)
+__global__ void __launch_bounds__(256) k_copy(const uint16_t *x, int M, int K, uint8_t *xw,
+                                              float *xdt, int ldxd) {
+    const int nb = K / 32, tiles_b = (nb + 7) / 8, ntiles = ((M + 3) / 4) * tiles_b;
+    const int lane = threadIdx.x & 31, nwarps = gridDim.x * (blockDim.x >> 5);
+    for (int wt = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); wt < ntiles; wt += nwarps) {
+        const int tr = wt / tiles_b, tb = wt - tr * tiles_b;
+        const int row = tr * 4 + (lane >> 3), b = tb * 8 + (lane & 7);
+        if (row >= M || b >= nb) continue;
+        const uint4 *p = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(row) * K + 32 * b);
+        const uint4 a = __ldg(p), c = __ldg(p + 1), d = __ldg(p + 2), e = __ldg(p + 3);
+        uint4 *o = reinterpret_cast<uint4 *>(xw + static_cast<int64_t>(row) * K + 32 * b);
+        o[0] = make_uint4(a.x ^ c.x, a.y ^ c.y, a.z ^ c.z, a.w ^ c.w);
+        o[1] = make_uint4(d.x ^ e.x, d.y ^ e.y, d.z ^ e.z, d.w ^ e.w);
+        xdt[static_cast<int64_t>(b) * ldxd + row] = __uint_as_float(a.x);
+    }
+}
+
 static double mean_cycles(const long long *d, int n) {
     long long h[2048];
     CK(cudaMemcpy(h, d, n * sizeof(long long), cudaMemcpyDeviceToHost));
@@ -357,6 +383,58 @@ int main() {
                "\"clocks_per_instruction_per_sm\": %.2f}\n", l / 128.0);
         const double b = run_sm<4, 128>(sms, 64, 20000, cyc, sink) / 20000.0;
         printf("{\"probe\": \"mbarrier\", \"clocks_per_hop\": %.0f}\n", b / 2.0);
+    }
+    // the quantizer's launch floor at the pp512 sizes: median of 25 launches, each
+    // after a 256 MB write that flushes L2, on the grid the quantizer uses
+    {
+        uint8_t *flush;
+        CK(cudaMalloc(&flush, 256u << 20));
+        cudaEvent_t e0, e1;
+        CK(cudaEventCreate(&e0));
+        CK(cudaEventCreate(&e1));
+        const int M = 512;
+        const int Ks[2] = {5120, 17408};
+        for (int ki = 0; ki < 2; ++ki) {
+            const int K = Ks[ki], nb = K / 32;
+            uint16_t *x;
+            uint8_t *xw;
+            float *xdt;
+            CK(cudaMalloc(&x, static_cast<size_t>(M) * K * 2));
+            CK(cudaMemset(x, 0x3c, static_cast<size_t>(M) * K * 2));
+            CK(cudaMalloc(&xw, static_cast<size_t>(M) * K));
+            CK(cudaMalloc(&xdt, static_cast<size_t>(nb) * M * 4));
+            const int want = (M * nb + 255) / 256, grid = want < sms * 8 ? want : sms * 8;
+            double med[2];
+            for (int mode = 0; mode < 2; ++mode) {
+                float t[25];
+                for (int r = 0; r < 27; ++r) {
+                    CK(cudaMemsetAsync(flush, r, 256u << 20));
+                    CK(cudaEventRecord(e0));
+                    if (mode == 0) k_empty<<<grid, 256>>>();
+                    else k_copy<<<grid, 256>>>(x, M, K, xw, xdt, M);
+                    CK(cudaGetLastError());
+                    CK(cudaEventRecord(e1));
+                    CK(cudaEventSynchronize(e1));
+                    float ms;
+                    CK(cudaEventElapsedTime(&ms, e0, e1));
+                    if (r >= 2) t[r - 2] = ms;
+                }
+                for (int i = 1; i < 25; ++i)   // insertion sort of 25 values
+                    for (int j = i; j > 0 && t[j] < t[j - 1]; --j) {
+                        const float tmp = t[j];
+                        t[j] = t[j - 1];
+                        t[j - 1] = tmp;
+                    }
+                med[mode] = t[12] * 1e3;
+            }
+            printf("{\"probe\": \"quantizer_launch_floor\", \"shape\": \"512x%d bf16\", \"grid\": %d, "
+                   "\"empty_kernel_us\": %.2f, \"same_pattern_copy_us\": %.2f}\n",
+                   K, grid, med[0], med[1]);
+            CK(cudaFree(x));
+            CK(cudaFree(xw));
+            CK(cudaFree(xdt));
+        }
+        CK(cudaFree(flush));
     }
     int err = 0;
     CK(cudaMemcpyFromSymbol(&err, g_err, sizeof(int)));

@@ -79,9 +79,11 @@ constexpr int kMaxExperts = 1024;
 // XB = 4: one activation byte per code.  XB = 8: two bytes per code, the e4m3
 // bytes of 16 h and of l where the 8-bit code is 16 h + l (0 <= l <= 15), so a
 // 128-element stage carries two activation tiles.
-template <int EPQ, int XB>
+// QN: the instance that also quantizes its output for the next projection; it
+// gives up a stage for a 4 KB staging tile per epilogue warp
+template <int EPQ, int XB, bool QN = false>
 struct TcCfg {
-    static constexpr int kStages = XB == 8 ? 4 : 5;
+    static constexpr int kStages = (XB == 8 || QN) ? 4 : 5;
     static constexpr int kBTile = XB == 8 ? 2 * kTileBytes : kTileBytes;   // activations per stage
     static constexpr int kEpiWarps = 4 * EPQ;
     // With 16 epilogue warps the producers form a warpgroup of their own (TMA,
@@ -103,8 +105,10 @@ struct TcCfg {
     static constexpr int kOffBar = kOffSB + kStages * kScaleBytes;
     static constexpr int kOffMisc = kOffBar + 32 * 8;
     static constexpr int kOffGrp = kOffMisc + 16 * 4;            // row offsets, tile prefix
-    static constexpr int kBytes = kOffGrp + 2 * (kMaxExperts + 1) * 4;
+    static constexpr int kOffQ = (kOffGrp + 2 * (kMaxExperts + 1) * 4 + 127) & ~127;
+    static constexpr int kBytes = kOffQ + (QN ? kEpiWarps * 4096 : 0);
     static constexpr int kSmem = kBytes + 1024;
+    static_assert(kSmem <= 232448, "shared memory above the per-block limit");
 };
 
 enum {
@@ -130,31 +134,6 @@ struct TcArgs {
     int32_t tail_first, tail_k;
     uint64_t wait_limit;
 };
-
-// One 32-block of the next projection's input, held one value per lane (the
-// warp's 32 TMEM lanes are 32 consecutive output features of one token):
-// rotate it across the lanes (strides 1 .. 16 by shuffles, then the fp32
-// 1/sqrt(32)), quantize it to a 4-bit code like the activation quantizer, and
-// return the lane's tc-form byte; *d gets the block's scale.  Warp-collective.
-__device__ __forceinline__ uint32_t quant_lane_block(float v, int lane, bool rot, float *d) {
-    if (rot) {
-#pragma unroll
-        for (int h = 1; h < 32; h <<= 1) {
-            const float p = __shfl_xor_sync(0xFFFFFFFFu, v, h);
-            v = (lane & h) ? __fsub_rn(p, v) : __fadd_rn(v, p);
-        }
-        v = __fmul_rn(v, kInvSqrt32);
-    }
-    float amax = fabsf(v);
-#pragma unroll
-    for (int h = 1; h < 32; h <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, h));
-    const float dd = __fdiv_rn(amax, 7.0f);
-    const float id = (dd != 0.0f) ? __frcp_rn(dd) : 0.0f;
-    const float t = (!(amax < INFINITY) || isinf(id)) ? degenerate_code(v, dd, -8.0f, 7.0f)
-                                                       : __fmul_rn(v, id);
-    *d = dd;
-    return tc_bytes(__float_as_uint(__fadd_rn(t, kRoundMagic)) & 0xFFu) & 0xFFu;
-}
 
 __device__ __forceinline__ void record(uint32_t bits) { atomicOr(&g_tc_status, bits); }
 
@@ -264,9 +243,9 @@ __device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a, const int *s_o
 template <int EPQ, int XB, bool kQN, bool kTail>
 __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const int *s_off,
                                                const int *s_tpre, uint64_t *bars, const float *s_sa,
-                                               const float *s_sb, uint32_t tmem, int warp, int lane,
-                                               volatile int *abort_flag) {
-    using C = TcCfg<EPQ, XB>;
+                                               const float *s_sb, float *s_q, uint32_t tmem,
+                                               int warp, int lane, volatile int *abort_flag) {
+    using C = TcCfg<EPQ, XB, kQN>;
     const int ew = warp - C::kProdWarps;
     const int quad = warp & 3;                 // TMEM lanes 32 quad .. 32 quad + 31
     const int part = ew >> 2;                  // share of the columns
@@ -345,29 +324,51 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
                 }
             }
         }
-        // the output quantized for the next projection: this warp's 32 lanes are
-        // one 32-block of it for every token column (N % 32 == 0, so a block is
-        // all inside or all outside the N rows)
-        if (kQN && ti.n0 + quad * 32 < a.N) {
-            const int nb0 = (ti.n0 + quad * 32) >> 5;
+        // the output quantized for the next projection.  The warp's 32 lanes are 32
+        // consecutive output features, one 32-block of the next projection's input
+        // for every token column (N % 32 == 0: a block is all inside or all outside
+        // the N rows).  The warp turns its 32 rows x 32 columns around through a
+        // 4 KB staging tile (16-byte chunks of a column XOR-swizzled by the column,
+        // so writes and reads are free of bank conflicts); then lane t holds token
+        // column t's whole block and rotates and quantizes it in registers, the
+        // step the activation quantizer takes, with the same arithmetic.
+        if constexpr (kQN) {
+            float *stg = s_q + (warp - C::kProdWarps) * 1024;
 #pragma unroll
             for (int c = 0; c < C::kMaxChunks; ++c) {
                 if (c < nch) {
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
-                        const int col = c0 + c * 16 + q;
+                        const int t = c * 16 + q;
                         const uint64_t pr = acc[8 * c + (q >> 1)];
-                        const float v = __uint_as_float(static_cast<uint32_t>(pr >> (32 * (q & 1))));
-                        float d;
-                        const uint32_t byte = quant_lane_block(v, lane, a.qn_rot != 0, &d);
-                        if (col >= ti.clo && col < ti.chi) {
-                            const int64_t g = ti.g0 + col;
-                            a.qn[g * a.N + n] = static_cast<uint8_t>(byte);
-                            if (lane == 0) a.qnd[nb0 * a.ldqnd + g] = d;
-                        }
+                        stg[t * 32 + ((((lane >> 2) ^ (t & 7))) << 2) + (lane & 3)] =
+                            __uint_as_float(static_cast<uint32_t>(pr >> (32 * (q & 1))));
                     }
                 }
             }
+            __syncwarp();
+            const int col = c0 + lane;
+            if (lane < 16 * nch && col >= ti.clo && col < ti.chi && ti.n0 + quad * 32 < a.N) {
+                float v[32];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float4 f = *reinterpret_cast<const float4 *>(
+                        stg + lane * 32 + ((k ^ (lane & 7)) << 2));
+                    v[4 * k] = f.x;
+                    v[4 * k + 1] = f.y;
+                    v[4 * k + 2] = f.z;
+                    v[4 * k + 3] = f.w;
+                }
+                if (a.qn_rot) rotate32(v);
+                uint32_t w[8];
+                const float d = quant_block_tc4(v, w);
+                const int64_t g = ti.g0 + col;
+                uint4 *dst = reinterpret_cast<uint4 *>(a.qn + g * a.N + ti.n0 + quad * 32);
+                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                a.qnd[((ti.n0 + quad * 32) >> 5) * a.ldqnd + g] = d;
+            }
+            __syncwarp();   // the staging tile is free for the next tile
         }
     }
     return true;
@@ -377,11 +378,11 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
 // quantized for the next projection.  kTail: the last partial wave's tiles are
 // cut into pieces (TcArgs::tail_first, tail_k).
 template <int EPQ, int XB, int kEpi, bool kTail = false>
-__global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_sa,
                    const __grid_constant__ CUtensorMap map_sb, const TcArgs a) {
-    using C = TcCfg<EPQ, XB>;
+    using C = TcCfg<EPQ, XB, kEpi == 2>;
     constexpr int kStages = C::kStages;
     constexpr bool kSums = kEpi == 1;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -394,6 +395,7 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
     volatile int *misc = reinterpret_cast<volatile int *>(smem + C::kOffMisc);
     int *s_off = reinterpret_cast<int *>(smem + C::kOffGrp);
     int *s_tpre = s_off + kMaxExperts + 1;
+    float *s_q = reinterpret_cast<float *>(smem + C::kOffQ);   // kEpi == 2: staging tiles
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nst = a.nb / 4;
@@ -583,7 +585,7 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB>::kThreads, 1)
         // ------------------------------------------------------- epilogue
         if constexpr (C::kRegSplit) reg_alloc<C::kEpiRegs>();
         if (!epilogue_tiles<EPQ, XB, kEpi == 2, kTail>(a, total, s_off, s_tpre, bars, s_sa, s_sb,
-                                                       tmem, warp, lane, abort_flag))
+                                                       s_q, tmem, warp, lane, abort_flag))
             set_abort(misc);
     } else {
         // ------------------------------------ epilogue with block sums
@@ -840,7 +842,7 @@ TcPlan plan_tc(int64_t M, int64_t N, int sms, bool allow_cut) {
 
 template <int EPQ, int XB, int kEpi, bool kTail = false>
 h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStream_t s) {
-    using C = TcCfg<EPQ, XB>;
+    using C = TcCfg<EPQ, XB, kEpi == 2>;
     constexpr int kSmem = C::kSmem;
     const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi, kTail>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -918,7 +920,7 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
             return H32_ERR_INVALID_ARG;
     } else {
         if (((N + kBM - 1) / kBM) * ((M + 15) / 16) * 8 > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
-        plan = plan_tc(M, N, sms, !qn && !block_sums);
+        plan = plan_tc(M, N, sms, !block_sums);
     }
     const int bn = plan.bn;
     const int64_t grid = plan.grid;
@@ -954,7 +956,9 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
         return plan.tail_k > 1 ? launch_tc<H32_TC_EPI_PER_QUAD, 8, 0, true>(maps, a, g, s)
                                : launch_tc<H32_TC_EPI_PER_QUAD, 8, 0>(maps, a, g, s);
     }
-    if (qn) return launch_tc<H32_TC_EPI_PER_QUAD, 4, 2>(maps, a, g, s);
+    if (qn)
+        return plan.tail_k > 1 ? launch_tc<H32_TC_EPI_PER_QUAD, 4, 2, true>(maps, a, g, s)
+                               : launch_tc<H32_TC_EPI_PER_QUAD, 4, 2>(maps, a, g, s);
     if (block_sums) return launch_tc<H32_TC_EPI_PER_QUAD, 4, 1>(maps, a, g, s);
     // the tile's 16-column chunks in even shares: 12 epilogue warps (3 per lane
     // quarter) when 16 would leave one warp with twice the others' chunks

@@ -66,27 +66,6 @@ __device__ __forceinline__ void load_block_f32(const float *__restrict__ p, floa
 // ----------------------------------------------------------------------------
 // the rotation: butterfly with strides 1, 2, 4, 8, 16, then the 1/sqrt(32) scale
 // ----------------------------------------------------------------------------
-// strides 1, 2, 4, 8, 16: the in-thread stages of every rotation size
-__device__ __forceinline__ void butterfly32(float (&v)[32]) {
-#pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if ((i & h) == 0) {
-                const float a = v[i], c = v[i + h];
-                v[i] = __fadd_rn(a, c);
-                v[i + h] = __fsub_rn(a, c);
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void rotate32(float (&v)[32]) {
-    butterfly32(v);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], kInvSqrt32);
-}
-
 // The kRot-point rotation (0 = none, 32, 64, 128) of the thread's 32-block,
 // which is 32-block `pos` (0 .. kRot/32 - 1) of its kRot-block.  The other
 // 32-blocks of the kRot-block are held by the lanes that differ from this one
@@ -318,38 +297,31 @@ __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restric
             }
         }
         rotate_block<kRot>(v, b, mask);
-        constexpr float kQmax = (kBits == 4) ? 7.0f : 127.0f;
-        constexpr float kQmin = (kBits == 4) ? -8.0f : -127.0f;
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        const float d = __fdiv_rn(amax, kQmax);
-        const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
-        uint32_t bits[32];
-        if (!(amax < INFINITY) || isinf(id)) {   // degenerate block: the clamped y / d
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                bits[i] = __float_as_uint(__fadd_rn(degenerate_code(v[i], d, kQmin, kQmax),
-                                                    kRoundMagic));
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                bits[i] = __float_as_uint(__fadd_rn(__fmul_rn(v[i], id), kRoundMagic));
-        }
+        float d;
         if constexpr (kBits == 4) {
-            // the codes as integer-valued floats (exact: bits holds code + 1.5 * 2^23),
-            // converted to e4m3 by the hardware (exact for |code| <= 8)
-            float c[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) c[i] = __fsub_rn(__uint_as_float(bits[i]), kRoundMagic);
             uint32_t w[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                w[k] = e4m3x4_of_ints(c[4 * k], c[4 * k + 1], c[4 * k + 2], c[4 * k + 3]);
+            d = quant_block_tc4(v, w);
             uint4 *dst = reinterpret_cast<uint4 *>(xw + int64_t(row) * K + 32 * b);
             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
         } else {
+            constexpr float kQmax = 127.0f, kQmin = -127.0f;
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            d = __fdiv_rn(amax, kQmax);
+            const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+            uint32_t bits[32];
+            if (!(amax < INFINITY) || isinf(id)) {   // degenerate block: the clamped y / d
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    bits[i] = __float_as_uint(__fadd_rn(degenerate_code(v[i], d, kQmin, kQmax),
+                                                        kRoundMagic));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    bits[i] = __float_as_uint(__fadd_rn(__fmul_rn(v[i], id), kRoundMagic));
+            }
             // 64 bytes per block: the 32 bytes of 16 h, then the 32 bytes of l
             // integer byte arithmetic here: measured faster than converting floats
             uint32_t wh[8], wl[8];

@@ -26,6 +26,28 @@ __device__ __forceinline__ float degenerate_code(float y, float d, float qmin, f
     return fminf(fmaxf(t, qmin), qmax);
 }
 
+// strides 1, 2, 4, 8, 16: the in-thread stages of every rotation size
+__device__ __forceinline__ void butterfly32(float (&v)[32]) {
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if ((i & h) == 0) {
+                const float a = v[i], c = v[i + h];
+                v[i] = __fadd_rn(a, c);
+                v[i + h] = __fsub_rn(a, c);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void rotate32(float (&v)[32]) {
+    butterfly32(v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], kInvSqrt32);
+}
+
+
 // tensor-core form: one byte per code, the e4m3 encoding of the integer code
 __device__ __forceinline__ uint32_t byte_sign_mask(uint32_t x) {
     uint32_t r;
@@ -86,6 +108,38 @@ __device__ __forceinline__ uint32_t e4m3x4_of_ints(float c0, float c1, float c2,
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(c1), "f"(c0));
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(c3), "f"(c2));
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// One 32-block y of activations to 4-bit codes in tensor-core form, the step
+// every 4-bit tc-form producer shares (the activation quantizer and the GEMM
+// that quantizes its own output): d = amax(|y|) / 7 (IEEE divide), codes
+// round-half-even(y * fl(1/d)) (the clamped y / d in a degenerate block), each
+// code as the e4m3 byte of the integer; w[k] holds codes 4k .. 4k + 3 from its
+// low byte up.  Returns d.
+__device__ __forceinline__ float quant_block_tc4(const float (&v)[32], uint32_t (&w)[8]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const float d = __fdiv_rn(amax, 7.0f);
+    const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+    uint32_t bits[32];
+    if (!(amax < INFINITY) || isinf(id)) {   // degenerate block: the clamped y / d
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            bits[i] = __float_as_uint(__fadd_rn(degenerate_code(v[i], d, -8.0f, 7.0f), kRoundMagic));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            bits[i] = __float_as_uint(__fadd_rn(__fmul_rn(v[i], id), kRoundMagic));
+    }
+    // the codes as integer-valued floats (exact: bits holds code + 1.5 * 2^23),
+    // converted to e4m3 by the hardware (exact for |code| <= 8)
+    float c[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) c[i] = __fsub_rn(__uint_as_float(bits[i]), kRoundMagic);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = e4m3x4_of_ints(c[4 * k], c[4 * k + 1], c[4 * k + 2], c[4 * k + 3]);
+    return d;
 }
 
 }  // namespace h32

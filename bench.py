@@ -42,18 +42,23 @@ WORKLOAD = ("pp512 GEMM chain, rotated 4-bit route: 512 tokens through attention
             "(quantize activations + W4A4 GEMM per projection)")
 # operand forms of the chain: "tc" = weights repacked once into tensor-core bytes,
 # activations quantized straight into that form; "q4_0" = Q4_0 weights and
-# nibble-packed activations consumed directly
-FORMS = ("tc", "q4_0")
+# nibble-packed activations consumed directly; "widen" = the Q4_0 weight planes
+# widened into tensor-core bytes in shared memory by the GEMM, activations in
+# tensor-core form
+FORMS = ("tc", "q4_0", "widen")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 _CSRC = os.path.join(ROOT, "hadamard_rotated_bit_gb300", "csrc")
 PROFILE_SUMMARY = {"tc": os.path.join(ROOT, "profiles", "gemm_tc_w4a4_pp512_ffn_gate_up.md"),
-                   "q4_0": os.path.join(ROOT, "profiles", "gemm_w4a4_pp512_ffn_gate_up.md")}
+                   "q4_0": os.path.join(ROOT, "profiles", "gemm_w4a4_pp512_ffn_gate_up.md"),
+                   "widen": os.path.join(ROOT, "profiles",
+                                         "gemm_tc_widen_w4a4_pp512_ffn_gate_up.md")}
 # the sources a GEMM kernel is compiled from (the profile's traffic is only
 # reported while they are unchanged)
 GEMM_SOURCES = {"tc": [os.path.join(_CSRC, f) for f in ("h32_gemm_tc.cu", "h32_common.cuh",
                                                         "h32_epilogue.cuh", "h32_tcform.cuh")],
                 "q4_0": [os.path.join(_CSRC, f) for f in ("h32_gemm.cu", "h32_common.cuh",
                                                           "h32_epilogue.cuh")]}
+GEMM_SOURCES["widen"] = GEMM_SOURCES["tc"]
 PEAKS_SUMMARY = os.path.join(ROOT, "profiles", "peaks_gb300.md")
 PEAKS_SOURCE = os.path.join(ROOT, "hadamard_rotated_bit_gb300", "peaks", "h32_peaks.cu")
 FP32_LANES_PER_SM = 128   # fp32 lanes per SM per clock (the unit count)
@@ -232,7 +237,7 @@ class Chain:
                 d = {"wq": wq if s == 0 else wq.clone(), "wd": wd if s == 0 else wd.clone(),
                      "x": x if s == 0 else x.clone(),
                      "y": torch.empty((M_TOKENS, wq.shape[0]), dtype=torch.float32, device=device)}
-                if form == "tc":
+                if form in ("tc", "widen"):
                     d["xq"] = torch.empty((M_TOKENS, K), dtype=torch.uint8, device=device)
                     d["xd"] = torch.zeros((K // 32, M_TOKENS), dtype=torch.float32, device=device)
                 else:
@@ -249,10 +254,16 @@ class Chain:
         p = self.sets[s % len(self.sets)][k // 2]
         tc = self.form == "tc"
         if k % 2 == 0:
+            if self.form == "widen":
+                return lambda: h.h32_quantize_act_q4_tc_e5m2(p["x"], xw=p["xq"], xdt=p["xd"],
+                                                             stream=stream)
             if tc:
                 return lambda: h.h32_quantize_act_q4_tc(p["x"], xw=p["xq"], xdt=p["xd"],
                                                         stream=stream)
             return lambda: h.h32_quantize_act_q4(p["x"], xq=p["xq"], xd=p["xd"], stream=stream)
+        if self.form == "widen":
+            return lambda: h.q4_0_x_q4_gemm_tc_widen(p["wq"], p["wd"], p["xq"], p["xd"],
+                                                     M=M_TOKENS, y=p["y"], stream=stream)
         if tc:
             return lambda: h.q4_0_x_q4_gemm_tc(p["wq"], p["wd"], p["xq"], p["xd"], M=M_TOKENS,
                                                y=p["y"], stream=stream)
@@ -266,14 +277,19 @@ class Chain:
         for i, p in enumerate(self.sets[s % len(self.sets)]):
             if events is not None:
                 events[2 * i][0].record(stream)
-            if tc:
+            if self.form == "widen":
+                h.h32_quantize_act_q4_tc_e5m2(p["x"], xw=p["xq"], xdt=p["xd"], stream=stream)
+            elif tc:
                 h.h32_quantize_act_q4_tc(p["x"], xw=p["xq"], xdt=p["xd"], stream=stream)
             else:
                 h.h32_quantize_act_q4(p["x"], xq=p["xq"], xd=p["xd"], stream=stream)
             if events is not None:
                 events[2 * i][1].record(stream)
                 events[2 * i + 1][0].record(stream)
-            if tc:
+            if self.form == "widen":
+                h.q4_0_x_q4_gemm_tc_widen(p["wq"], p["wd"], p["xq"], p["xd"], M=M_TOKENS,
+                                          y=p["y"], stream=stream)
+            elif tc:
                 h.q4_0_x_q4_gemm_tc(p["wq"], p["wd"], p["xq"], p["xd"], M=M_TOKENS, y=p["y"],
                                     stream=stream)
             else:
@@ -283,10 +299,11 @@ class Chain:
 
 
 def kernel_names(form):
-    sfx = "_tc" if form == "tc" else ""
+    qs = {"tc": "_tc", "q4_0": "", "widen": "_tc_e5m2"}[form]
+    gs = {"tc": "_tc", "q4_0": "", "widen": "_tc_widen"}[form]
     names = []
     for p in CHAIN:
-        names += [f"h32_quantize_act_q4{sfx}[{p.name}]", f"q4_0_x_q4_gemm{sfx}[{p.name}]"]
+        names += [f"h32_quantize_act_q4{qs}[{p.name}]", f"q4_0_x_q4_gemm{gs}[{p.name}]"]
     return names
 
 
@@ -295,18 +312,20 @@ def algorithmic(p, form="tc", M=M_TOKENS):
     bf16 in, 4-bit codes (0.5 B) and fp32 scales out for the quantizer (2.625 B an
     element); Q4_0 weights (0.5 B a code, fp16 scales), 4-bit activations and the
     fp32 output for the GEMM.  The tc form stores a code in a byte: its actual
-    bytes are the `*_traffic_bytes`."""
+    bytes are the `*_traffic_bytes` (the widening form reads the Q4_0 weights
+    themselves and tc-form activations)."""
     N, K = p.N, p.K
     nb = K // 32
-    code = 1 if form == "tc" else 0.5          # bytes per stored 4-bit code
+    code = 1 if form == "tc" else 0.5          # bytes per stored 4-bit weight code
     wscale = 4 if form == "tc" else 2          # fp32 (tc) or fp16 (Q4_0) weight scales
+    xcode = 0.5 if form == "q4_0" else 1       # bytes per stored 4-bit activation code
     return {
         "quant_bytes": int(M * K * 2 + M * K * 0.5 + M * nb * 4),
-        "quant_traffic_bytes": int(M * K * 2 + M * K * code + M * nb * 4),
+        "quant_traffic_bytes": int(M * K * 2 + M * K * xcode + M * nb * 4),
         "gemm_alu_ops": 2 * M * N * nb,                            # d_w*d_x and one fma per block
         "gemm_int_ops": 2 * M * N * K,                             # 2 MNK (multiply + add)
         "gemm_bytes": int(N * K * 0.5 + N * nb * 2 + M * K * 0.5 + M * nb * 4 + M * N * 4),
-        "gemm_traffic_bytes": int(N * K * code + N * nb * wscale + M * K * code + M * nb * 4
+        "gemm_traffic_bytes": int(N * K * code + N * nb * wscale + M * K * xcode + M * nb * 4
                                   + M * N * 4),
     }
 
@@ -680,6 +699,11 @@ def run_only_gemm(args):
 
         def gemm():
             h32.q4_0_x_q4_gemm_tc(wq, wd, xq, xd, M=M_TOKENS, y=y)
+    elif args.form == "widen":
+        xq, xd = h32.h32_quantize_act_q4_tc_e5m2(x)
+
+        def gemm():
+            h32.q4_0_x_q4_gemm_tc_widen(wq, wd, xq, xd, M=M_TOKENS, y=y)
     else:
         xq, xd = h32.h32_quantize_act_q4(x)
 
@@ -837,10 +861,11 @@ def suite_tiny(torch, h32, dev, stream, steps, warmup, pk):
 def suite_chain_routes(torch, h32, dev, stream, steps, warmup, pk):
     """The pp512 chain on the exact 8-bit route (tensor-core form and Q4_0-direct),
     on the unrotated 4-bit route (tensor-core form) and on the rotated 4-bit route
-    with the Q4_0-direct GEMM."""
+    with the Q4_0-direct GEMM and with the GEMM that widens the Q4_0 planes in
+    shared memory."""
     out = []
     for route in ("q8_rotated_tc", "q8_rotated_q4_0_direct", "q4_unrotated",
-                  "q4_rotated_q4_0_direct"):
+                  "q4_rotated_q4_0_direct", "q4_rotated_widen"):
         rot = route != "q4_unrotated"
         tc = route in ("q4_unrotated", "q8_rotated_tc")
         bufs = []
@@ -865,6 +890,9 @@ def suite_chain_routes(torch, h32, dev, stream, steps, warmup, pk):
                 elif tc:
                     xw, xdt = h32.h32_quantize_act_q4_tc(x, rotate=rot, stream=stream)
                     h32.q4_0_x_q4_gemm_tc(wq, wd, xw, xdt, M=M_TOKENS, y=y, stream=stream)
+                elif route == "q4_rotated_widen":
+                    xw, xdt = h32.h32_quantize_act_q4_tc_e5m2(x, rotate=rot, stream=stream)
+                    h32.q4_0_x_q4_gemm_tc_widen(wq, wd, xw, xdt, M=M_TOKENS, y=y, stream=stream)
                 else:
                     xq, xd = h32.h32_quantize_act_q4(x, rotate=rot, stream=stream)
                     h32.q4_0_x_q4_gemm(wq, wd, xq, xd, y=y, stream=stream)
@@ -916,7 +944,8 @@ def suite_rotations(torch, h32, dev, stream, steps, warmup):
 def suite_fused_producer(torch, h32, dev, stream, steps, warmup):
     """The attention projection (512 x 5120 x 5120) followed by the quantization of
     its output for the next projection: separately (GEMM writes y, the quantizer
-    reads it back) and fused into the GEMM's epilogue (with and without y)."""
+    reads it back) and fused into the GEMM's epilogue (with and without y), next to
+    the GEMM alone."""
     p = wl.ATTN
     wq, wd = h32.h32_rotate_quantize_weights_q4_0(torch.from_numpy(p.weights(0, wl.CFG_ATTN)).to(dev))
     wp, wsc = h32.h32_prepack_weights_q4_0_tc(wq, wd)
@@ -938,8 +967,12 @@ def suite_fused_producer(torch, h32, dev, stream, steps, warmup):
     def fused():
         h32.q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=M_TOKENS, want_y=False, xw_next=xn,
                                          xdt_next=xnd, stream=stream)
+
+    def gemm_alone():
+        h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M_TOKENS, y=y, stream=stream)
     out = {}
-    for name, fn in (("separate", separate), ("fused_with_y", fused_y), ("fused", fused)):
+    for name, fn in (("gemm_alone", gemm_alone), ("separate", separate), ("fused_with_y", fused_y),
+                     ("fused", fused)):
         out[name] = round(_events_time(torch, fn, steps, warmup, stream), 4)
     return [{"suite": "attn_gemm_then_next_quantization_pp512", "unit": "ms", "ms": out,
              "value": out["fused"]}]
@@ -1022,6 +1055,35 @@ def suite_moe(torch, h32, dev, stream, steps, warmup, pk):
                 "value": round(cfg.T / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
                 "operand_form": "tc", "gemm_ms": {k: round(v, 4) for k, v in tt.items()},
                 "gemm_eff_TOPS": round(ops / ((tt["gate_up_ms"] + tt["down_ms"]) / 1e3) / 1e12, 1),
+                "weight_bytes": int(E * (N_gu * cfg.hidden + N_dn * cfg.ffn) * 1.125),
+                **pk.fields(ms, ops, moe_alu, moe_bytes)})
+
+    # the same expert GEMMs on the experts' Q4_0 planes themselves, widened into
+    # tensor-core bytes in shared memory (half the weight bytes of the repacked form)
+    wq_gu2, wd_gu2 = wq_gu.reshape(-1, wq_gu.shape[2]), wd_gu.reshape(-1, wd_gu.shape[2])
+    wq_dn2, wd_dn2 = wq_dn.reshape(-1, wq_dn.shape[2]), wd_dn.reshape(-1, wd_dn.shape[2])
+
+    def gu_widen():
+        h32.q4_0_x_q4_gemm_tc_widen_experts(wq_gu2, wd_gu2, xw_gu, xt_gu, offs, N_gu, R=R,
+                                            y=y_gu, stream=stream)
+
+    def dn_widen():
+        h32.q4_0_x_q4_gemm_tc_widen_experts(wq_dn2, wd_dn2, xw_dn, xt_dn, offs, N_dn, R=R,
+                                            y=y_dn, stream=stream)
+
+    def step_widen():
+        h32.h32_quantize_act_q4_tc_e5m2_gather(xg, ridx, xw=xw_gu, xdt=xt_gu, stream=stream)
+        gu_widen()
+        h32.h32_quantize_act_q4_tc_e5m2(xn, xw=xw_dn, xdt=xt_dn, stream=stream)
+        dn_widen()
+    ms = _events_time(torch, step_widen, steps, warmup, stream)   # leaves xw_* in e5m2 form
+    tw = {"gate_up_ms": _events_time(torch, gu_widen, steps, warmup, stream),
+          "down_ms": _events_time(torch, dn_widen, steps, warmup, stream)}
+    out.append({"suite": "moe_1024_tokens_top8_128_experts_widen",
+                "value": round(cfg.T / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+                "operand_form": "widen", "gemm_ms": {k: round(v, 4) for k, v in tw.items()},
+                "gemm_eff_TOPS": round(ops / ((tw["gate_up_ms"] + tw["down_ms"]) / 1e3) / 1e12, 1),
+                "weight_bytes": int(E * (N_gu * cfg.hidden + N_dn * cfg.ffn) * 0.5625),
                 **pk.fields(ms, ops, moe_alu, moe_bytes)})
 
     # the whole expert layer on the GPU: the router (top 8 of the logits, their

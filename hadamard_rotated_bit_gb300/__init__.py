@@ -61,6 +61,12 @@ _SIGS = {
                                             _I64, _P, _P, _I64, _INT, _P]),
     "h32_quantize_act_q8_tc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _I64, _INT, _P]),
     "q4_0_x_q8_gemm_tc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P]),
+    "h32_quantize_act_q4_tc_e5m2": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _I64, _INT, _P]),
+    "h32_quantize_act_q4_tc_e5m2_gather": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _P,
+                                                  _I64, _INT, _P]),
+    "q4_0_x_q4_gemm_tc_widen": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P]),
+    "q4_0_x_q4_gemm_tc_widen_experts": (_INT, [_P, _P, ctypes.c_int32, _P, _P, _I64, _P, _I64,
+                                               _I64, _I64, _P, _I64, _P, _P]),
     "h32_quantize_act_q4_tc_gather": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _P, _I64,
                                              _INT, _P]),
     "q4_0_x_q4_gemm_tc_experts": (_INT, [_P, _P, _I64, ctypes.c_int32, _P, _P, _I64, _P, _I64, _I64,
@@ -370,6 +376,12 @@ def h32_quantize_act_q4_tc(x, rotate=True, xw=None, xdt=None, stream=None):
     return _quantize_tc("h32_quantize_act_q4_tc", 1, x, rotate, xw, xdt, stream)
 
 
+def h32_quantize_act_q4_tc_e5m2(x, rotate=True, xw=None, xdt=None, stream=None):
+    """As h32_quantize_act_q4_tc with each code c stored as the e5m2 byte of 512 c
+    (the activations of the widening GEMMs)."""
+    return _quantize_tc("h32_quantize_act_q4_tc_e5m2", 1, x, rotate, xw, xdt, stream)
+
+
 def h32_quantize_act_q8_tc(x, rotate=True, xw=None, xdt=None, stream=None):
     """x [M][K] bf16/fp32 -> (xw8 [M][2K] uint8: per 32-block the e4m3 bytes of 16 h
     then of l, code = 16 h + l; xdt [K/32][ldxd] fp32 scales)."""
@@ -461,9 +473,84 @@ def _gemm_tc(fn, wp, wsc, xw, xdt, M, y, block_sums, stream):
     return (y, S) if S is not None else y
 
 
+def _widen_operands(wq, wd, xw, xdt, rows):
+    """Check Q4_0 weight planes and tc-form activations over `rows` rows; returns (N, K)."""
+    torch = _torch()
+    if wq.dim() != 2:
+        raise ValueError("wq must be 2-D [N][K/2]")
+    N, K = wq.shape[0], wq.shape[1] * 2
+    _need(wq, "wq", (torch.uint8,), (N, K // 2))
+    _need(wd, "wd", _fp16_bits(), (N, K // 32))
+    _need(xw, "xw", (torch.uint8,), (_ge(rows), K))
+    _need(xdt, "xdt", (torch.float32,), (_ge(K // 32), _ge(rows)))
+    return N, K
+
+
+def q4_0_x_q4_gemm_tc_widen(wq, wd, xw, xdt, M=None, y=None, block_sums=None, stream=None):
+    """The W4A4 product on the Q4_0 planes (wq [N][K/2], wd [N][K/32] fp16 bits),
+    widened in shared memory, against activations from
+    h32_quantize_act_q4_tc_e5m2; bit-identical to q4_0_x_q4_gemm_tc."""
+    torch = _torch()
+    if M is None:
+        M = xw.shape[0]
+    N, K = _widen_operands(wq, wd, xw, xdt, M)
+    dev = wq.device
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _need(y, "y", (torch.float32,), (_ge(M), _ge(N)), pitched=True)
+    ldy = _rows(y, "y")
+    S = _sums(block_sums, M, N, K // 32, dev)
+    _same_gpu(("wq", wq), ("wd", wd), ("xw", xw), ("xdt", xdt), ("y", y), ("S", S))
+    st = lib().q4_0_x_q4_gemm_tc_widen(_ptr(wq), _ptr(wd), _ptr(xw), _ptr(xdt), xdt.shape[1], M, N,
+                                       K, _ptr(y), ldy, _ptr(S), _stream(stream))
+    _check("q4_0_x_q4_gemm_tc_widen", st)
+    return (y, S) if S is not None else y
+
+
+def q4_0_x_q4_gemm_tc_widen_experts(wq, wd, xw, xdt, expert_off, N, R=None, y=None,
+                                    block_sums=None, stream=None):
+    """Expert-batched product on the experts' Q4_0 planes stacked as E * N rows
+    (wq [E*N][K/2], wd [E*N][K/32]), widened in shared memory; xw / xdt in grouped
+    order from h32_quantize_act_q4_tc_e5m2_gather, expert_off [E+1] int32 -> y [R][N]
+    fp32 in grouped order."""
+    torch = _torch()
+    if wq.dim() != 2 or N <= 0 or wq.shape[0] % N != 0:
+        raise ValueError("wq must be 2-D with E * N rows")
+    E = wq.shape[0] // N
+    if R is None:
+        R = xw.shape[0]
+    EN, K = _widen_operands(wq, wd, xw, xdt, R)
+    dev = wq.device
+    _need(expert_off, "expert_off", (torch.int32,), (_ge(E + 1),))
+    if y is None:
+        y = torch.empty((R, N), dtype=torch.float32, device=dev)
+    _need(y, "y", (torch.float32,), (_ge(R), _ge(N)), pitched=True)
+    ldy = _rows(y, "y") if R > 0 else N
+    S = _sums(block_sums, R, N, K // 32, dev)
+    _same_gpu(("wq", wq), ("wd", wd), ("xw", xw), ("xdt", xdt),
+              ("expert_off", expert_off), ("y", y), ("S", S))
+    st = lib().q4_0_x_q4_gemm_tc_widen_experts(_ptr(wq), _ptr(wd), E, _ptr(xw), _ptr(xdt),
+                                               xdt.shape[1], _ptr(expert_off), R, N, K, _ptr(y),
+                                               ldy, _ptr(S), _stream(stream))
+    _check("q4_0_x_q4_gemm_tc_widen_experts", st)
+    return (y, S) if S is not None else y
+
+
 def h32_quantize_act_q4_tc_gather(x, row_idx, rotate=True, xw=None, xdt=None, stream=None):
     """x [T][K] bf16/fp32, row_idx [R] int32 -> (xw [R][K] uint8, xdt [K/32][ldxd] fp32):
     output row r is the tc-form quantization of x[row_idx[r]]."""
+    return _quantize_tc_gather("h32_quantize_act_q4_tc_gather", x, row_idx, rotate, xw, xdt,
+                               stream)
+
+
+def h32_quantize_act_q4_tc_e5m2_gather(x, row_idx, rotate=True, xw=None, xdt=None, stream=None):
+    """The row gather of h32_quantize_act_q4_tc_e5m2 (activations of the widening
+    expert GEMM in grouped order)."""
+    return _quantize_tc_gather("h32_quantize_act_q4_tc_e5m2_gather", x, row_idx, rotate, xw, xdt,
+                               stream)
+
+
+def _quantize_tc_gather(fn, x, row_idx, rotate, xw, xdt, stream):
     torch = _torch()
     dt = _act_dtype(x)
     _need(x, "x", (x.dtype,), (_ge(0), _ge(0)), pitched=True)
@@ -481,10 +568,9 @@ def h32_quantize_act_q4_tc_gather(x, row_idx, rotate=True, xw=None, xdt=None, st
         xdt = torch.zeros((K // 32, _round4(R)), dtype=torch.float32, device=dev)
     _need(xdt, "xdt", (torch.float32,), (_ge(K // 32), _ge(R)))
     _same_gpu(("x", x), ("row_idx", row_idx), ("xw", xw), ("xdt", xdt))
-    st = lib().h32_quantize_act_q4_tc_gather(_ptr(x), dt, T, K, ldx, _ptr(row_idx), R, _ptr(xw),
-                                             _ptr(xdt), xdt.shape[1], _rot_arg(rotate),
-                                             _stream(stream))
-    _check("h32_quantize_act_q4_tc_gather", st)
+    st = getattr(lib(), fn)(_ptr(x), dt, T, K, ldx, _ptr(row_idx), R, _ptr(xw), _ptr(xdt),
+                            xdt.shape[1], _rot_arg(rotate), _stream(stream))
+    _check(fn, st)
     return xw, xdt
 
 

@@ -275,6 +275,11 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
            | ((M >> 4) << 24);  // M / 16
 }
 
+// The same with A = E4M3 and B = E5M2 (kind::f8f6f4 takes any pair of its types)
+__host__ __device__ constexpr uint32_t idesc_e4m3_e5m2_f32(uint32_t M, uint32_t N) {
+    return idesc_e4m3_f32(M, N) | (1u << 10);   // B format: E5M2
+}
+
 #endif  // __CUDACC__
 
 }  // namespace h32

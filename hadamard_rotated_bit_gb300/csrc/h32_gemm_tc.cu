@@ -29,6 +29,16 @@
 // on GB300, one block per hand-off (four buffers) is slower, as every hand-off
 // puts all epilogue warps in step.  Every wait is bounded.
 //
+// The widening instance (q4_0_x_q4_gemm_tc_widen[_experts]) takes the Q4_0
+// planes themselves, half the weight bytes of the repacked form: TMA brings
+// each stage's 128 x 64-byte tile of Q4_0 nibbles and the fp16 scales, and
+// warps 2 and 3 spread the nibbles into bytes 0x0q of the 128B-swizzled tile
+// the MMA reads (two masks and a shift per 8 codes).  Read as e4m3, 0x0q is
+// exactly q * 2^-9 for every q = 0..15; the activations of this form are the
+// e5m2 bytes of 512 times their codes (exact), so every product is the integer
+// q x, and one more MMA per block against a constant tile of -8 * 2^-9 (e4m3
+// 0x88) leaves S = sum (q - 8) x in the accumulator exactly as before.
+//
 // Schedule: one persistent CTA per SM takes tiles t = blockIdx.x, + gridDim.x,
 // ...  The host simulates that assignment once per shape to choose the token
 // width of a tile and, where it pays, a second kernel instance whose last
@@ -66,6 +76,8 @@ constexpr int kBM = 128;             // weight rows per tile (MMA M, TMEM lanes)
 constexpr int kBNMax = 128;          // tokens per tile (MMA N)
 constexpr int kMaxStages = 5;        // 128-element K stages in flight (at most)
 constexpr int kTileBytes = 16384;    // 128 rows x 128 bytes
+constexpr int kNibBytes = 8192;      // widening instance: 128 rows x 64 bytes of Q4_0 nibbles
+constexpr int kWidenWarps = 2;       // widening instance: warps 2 and 3
 constexpr int kScaleBytes = 2048;    // 4 blocks x 128 fp32
 #ifndef H32_TC_GROUP
 #define H32_TC_GROUP 2
@@ -80,10 +92,14 @@ constexpr int kMaxExperts = 1024;
 // bytes of 16 h and of l where the 8-bit code is 16 h + l (0 <= l <= 15), so a
 // 128-element stage carries two activation tiles.
 // QN: the instance that also quantizes its output for the next projection; it
-// gives up a stage for a 4 KB staging tile per epilogue warp
-template <int EPQ, int XB, bool QN = false>
+// gives up a stage for a 4 KB staging tile per epilogue warp.
+// WQ: the widening instance (Q4_0 nibbles and fp16 scales in, widened in
+// shared memory); a stage also holds the nibble tile, and a constant tile of
+// -8 * 2^-9 follows the stages.
+template <int EPQ, int XB, bool QN = false, bool WQ = false>
 struct TcCfg {
-    static constexpr int kStages = (XB == 8 || QN) ? 4 : 5;
+    static_assert(!WQ || (EPQ == 4 && XB == 4 && !QN), "widening: 4-bit route, 16 epilogue warps");
+    static constexpr int kStages = (XB == 8 || QN || WQ) ? 4 : 5;
     static constexpr int kBTile = XB == 8 ? 2 * kTileBytes : kTileBytes;   // activations per stage
     static constexpr int kEpiWarps = 4 * EPQ;
     // With 16 epilogue warps the producers form a warpgroup of their own (TMA,
@@ -100,7 +116,9 @@ struct TcCfg {
     static constexpr int kMaxChunks = (8 + EPQ - 1) / EPQ;  // 16-column chunks per warp
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kTileBytes;
-    static constexpr int kOffSA = kOffB + kStages * kBTile;
+    static constexpr int kOffN = kOffB + kStages * kBTile;                  // WQ: nibble tiles
+    static constexpr int kOffC = kOffN + (WQ ? kStages * kNibBytes : 0);    // WQ: the -8 tile
+    static constexpr int kOffSA = kOffC + (WQ ? kTileBytes : 0);
     static constexpr int kOffSB = kOffSA + kStages * kScaleBytes;
     static constexpr int kOffBar = kOffSB + kStages * kScaleBytes;
     static constexpr int kOffMisc = kOffBar + 32 * 8;
@@ -116,8 +134,10 @@ enum {
     kBarEmpty = kBarFull + kMaxStages,
     kBarSFull = kBarEmpty + kMaxStages,
     kBarSEmpty = kBarSFull + kBufs,
-    kBarDrain = kBarSEmpty + kBufs
+    kBarDrain = kBarSEmpty + kBufs,
+    kBarWide = kBarDrain + 1    // widening instance: a stage's e4m3 weight tile is written
 };
+static_assert(kBarWide + kMaxStages <= 32, "barriers above their shared-memory slots");
 enum { kMiscTmem = 0, kMiscAbort = 1, kMiscBad = 2, kMiscTotal = 3 };
 
 struct TcArgs {
@@ -235,17 +255,39 @@ __device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a, const int *s_o
     return ti;
 }
 
+// The weight scales of the thread's row for the four blocks of K stage `st`
+// held in shared-memory stage `s`: fp32 [128 rows][4] from the repacked form,
+// or (widening instance) fp16 [128 rows][8], the scales of stages st & ~1 and
+// st | 1 (the TMA box starts on a 16-byte boundary), widened exactly.
+template <bool kWQ>
+__device__ __forceinline__ void stage_dw(const float *s_sa, int s, int row, int st, float (&dw)[4]) {
+    if constexpr (kWQ) {
+        const uint2 h = *reinterpret_cast<const uint2 *>(
+            reinterpret_cast<const uint8_t *>(s_sa) + s * kScaleBytes + row * 16 + (st & 1) * 8);
+        const uint16_t hs[4] = {static_cast<uint16_t>(h.x), static_cast<uint16_t>(h.x >> 16),
+                                static_cast<uint16_t>(h.y), static_cast<uint16_t>(h.y >> 16)};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) asm("cvt.f32.f16 %0, %1;" : "=f"(dw[j]) : "h"(hs[j]));
+    } else {
+        const float4 d4 = *reinterpret_cast<const float4 *>(s_sa + s * (kScaleBytes / 4) + 4 * row);
+        dw[0] = d4.x;
+        dw[1] = d4.y;
+        dw[2] = d4.z;
+        dw[3] = d4.w;
+    }
+}
+
 // The epilogue of one warp over all of its tiles, without block sums: ring
 // positions of the shared-memory stages and TMEM buffers are carried as
 // counters and phase bits, arrivals come from one elected lane.  Returns false
 // when a wait gave up.  A warp holds its lane quarter's 32 weight rows (one a
 // thread, the 32x32b TMEM fragment) times its share of the tile's columns.
-template <int EPQ, int XB, bool kQN, bool kTail>
+template <int EPQ, int XB, bool kQN, bool kTail, bool kWQ>
 __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const int *s_off,
                                                const int *s_tpre, uint64_t *bars, const float *s_sa,
                                                const float *s_sb, float *s_q, uint32_t tmem,
                                                int warp, int lane, volatile int *abort_flag) {
-    using C = TcCfg<EPQ, XB, kQN>;
+    using C = TcCfg<EPQ, XB, kQN, kWQ>;
     const int ew = warp - C::kProdWarps;
     const int quad = warp & 3;                 // TMEM lanes 32 quad .. 32 quad + 31
     const int part = ew >> 2;                  // share of the columns
@@ -267,8 +309,8 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
         for (int i = 0; i < 8 * C::kMaxChunks; ++i) acc[i] = 0ull;
         for (int st = 0; st < nst; ++st) {
             if (!warp_wait(&bars[kBarFull + s], sph, lim, abort_flag)) return false;
-            const float4 dw4 = *reinterpret_cast<const float4 *>(s_sa + s * (kScaleBytes / 4) + 4 * row);
-            const float dws[4] = {dw4.x, dw4.y, dw4.z, dw4.w};
+            float dws[4];
+            stage_dw<kWQ>(s_sa, s, row, st, dws);
             const float *sb = s_sb + s * (kScaleBytes / 4) + c0;   // [4 blocks][bn tokens]
 #pragma unroll
             for (int j0 = 0; j0 < 4; j0 += kGroup) {
@@ -374,15 +416,66 @@ __device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const
     return true;
 }
 
+// The widening warps (2 and 3) of the widening instance over all of the CTA's
+// tiles: per K stage, once TMA has landed the stage, the 128 x 64-byte tile of
+// Q4_0 bytes becomes the 128 x 128-byte tile of code bytes 0x0q in the layout the
+// MMA reads (128B swizzle: the 16-byte chunk c of row r sits at chunk c ^ (r & 7)
+// of the row, rows in 8-row atoms of 1 KB).  Thread wt (0..63) takes the
+// (row, block) items wt, wt + 64, ...: a warp's 32 items are 8 rows x 4 blocks,
+// so eight lanes read 128 contiguous bytes and write eight distinct chunk
+// positions (free of bank conflicts).  Block j of a row: its 16 Q4_0 bytes give
+// chunk 2 j (elements 0..15, the low nibbles) and chunk 2 j + 1 (16..31).
+// Returns false when a wait gave up.
+template <bool kTail>
+__device__ __forceinline__ bool widen_tiles(const TcArgs &a, int total, const int *s_off,
+                                            const int *s_tpre, uint64_t *bars, const uint8_t *s_n,
+                                            uint8_t *s_a, int wt, volatile int *abort_flag) {
+    using C = TcCfg<4, 4, false, true>;
+    const int nst = a.nb / 4;
+    uint32_t ks = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const TcTile ti = tc_tile<kTail>(t, a, s_off, s_tpre);
+        if (kTail && ti.ncols == 0) continue;
+        for (int st = 0; st < nst; ++st, ++ks) {
+            const int s = ks % C::kStages;
+            // (measured: a suspended wait by one lane makes the MMA wait longer for
+            // the widened tile; a spinning lane is no faster than the whole warp)
+            if (!warp_wait(&bars[kBarFull + s], (ks / C::kStages) & 1, a.wait_limit, abort_flag))
+                return false;
+            const uint8_t *nib = s_n + s * kNibBytes;
+            uint8_t *wide = s_a + s * kTileBytes;
+#pragma unroll 2
+            for (int it = 0; it < 8; ++it) {
+                const int i = it * 64 + wt, r = i >> 2, j = i & 3;
+                const uint4 x = *reinterpret_cast<const uint4 *>(nib + r * 64 + j * 16);
+                uint4 lo, hi;
+                widen_q4_0_word(x.x, lo.x, hi.x);
+                widen_q4_0_word(x.y, lo.y, hi.y);
+                widen_q4_0_word(x.z, lo.z, hi.z);
+                widen_q4_0_word(x.w, lo.w, hi.w);
+                uint8_t *rp = wide + (r >> 3) * 1024 + (r & 7) * 128;
+                *reinterpret_cast<uint4 *>(rp + (((2 * j) ^ (r & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4 *>(rp + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
+            }
+            // the MMA reads the tile through the async proxy
+            fence_proxy_async_smem();
+            __syncwarp();
+            elect_arrive(&bars[kBarWide + s]);
+        }
+    }
+    return true;
+}
+
 // kEpi: 0 = y only, 1 = y and the block sums, 2 = y (optional) and the output
 // quantized for the next projection.  kTail: the last partial wave's tiles are
-// cut into pieces (TcArgs::tail_first, tail_k).
-template <int EPQ, int XB, int kEpi, bool kTail = false>
-__global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2>::kThreads, 1)
+// cut into pieces (TcArgs::tail_first, tail_k).  kWQ: the widening instance
+// (map_a over the Q4_0 nibbles, map_sa over the fp16 scales).
+template <int EPQ, int XB, int kEpi, bool kTail = false, bool kWQ = false>
+__global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2, kWQ>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_sa,
                    const __grid_constant__ CUtensorMap map_sb, const TcArgs a) {
-    using C = TcCfg<EPQ, XB, kEpi == 2>;
+    using C = TcCfg<EPQ, XB, kEpi == 2, kWQ>;
     constexpr int kStages = C::kStages;
     constexpr bool kSums = kEpi == 1;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -396,11 +489,14 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2>::kThreads, 1)
     int *s_off = reinterpret_cast<int *>(smem + C::kOffGrp);
     int *s_tpre = s_off + kMaxExperts + 1;
     float *s_q = reinterpret_cast<float *>(smem + C::kOffQ);   // kEpi == 2: staging tiles
+    uint8_t *s_n = smem + C::kOffN;                             // kWQ: Q4_0 nibble tiles
+    uint8_t *s_c = smem + C::kOffC;                             // kWQ: the constant tile
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nst = a.nb / 4;
     const uint64_t lim = a.wait_limit;
-    const uint32_t stage_tx = kTileBytes + (XB / 4) * a.bn * 128 + kScaleBytes + a.bn * 16;
+    const uint32_t stage_tx =
+        (kWQ ? kNibBytes : kTileBytes) + (XB / 4) * a.bn * 128 + kScaleBytes + a.bn * 16;
     const int E = a.E;
     const int nt = (a.N + kBM - 1) / kBM;
 
@@ -414,9 +510,19 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2>::kThreads, 1)
             mbar_init(&bars[kBarSEmpty + i], C::kEpiWarps);
         }
         mbar_init(&bars[kBarDrain], 1);
+        if constexpr (kWQ)
+            for (int i = 0; i < kStages; ++i) mbar_init(&bars[kBarWide + i], kWidenWarps);
         misc[kMiscAbort] = 0;
         misc[kMiscBad] = 0;
         fence_barrier_init();
+    }
+    if constexpr (kWQ) {
+        // the constant A operand: every weight -8 * 2^-9 = -2^-6 (e4m3 0x88), so
+        // one more MMA per block adds -8 times the activation block sum
+        uint4 *c = reinterpret_cast<uint4 *>(s_c);
+        for (int i = tid; i < kTileBytes / 16; i += C::kThreads)
+            c[i] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+        fence_proxy_async_smem();
     }
     // the previous kernel of the stream (launched ahead of this one) is done
     // before anything here touches global memory
@@ -505,14 +611,18 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2>::kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&bars[kBarFull + s], stage_tx);
-                    tma_load_2d(s_a + s * kTileBytes, &map_a, &bars[kBarFull + s], st * 128, ti.wrow);
+                    if constexpr (kWQ)
+                        tma_load_2d(s_n + s * kNibBytes, &map_a, &bars[kBarFull + s], st * 64, ti.wrow);
+                    else
+                        tma_load_2d(s_a + s * kTileBytes, &map_a, &bars[kBarFull + s], st * 128,
+                                    ti.wrow);
                     tma_load_2d(s_b + s * C::kBTile, &map_b, &bars[kBarFull + s], st * 128 * (XB / 4),
                                 ti.g0);
                     if constexpr (XB == 8)
                         tma_load_2d(s_b + s * C::kBTile + kTileBytes, &map_b, &bars[kBarFull + s],
                                     st * 256 + 128, ti.g0);
-                    tma_load_2d(s_sa + s * (kScaleBytes / 4), &map_sa, &bars[kBarFull + s], st * 4,
-                                ti.wrow);
+                    tma_load_2d(s_sa + s * (kScaleBytes / 4), &map_sa, &bars[kBarFull + s],
+                                kWQ ? (st * 4) & ~7 : st * 4, ti.wrow);
                     tma_load_2d(s_sb + s * (kScaleBytes / 4), &map_sb, &bars[kBarFull + s], ti.g0,
                                 st * 4);
                 }
@@ -532,16 +642,21 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2>::kThreads, 1)
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const TcTile ti = tc_tile<kTail>(t, a, s_off, s_tpre);
                 if (kTail && ti.ncols == 0) continue;
-                const uint32_t idesc = idesc_e4m3_f32(kBM, ti.ncols);
+                const uint32_t idesc =
+                    kWQ ? idesc_e4m3_e5m2_f32(kBM, ti.ncols) : idesc_e4m3_f32(kBM, ti.ncols);
                 for (int st = 0; st < nst && ok; ++st, ++ks) {
                     const int s = ks % kStages;
-                    if (!mbar_wait_bounded(&bars[kBarFull + s], (ks / kStages) & 1, lim, abort_flag)) {
+                    // the widening instance's weight tile is ready once the widening
+                    // warps, which waited for the stage themselves, have written it
+                    if (!mbar_wait_bounded(&bars[(kWQ ? kBarWide : kBarFull) + s], (ks / kStages) & 1,
+                                           lim, abort_flag)) {
                         set_abort(misc);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint64_t da = smem_desc_sw128(smem_u32(s_a + s * kTileBytes));
+                    const uint64_t dc = smem_desc_sw128(smem_u32(s_c));
                     const uint64_t db = smem_desc_sw128(smem_u32(s_b + s * C::kBTile));
                     for (int j0 = 0; j0 < 4; j0 += kGroup, ++kg) {
                         const int gb = kg % kBufs;
@@ -558,7 +673,12 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2>::kThreads, 1)
                             // block j's 32 weight bytes start 32 j bytes into each 128-byte row
                             const uint64_t koff = (32 * j) >> 4;
                             const uint32_t slot = tmem + (gb * kGroup + i) * 128;
-                            if constexpr (XB == 4) {
+                            if constexpr (kWQ) {
+                                // (q 2^-9)(512 x) summed, then (-8 2^-9)(512 x):
+                                // S = sum q x - 8 sum x, integers below 2^24, exact
+                                mma_f8f6f4(slot, da + koff, db + koff, idesc, 0);
+                                mma_f8f6f4(slot, dc + koff, db + koff, idesc, 1);
+                            } else if constexpr (XB == 4) {
                                 mma_f8f6f4(slot, da + koff, db + koff, idesc, 0);
                             } else {
                                 // S = sum w (16 h) + sum w l: two MMAs into one accumulator
@@ -579,13 +699,18 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2>::kThreads, 1)
             mbar_wait_bounded(&bars[kBarDrain], 0, kDrainPolls, nullptr);
         }
     } else if (warp < C::kProdWarps) {
-        // the producer warpgroup's two idle warps
+        // the producer warpgroup's other two warps: idle, or the widening warps
         if constexpr (C::kRegSplit) reg_dealloc<C::kProdRegs>();
+        if constexpr (kWQ) {
+            if (!widen_tiles<kTail>(a, total, s_off, s_tpre, bars, s_n, s_a, (warp - 2) * 32 + lane,
+                                    abort_flag))
+                set_abort(misc);
+        }
     } else if constexpr (!kSums) {
         // ------------------------------------------------------- epilogue
         if constexpr (C::kRegSplit) reg_alloc<C::kEpiRegs>();
-        if (!epilogue_tiles<EPQ, XB, kEpi == 2, kTail>(a, total, s_off, s_tpre, bars, s_sa, s_sb,
-                                                       s_q, tmem, warp, lane, abort_flag))
+        if (!epilogue_tiles<EPQ, XB, kEpi == 2, kTail, kWQ>(a, total, s_off, s_tpre, bars, s_sa,
+                                                            s_sb, s_q, tmem, warp, lane, abort_flag))
             set_abort(misc);
     } else {
         // ------------------------------------ epilogue with block sums
@@ -614,10 +739,9 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2>::kThreads, 1)
                     ok = false;
                     break;
                 }
-                const float *sa = s_sa + s * (kScaleBytes / 4);   // [128 rows][4 blocks]
                 const float *sb = s_sb + s * (kScaleBytes / 4);   // [4 blocks][bn tokens]
-                const float4 dw4 = *reinterpret_cast<const float4 *>(sa + 4 * row);
-                const float dws[4] = {dw4.x, dw4.y, dw4.z, dw4.w};
+                float dws[4];
+                stage_dw<kWQ>(s_sa, s, row, st, dws);
 #pragma unroll
                 for (int j0 = 0; j0 < 4; j0 += kGroup, ++kg) {
                     const int gb = kg % kBufs;
@@ -840,11 +964,11 @@ TcPlan plan_tc(int64_t M, int64_t N, int sms, bool allow_cut) {
     return plan;
 }
 
-template <int EPQ, int XB, int kEpi, bool kTail = false>
+template <int EPQ, int XB, int kEpi, bool kTail = false, bool kWQ = false>
 h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStream_t s) {
-    using C = TcCfg<EPQ, XB, kEpi == 2>;
+    using C = TcCfg<EPQ, XB, kEpi == 2, kWQ>;
     constexpr int kSmem = C::kSmem;
-    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi, kTail>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi, kTail, kWQ>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return launch_status(e);
     if constexpr (C::kRegSplit) {
@@ -853,7 +977,7 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
         // (read once per kernel; a failed read leaves -1 and refuses every launch)
         static const int regs = [] {
             cudaFuncAttributes fa{};
-            return cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi, kTail>) == cudaSuccess
+            return cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi, kTail, kWQ>) == cudaSuccess
                        ? fa.numRegs
                        : -1;
         }();
@@ -862,7 +986,7 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
             return H32_ERR_UNSUPPORTED;
         }
     }
-    const cudaError_t el = launch_pdl(gemm_tc_kernel<EPQ, XB, kEpi, kTail>, dim3(grid), dim3(C::kThreads),
+    const cudaError_t el = launch_pdl(gemm_tc_kernel<EPQ, XB, kEpi, kTail, kWQ>, dim3(grid), dim3(C::kThreads),
                                       kSmem, s, maps[0], maps[1], maps[2], maps[3], a);
     return launch_status(el != cudaSuccess ? el : cudaGetLastError());
 }
@@ -888,11 +1012,15 @@ namespace {
 
 // Shared by the dense and the expert-batched entry points: checks, tensor
 // maps, launch.  E groups of weight rows [E * N][K]; expert_off null = dense.
+// With wd16 set (the widening instance), wp holds the Q4_0 nibbles [E * N][K / 2]
+// and wd16 the fp16 scales [E * N][K / 32]; wsc and ldws are unused.
 h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t ldws, int64_t E,
                        const uint8_t *xw, const float *xdt, int64_t ldxd,
                        const int32_t *expert_off, int64_t M, int64_t N, int64_t K, float *y,
                        int64_t ldy, int32_t *block_sums, void *stream, uint8_t *qn = nullptr,
-                       float *qnd = nullptr, int64_t ldqnd = 0, int qn_rot = 0) {
+                       float *qnd = nullptr, int64_t ldqnd = 0, int qn_rot = 0,
+                       const uint16_t *wd16 = nullptr) {
+    if (wd16) ldws = K / 32;
     if (M < 0 || N <= 0 || K <= 0 || (K % 128) != 0 || (N % 16) != 0 || (y && ldy < N) ||
         ldws < K / 32 || (ldws % 4) != 0 || ldxd < M || (ldxd % 4) != 0 || E < 1 ||
         E > kMaxExperts)
@@ -900,9 +1028,13 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     if (qn && ((N % 32) != 0 || !qnd || ldqnd < M || block_sums ||
                (qn_rot != 0 && qn_rot != 1 && qn_rot != 32)))
         return H32_ERR_INVALID_ARG;
+    // the widening instance: fp16 scale rows of K / 16 bytes, a multiple of 16
+    // for their tensor map
+    if (wd16 && ((K % 256) != 0 || xbits != 4 || qn)) return H32_ERR_INVALID_ARG;
     if (M == 0) return H32_OK;
-    if (!wp || !wsc || !xw || !xdt || (!y && !qn)) return H32_ERR_INVALID_ARG;
-    if (!aligned16(wp) || !aligned16(wsc) || !aligned16(xw) || !aligned16(xdt) ||
+    if (!wp || (!wsc && !wd16) || !xw || !xdt || (!y && !qn)) return H32_ERR_INVALID_ARG;
+    if (!aligned16(wp) || (wsc && !aligned16(wsc)) || (wd16 && !aligned16(wd16)) ||
+        !aligned16(xw) || !aligned16(xdt) ||
         (y && !aligned16(y)) || (qn && (!aligned16(qn) || !aligned16(qnd))) ||
         (block_sums && !aligned16(block_sums)) || (expert_off && !aligned16(expert_off)) ||
         (y && (ldy % 4) != 0))
@@ -925,11 +1057,19 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     const int bn = plan.bn;
     const int64_t grid = plan.grid;
     CUtensorMap maps[4];
-    H32_TRY(make_map(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wp, K, E * N, K, 128, kBM, true));
+    if (wd16) {
+        H32_TRY(make_map(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wp, K / 2, E * N, K / 2, 64,
+                         kBM, false));
+        H32_TRY(make_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, wd16, K / 32, E * N, K / 16,
+                         8, kBM, false));
+    } else {
+        H32_TRY(make_map(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wp, K, E * N, K, 128, kBM,
+                         true));
+        H32_TRY(make_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, wsc, ldws, E * N, ldws * 4,
+                         4, kBM, false));
+    }
     const int64_t xrow = K * (xbits / 4);   // activation bytes per row
     H32_TRY(make_map(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xw, xrow, M, xrow, 128, bn, true));
-    H32_TRY(make_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, wsc, ldws, E * N, ldws * 4, 4,
-                     kBM, false));
     H32_TRY(make_map(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, xdt, ldxd, K / 32, ldxd * 4, bn, 4,
                      false));
     TcArgs a{};
@@ -951,6 +1091,11 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     a.wait_limit = wait_limit();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int g = static_cast<int>(grid);
+    if (wd16) {
+        if (block_sums) return launch_tc<4, 4, 1, false, true>(maps, a, g, s);
+        return plan.tail_k > 1 ? launch_tc<4, 4, 0, true, true>(maps, a, g, s)
+                               : launch_tc<4, 4, 0, false, true>(maps, a, g, s);
+    }
     if (xbits == 8) {
         if (block_sums) return launch_tc<H32_TC_EPI_PER_QUAD, 8, 1>(maps, a, g, s);
         return plan.tail_k > 1 ? launch_tc<H32_TC_EPI_PER_QUAD, 8, 0, true>(maps, a, g, s)
@@ -994,6 +1139,26 @@ extern "C" h32_status q4_0_x_q4_gemm_tc_quant_next(const uint8_t *wp, const floa
     if (!xw_next) return H32_ERR_INVALID_ARG;
     return h32::run_gemm_tc(4, wp, wsc, ldws, 1, xw, xdt, ldxd, nullptr, M, N, K, y, ldy, nullptr,
                             stream, xw_next, xdt_next, ldxd_next, rotate_next);
+}
+
+extern "C" h32_status q4_0_x_q4_gemm_tc_widen(const uint8_t *wq, const uint16_t *wd,
+                                              const uint8_t *xw, const float *xdt, int64_t ldxd,
+                                              int64_t M, int64_t N, int64_t K, float *y,
+                                              int64_t ldy, int32_t *block_sums, void *stream) {
+    if (!wd) return H32_ERR_INVALID_ARG;
+    return h32::run_gemm_tc(4, wq, nullptr, 0, 1, xw, xdt, ldxd, nullptr, M, N, K, y, ldy,
+                            block_sums, stream, nullptr, nullptr, 0, 0, wd);
+}
+
+extern "C" h32_status q4_0_x_q4_gemm_tc_widen_experts(const uint8_t *wq, const uint16_t *wd,
+                                                      int32_t E, const uint8_t *xw,
+                                                      const float *xdt, int64_t ldxd,
+                                                      const int32_t *expert_off, int64_t R,
+                                                      int64_t N, int64_t K, float *y, int64_t ldy,
+                                                      int32_t *block_sums, void *stream) {
+    if (!wd || !expert_off) return H32_ERR_INVALID_ARG;
+    return h32::run_gemm_tc(4, wq, nullptr, 0, E, xw, xdt, ldxd, expert_off, R, N, K, y, ldy,
+                            block_sums, stream, nullptr, nullptr, 0, 0, wd);
 }
 
 extern "C" h32_status q4_0_x_q8_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws,

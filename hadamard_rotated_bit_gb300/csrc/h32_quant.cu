@@ -249,8 +249,10 @@ __global__ void __launch_bounds__(256) quant_w_kernel(const float *__restrict__ 
 // against 180 us for one row of 32 blocks per warp and 236 us for a block-major
 // walk).  With kGather,
 // output row r is the quantized input row row_idx[r] (an index outside
-// [0, T) records kStatusGuard and yields zero codes and a zero scale).
-template <bool kBf16, int kBits, int kRot, bool kGather>
+// [0, T) records kStatusGuard and yields zero codes and a zero scale).  kE5
+// (4-bit only): the codes as the e5m2 bytes of 512 times the code, the
+// activation side of the GEMM that widens Q4_0 weights in shared memory.
+template <bool kBf16, int kBits, int kRot, bool kGather, bool kE5 = false>
 __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restrict__ x, uint32_t nblk,
                                                           uint32_t M, uint32_t K, int64_t ldx,
                                                           const int32_t *__restrict__ row_idx,
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__(256) quant_act_tc_kernel(const void *__restric
         float d;
         if constexpr (kBits == 4) {
             uint32_t w[8];
-            d = quant_block_tc4(v, w);
+            d = quant_block_tc4<kE5>(v, w);
             uint4 *dst = reinterpret_cast<uint4 *>(xw + int64_t(row) * K + 32 * b);
             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -474,7 +476,7 @@ extern "C" h32_status h32_rotate_quantize_weights_q4_0(const float *w, int64_t N
 
 namespace h32 {
 namespace {
-template <int kBits>
+template <int kBits, bool kE5 = false>
 h32_status quantize_act_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K, int64_t ldx,
                            const int32_t *row_idx, int64_t T, uint8_t *xw, float *xdt,
                            int64_t ldxd, int rotate, void *stream) {
@@ -498,7 +500,7 @@ h32_status quantize_act_tc(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint32_t m32 = static_cast<uint32_t>(M), k32 = static_cast<uint32_t>(K);
 #define H32_QTC(BF, ROT, GA)                                                                  \
-    e = launch_pdl(quant_act_tc_kernel<BF, kBits, ROT, GA>, dim3(grid), dim3(256), 0, s, x, nblk, \
+    e = launch_pdl(quant_act_tc_kernel<BF, kBits, ROT, GA, kE5>, dim3(grid), dim3(256), 0, s, x, nblk, \
                    m32, k32, ldx, row_idx, T, xw, xdt, ldxd)
 #define H32_QTC_R(ROT)                    \
     do {                                  \
@@ -540,6 +542,23 @@ extern "C" h32_status h32_quantize_act_q4_tc_gather(const void *x, h32_in_dtype 
                                                     int64_t ldxd, int rotate, void *stream) {
     if (!row_idx) return H32_ERR_INVALID_ARG;
     return h32::quantize_act_tc<4>(x, dt, R, K, ldx, row_idx, T, xw, xdt, ldxd, rotate, stream);
+}
+
+extern "C" h32_status h32_quantize_act_q4_tc_e5m2(const void *x, h32_in_dtype dt, int64_t M,
+                                                  int64_t K, int64_t ldx, uint8_t *xw, float *xdt,
+                                                  int64_t ldxd, int rotate, void *stream) {
+    return h32::quantize_act_tc<4, true>(x, dt, M, K, ldx, nullptr, M, xw, xdt, ldxd, rotate,
+                                         stream);
+}
+
+extern "C" h32_status h32_quantize_act_q4_tc_e5m2_gather(const void *x, h32_in_dtype dt,
+                                                         int64_t T, int64_t K, int64_t ldx,
+                                                         const int32_t *row_idx, int64_t R,
+                                                         uint8_t *xw, float *xdt, int64_t ldxd,
+                                                         int rotate, void *stream) {
+    if (!row_idx) return H32_ERR_INVALID_ARG;
+    return h32::quantize_act_tc<4, true>(x, dt, R, K, ldx, row_idx, T, xw, xdt, ldxd, rotate,
+                                         stream);
 }
 
 extern "C" h32_status h32_prepack_weights_q4_0_tc(const uint8_t *wq, const uint16_t *wd, int64_t N,

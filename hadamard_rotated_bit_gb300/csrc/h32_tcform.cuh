@@ -100,6 +100,17 @@ __device__ __forceinline__ void tc_bytes_q8(uint32_t c, uint32_t &hi, uint32_t &
 }
 
 
+// The widening form of the weight codes: the Q4_0 code q (0..15) itself as
+// the byte 0x0q, which read as e4m3 is q * 2^-9 exactly (exponent field 0:
+// subnormals m * 2^-9 for q < 8; field 1: (8 + m) * 2^-9 for q >= 8).  Eight
+// codes of one word of a Q4_0 block (byte j of the block: element j in the low
+// nibble, element j + 16 in the high one) -> the bytes of the low-nibble
+// elements j..j+3 in `lo` and of the high-nibble elements j+16..j+19 in `hi`.
+__device__ __forceinline__ void widen_q4_0_word(uint32_t x, uint32_t &lo, uint32_t &hi) {
+    lo = x & 0x0F0F0F0Fu;
+    hi = (x >> 4) & 0x0F0F0F0Fu;
+}
+
 // four integer-valued floats (each exactly representable in e4m3: |c| <= 16,
 // or a multiple of 16 up to 128) -> their e4m3 bytes, c0 in the lowest byte.
 // The hardware conversion is exact for such values.
@@ -110,12 +121,30 @@ __device__ __forceinline__ uint32_t e4m3x4_of_ints(float c0, float c1, float c2,
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
+// The activation side of the widening form: four integer codes |c| <= 8 ->
+// the e5m2 bytes of 512 c (exact: at most three significant bits, exponent
+// within range), so that with weights read as q * 2^-9 every product is the
+// integer q c.  0 = 0x00, 1 = 0x60, 2 = 0x64, 3 = 0x66, 4 = 0x68, 5 = 0x69,
+// 6 = 0x6A, 7 = 0x6B, 8 = 0x6C, the sign in bit 7.
+__device__ __forceinline__ uint32_t e5m2x4_of_ints_x512(float c0, float c1, float c2, float c3) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;"
+        : "=h"(lo)
+        : "f"(__fmul_rn(c1, 512.0f)), "f"(__fmul_rn(c0, 512.0f)));
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;"
+        : "=h"(hi)
+        : "f"(__fmul_rn(c3, 512.0f)), "f"(__fmul_rn(c2, 512.0f)));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
 // One 32-block y of activations to 4-bit codes in tensor-core form, the step
 // every 4-bit tc-form producer shares (the activation quantizer and the GEMM
 // that quantizes its own output): d = amax(|y|) / 7 (IEEE divide), codes
 // round-half-even(y * fl(1/d)) (the clamped y / d in a degenerate block), each
-// code as the e4m3 byte of the integer; w[k] holds codes 4k .. 4k + 3 from its
-// low byte up.  Returns d.
+// code as the e4m3 byte of the integer (kE5: the e5m2 byte of 512 times the
+// integer, the widening form); w[k] holds codes 4k .. 4k + 3 from its low byte
+// up.  Returns d.
+template <bool kE5 = false>
 __device__ __forceinline__ float quant_block_tc4(const float (&v)[32], uint32_t (&w)[8]) {
     float amax = 0.0f;
 #pragma unroll
@@ -138,7 +167,12 @@ __device__ __forceinline__ float quant_block_tc4(const float (&v)[32], uint32_t 
 #pragma unroll
     for (int i = 0; i < 32; ++i) c[i] = __fsub_rn(__uint_as_float(bits[i]), kRoundMagic);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) w[k] = e4m3x4_of_ints(c[4 * k], c[4 * k + 1], c[4 * k + 2], c[4 * k + 3]);
+    for (int k = 0; k < 8; ++k) {
+        if constexpr (kE5)
+            w[k] = e5m2x4_of_ints_x512(c[4 * k], c[4 * k + 1], c[4 * k + 2], c[4 * k + 3]);
+        else
+            w[k] = e4m3x4_of_ints(c[4 * k], c[4 * k + 1], c[4 * k + 2], c[4 * k + 3]);
+    }
     return d;
 }
 

@@ -256,6 +256,77 @@ h32_status q4_0_x_q4_gemm_tc_quant_next(const uint8_t *wp, const float *wsc, int
                                         int rotate_next, void *stream);
 
 /*
+ * ---------------------------------------------------------------------------
+ * Widening form.  The GEMMs below read the Q4_0 weight planes themselves
+ * (half the weight bytes of the tc form; no repack) and widen each K stage's
+ * nibbles in shared memory ("Why prompts are a matrix-unit problem": the codes
+ * go to the matrix units as small integers).  A code q (0..15) becomes the byte
+ * 0x0q, which the FP8 tensor cores read as e4m3 q * 2^-9, exactly; the
+ * activations of this form are the e5m2 bytes of 512 times their codes, also
+ * exact, so every product is the integer q x.  One more tensor-core product
+ * per block, against weights of -8 * 2^-9, subtracts 8 times the activation
+ * block sum: S = sum (q - 8) x exactly, and the results are bit-identical to
+ * the tc form and to the Q4_0 entry points.
+ * ---------------------------------------------------------------------------
+ */
+
+/*
+ * Rotate and quantize activations exactly as h32_quantize_act_q4_tc (same
+ * codes, same scales, same layouts), each code c stored as the e5m2 byte of
+ * 512 c: 0 = 0x00, 1 = 0x60, 2 = 0x64, 3 = 0x66, 4 = 0x68, 5 = 0x69, 6 = 0x6A,
+ * 7 = 0x6B, 8 = 0x6C, bit 7 the sign.
+ *   xw     [M][K] out: one byte per code, element order
+ *   xdt    [K/32][ldxd] out: fp32 scales, as for h32_quantize_act_q4_tc
+ */
+h32_status h32_quantize_act_q4_tc_e5m2(const void *x, h32_in_dtype dt, int64_t M, int64_t K,
+                                       int64_t ldx, uint8_t *xw, float *xdt, int64_t ldxd,
+                                       int rotate, void *stream);
+
+/*
+ * The same with the row gather of h32_quantize_act_q4_tc_gather (output row r
+ * is input row row_idx[r]; an index outside [0, T) records
+ * H32_ERR_DEVICE_GUARD and its row gets zero codes and a zero scale).
+ */
+h32_status h32_quantize_act_q4_tc_e5m2_gather(const void *x, h32_in_dtype dt, int64_t T,
+                                              int64_t K, int64_t ldx, const int32_t *row_idx,
+                                              int64_t R, uint8_t *xw, float *xdt, int64_t ldxd,
+                                              int rotate, void *stream);
+
+/*
+ * The W4A4 product of q4_0_x_q4_gemm on the Q4_0 planes, widened in shared
+ * memory:
+ *   y[m][n] = sum over blocks b in order of acc = fma(fp32(d_w * d_x), S, acc)
+ * with d_w = wd[n][b] (fp16, widened exactly), d_x = xdt[b][m]; bit-identical to
+ * q4_0_x_q4_gemm_tc and q4_0_x_q4_gemm.
+ *   wq, wd          [N][K/2], [N][K/32] Q4_0 planes as written by
+ *                   h32_rotate_quantize_weights_q4_0 (fp16 scale bit patterns)
+ *   xw, xdt, ldxd   from h32_quantize_act_q4_tc_e5m2
+ *   y               [M][ldy] fp32 out;  block_sums nullable int32 [M][N][K/32]
+ * Requires K % 256 == 0 (the scale rows, K/16 bytes, feed a tensor copy of
+ * 16-byte units) and N % 16 == 0.
+ */
+h32_status q4_0_x_q4_gemm_tc_widen(const uint8_t *wq, const uint16_t *wd, const uint8_t *xw,
+                                   const float *xdt, int64_t ldxd, int64_t M, int64_t N,
+                                   int64_t K, float *y, int64_t ldy, int32_t *block_sums,
+                                   void *stream);
+
+/*
+ * The expert-batched product of q4_0_x_q4_gemm_tc_experts on the experts' Q4_0
+ * planes, widened in shared memory as in q4_0_x_q4_gemm_tc_widen.
+ *   wq     [E][N][K/2] Q4_0 codes;  wd [E][N][K/32] fp16 scales (the experts'
+ *          planes stacked as E * N rows)
+ *   xw, xdt, ldxd   in grouped order, from h32_quantize_act_q4_tc_e5m2_gather
+ *                   (or h32_quantize_act_q4_tc_e5m2 of rows already grouped)
+ *   expert_off, R, y, block_sums as for q4_0_x_q4_gemm_tc_experts
+ * Requires 1 <= E <= 1024, K % 256 == 0 and N % 16 == 0.
+ */
+h32_status q4_0_x_q4_gemm_tc_widen_experts(const uint8_t *wq, const uint16_t *wd, int32_t E,
+                                           const uint8_t *xw, const float *xdt, int64_t ldxd,
+                                           const int32_t *expert_off, int64_t R, int64_t N,
+                                           int64_t K, float *y, int64_t ldy,
+                                           int32_t *block_sums, void *stream);
+
+/*
  * The W4A8 product of q4_0_x_q8_gemm on tc-form operands (weights from
  * h32_prepack_weights_q4_0_tc, activations from h32_quantize_act_q8_tc):
  * S = sum w (16 h) + sum w l per block (two MMAs into one accumulator, every

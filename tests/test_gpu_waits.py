@@ -76,11 +76,12 @@ def _exact_small_case(h32):
     assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
 
 
-@pytest.mark.parametrize("kind", ["q4_tc", "q8_tc", "experts_tc"])
+@pytest.mark.parametrize("kind", ["q4_tc", "q8_tc", "experts_tc", "widen", "widen_experts"])
 def test_tc_gemm_one_poll_wait_bound(h32, kind):
     """The tensor-core-form GEMM (the chain's kernel, its 8-bit and its expert
-    instances) under a one-poll wait bound: the TMA, MMA and epilogue roles that
-    give up record H32_ERR_TIMEOUT, drain their copies and MMAs, free TMEM and
+    instances, and the instances that widen Q4_0 planes in shared memory) under
+    a one-poll wait bound: the TMA, MMA, widening and epilogue roles that give
+    up record H32_ERR_TIMEOUT, drain their copies and MMAs, free TMEM and
     return; the status is reported once and the same context then computes
     exact results."""
     import torch
@@ -92,6 +93,9 @@ def test_tc_gemm_one_poll_wait_bound(h32, kind):
     E = 8
     off = torch.tensor([i * M // E for i in range(E + 1)], dtype=torch.int32, device="cuda")
     wpe, wsce = _tc_ones(h32, E * 512, K, 0.0625)
+    # Q4_0 planes: every code 9 (value +1), scales fp16 0.0625
+    wq = torch.full((E * 512, K // 2), 0x99, dtype=torch.uint8, device="cuda")
+    wd = torch.full((E * 512, K // 32), 0x2C00, dtype=torch.int16, device="cuda")
     assert h32.h32_device_status() == 0
     h32.h32_set_wait_limit(1)
     try:
@@ -100,8 +104,12 @@ def test_tc_gemm_one_poll_wait_bound(h32, kind):
                 h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M)
             elif kind == "q8_tc":
                 h32.q4_0_x_q8_gemm_tc(wp, wsc, xw, xdt, M=M)
-            else:
+            elif kind == "experts_tc":
                 h32.q4_0_x_q4_gemm_tc_experts(wpe, wsce, xw, xdt, off, 512, R=M)
+            elif kind == "widen":
+                h32.q4_0_x_q4_gemm_tc_widen(wq, wd, xw, xdt, M=M)
+            else:
+                h32.q4_0_x_q4_gemm_tc_widen_experts(wq, wd, xw, xdt, off, 512, R=M)
         st = h32.h32_device_status()
     finally:
         h32.h32_set_wait_limit(0)

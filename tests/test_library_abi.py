@@ -123,6 +123,38 @@ def test_tc_form_bad_arguments(lib):
     assert _call("q4_0_x_q4_gemm_tc", p, p, 4, p, p, 8, 0, 16, 128, p, 16, None, s) == h32.H32_OK
 
 
+def test_widen_bad_arguments(lib):
+    """The GEMMs on Q4_0 planes widened in shared memory: K % 256 (the fp16 scale
+    rows feed a tensor copy of 16-byte units), null or misaligned scales, the
+    expert count and offsets; M = 0 enqueues nothing."""
+    p = ctypes.c_void_p(256)
+    bad = ctypes.c_void_p(264)
+    s = ctypes.c_void_p(0)
+    assert _call("q4_0_x_q4_gemm_tc_widen", p, p, p, p, 8, 8, 16, 384, p, 16, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc_widen", p, None, p, p, 8, 8, 16, 256, p, 16, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc_widen", p, bad, p, p, 8, 8, 16, 256, p, 16, None,
+                 s) == h32.H32_ERR_ALIGNMENT
+    assert _call("q4_0_x_q4_gemm_tc_widen", p, p, p, p, 8, 8, 24, 256, p, 24, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc_widen_experts", p, p, 0, p, p, 8, p, 8, 16, 256, p, 16, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc_widen_experts", p, p, 2, p, p, 8, None, 8, 16, 256, p, 16,
+                 None, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc_widen_experts", p, p, 2, p, p, 8, p, 8, 16, 128, p, 16, None,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("q4_0_x_q4_gemm_tc_widen", p, p, p, p, 8, 0, 16, 256, p, 16, None,
+                 s) == h32.H32_OK
+    # the widening form's activation quantizers: ldxd < M, null index, misaligned index
+    assert _call("h32_quantize_act_q4_tc_e5m2", p, 1, 8, 64, 64, p, p, 4, 1,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_quantize_act_q4_tc_e5m2_gather", p, 1, 4, 64, 64, None, 8, p, p, 8, 1,
+                 s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_quantize_act_q4_tc_e5m2_gather", p, 1, 4, 64, 64, bad, 8, p, p, 8, 1,
+                 s) == h32.H32_ERR_ALIGNMENT
+
+
 def test_rotation_size_validated(lib):
     p = ctypes.c_void_p(256)
     s = ctypes.c_void_p(0)

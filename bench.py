@@ -680,9 +680,64 @@ def run_peaks(args):
     return lines
 
 
+def run_only_moe_gemm(args):
+    """A small case for profilers: one expert GEMM of the MoE micro-batch
+    (1024 tokens, 128 experts, top 8) alone, in the operand form `args.form`
+    (tc or widen), `warmup + steps` launches timed with CUDA events."""
+    import torch
+    import hadamard_rotated_bit_gb300 as h32
+    from hadamard_rotated_bit_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", 0)
+    cfg = wl.MOE
+    row_idx, off, _ = wl.moe_routing(cfg)
+    x_gu, x_dn = wl.moe_inputs(cfg)
+    w_gu, w_dn = wl.moe_weights(cfg)
+    up = args.only_gemm == "moe_gate_up"
+    x, w = (x_gu, w_gu) if up else (x_dn, w_dn)
+    E, N, K = w.shape
+    R = int(off[-1])
+    wq, wd = h32.h32_rotate_quantize_weights_q4_0(torch.from_numpy(w.reshape(E * N, K)).to(dev))
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    ridx = torch.from_numpy(row_idx).to(dev)
+    offs = torch.from_numpy(off).to(dev)
+    y = torch.empty((R, N), dtype=torch.float32, device=dev)
+    if args.form == "widen":
+        xw, xdt = (h32.h32_quantize_act_q4_tc_e5m2_gather(xt, ridx) if up
+                   else h32.h32_quantize_act_q4_tc_e5m2(xt))
+
+        def gemm():
+            h32.q4_0_x_q4_gemm_tc_widen_experts(wq, wd, xw, xdt, offs, N, R=R, y=y)
+    elif args.form == "tc":
+        wq, wd = h32.h32_prepack_weights_q4_0_tc(wq, wd)
+        xw, xdt = h32.h32_quantize_act_q4_tc_gather(xt, ridx) if up else h32.h32_quantize_act_q4_tc(xt)
+
+        def gemm():
+            h32.q4_0_x_q4_gemm_tc_experts(wq, wd, xw, xdt, offs, N, R=R, y=y)
+    else:
+        raise SystemExit("--only-gemm moe_*: --form tc or widen")
+    for _ in range(args.warmup):
+        gemm()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record()
+    for _ in range(args.steps):
+        gemm()
+    t1.record()
+    torch.cuda.synchronize()
+    if h32.h32_device_status() != 0:
+        raise RuntimeError("device status not OK")
+    ms = t0.elapsed_time(t1) / args.steps
+    return {"only_gemm": args.only_gemm, "form": args.form, "ms_per_launch": round(ms, 5),
+            "eff_TOPS": round(2 * R * N * K / (ms / 1e3) / 1e12, 1),
+            "steps": args.steps, "warmup": args.warmup}
+
+
 def run_only_gemm(args):
     """A small case for profilers: one projection's GEMM alone (resident
     inputs, `warmup + steps` launches), timed with CUDA events."""
+    if args.only_gemm.startswith("moe_"):
+        return run_only_moe_gemm(args)
     import torch
     import hadamard_rotated_bit_gb300 as h32
     from hadamard_rotated_bit_gb300 import _build
@@ -1253,7 +1308,8 @@ def main(argv=None):
     ap.add_argument("--suite", action="store_true",
                     help="measure the other configurations (8-bit and unrotated routes, MoE, "
                          "long prompts, streaming quantizer), one JSON line each")
-    ap.add_argument("--only-gemm", choices=[p.name for p in CHAIN], default=None,
+    ap.add_argument("--only-gemm", choices=[p.name for p in CHAIN] + ["moe_gate_up", "moe_down"],
+                    default=None,
                     help="time one projection's GEMM alone (a small case for profilers)")
     ap.add_argument("--only-quant", choices=["q4", "q8", "q4_tc", "q8_tc"], default=None,
                     help="time the activation quantizer alone on a 16384 x 17408 bf16 matrix "

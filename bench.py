@@ -139,10 +139,15 @@ def load_rates():
 
 
 def source_sha(paths) -> str:
+    """Hash of the code of the given sources, comments and blank lines left out
+    (a comment edit does not make a profile's counters stale)."""
     h = hashlib.sha256()
     for path in paths:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip()).encode())
     return h.hexdigest()[:16]
 
 

@@ -20,7 +20,8 @@
 //   warp 1      TMEM allocator and MMA issuer: one K=32 MMA per block into one
 //               of four 128-column TMEM slots; a commit per two blocks
 //   warps 2, 3  idle (with 16 epilogue warps: they complete the producers'
-//               warpgroup, which hands its registers to the epilogue)
+//               warpgroup, which hands its registers to the epilogue); the
+//               widening warps in the widening instance (below)
 //   the rest    epilogue (16 warps, four per TMEM lane quarter, each a
 //               quarter of the tile's columns; or 12 warps, three per quarter):
 //               tcgen05.ld each block's S, fold the scales in with packed fp32

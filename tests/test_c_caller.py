@@ -38,12 +38,15 @@ def test_c_caller_builds(tmp_path):
 
 
 @pytest.mark.gpu
-def test_c_caller_matches_the_oracle(tmp_path):
+@pytest.mark.parametrize("K", [384, 512])
+def test_c_caller_matches_the_oracle(tmp_path, K):
+    """K = 384: the tensor-core route; K = 512: also the widening route (its
+    output appended), both bit-exact."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     exe = _compile(tmp_path)
-    M, N, K = 70, 144, 384
+    M, N = 70, 144
     x = wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, 290)
     w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, 291)
     inp, out = tmp_path / "in.bin", tmp_path / "out.bin"
@@ -53,8 +56,10 @@ def test_c_caller_matches_the_oracle(tmp_path):
         f.write(np.ascontiguousarray(w, np.float32).tobytes())
     r = subprocess.run([exe, str(inp), str(out)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
-    y = np.fromfile(out, np.float32).reshape(M, N)
+    routes = 2 if K % 256 == 0 else 1
+    ys = np.fromfile(out, np.float32).reshape(routes, M, N)
     wq, wd = oracle.quantize_weights_q4_0(w)
     xq, xd = oracle.quantize_act_q4(x)
     r32, _, _ = oracle.gemm(wq, wd, xq, xd, K)
-    assert np.array_equal(y.view(np.uint32), r32.view(np.uint32))
+    for y in ys:
+        assert np.array_equal(y.view(np.uint32), r32.view(np.uint32))

@@ -36,7 +36,7 @@ def _oracle_operands(name):
     return wq, wd, xq, xd, p.K
 
 
-@pytest.mark.parametrize("form", ["tc", "q4_0"])
+@pytest.mark.parametrize("form", ["tc", "q4_0", "widen"])
 def test_timed_chain_outputs(h32, form):
     import torch
     import bench

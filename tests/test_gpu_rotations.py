@@ -31,6 +31,14 @@ def e4m3_value(b):
     return sign * np.where(e == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * 2.0 ** (e - 7.0))
 
 
+def e5m2_value(b):
+    b = b.astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 2) & 0x1F
+    m = b & 3
+    return sign * np.where(e == 0, m / 4.0 * 2.0 ** -14, (1 + m / 4.0) * 2.0 ** (e - 15.0))
+
+
 def _acts(M, K, tid, bf16=True):
     x = wl.act_normal_outliers(M, K, 0.01, 25.0, 0, wl.CFG_TEST, tid)
     return wl.f32_to_bf16_bits(x) if bf16 else x
@@ -69,6 +77,10 @@ def test_tc_quantizers(h32, n, M, K):
     rq, rd = oracle.quantize_act_q4(x, n)
     assert np.array_equal(e4m3_value(np_of(xw)), oracle.decode_act4(rq, K).astype(np.float64))
     assert np.array_equal(np_of(xdt)[:, :M].T.view(np.uint32), rd.view(np.uint32))
+    xw5, xdt5 = h32.h32_quantize_act_q4_tc_e5m2(torch_bf16(x), rotate=n)
+    assert np.array_equal(e5m2_value(np_of(xw5)) / 512.0,
+                          oracle.decode_act4(rq, K).astype(np.float64))
+    assert np.array_equal(np_of(xdt5)[:, :M].T.view(np.uint32), rd.view(np.uint32))
     r8, rd8 = oracle.quantize_act_q8(x, n)
     v = e4m3_value(np_of(xw8)).reshape(M, K // 32, 2, 32)
     assert np.array_equal((v[:, :, 0] + v[:, :, 1]).reshape(M, K), r8.astype(np.float64))
@@ -103,8 +115,9 @@ def test_weight_quantizer(h32, n):
 
 @pytest.mark.parametrize("n", [64, 128])
 def test_products_with_larger_rotation(h32, n):
-    """The tensor-core-form W4A4 and W4A8 products and the Q4_0-direct W4A4
-    product on n-point-rotated operands, bit for bit against the oracle."""
+    """The tensor-core-form W4A4 and W4A8 products, the widening-form W4A4
+    product and the Q4_0-direct W4A4 product on n-point-rotated operands, bit for
+    bit against the oracle."""
     import torch
     M, N, K = 70, 160, 1024
     x = _acts(M, K, 440 + n)
@@ -125,6 +138,13 @@ def test_products_with_larger_rotation(h32, n):
         assert h32.h32_device_status() == 0
         r32, _, _ = oracle.gemm(rwq, rwd, rxq, rxd, K)
         assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32)), bits
+    xw5, xdt5 = h32.h32_quantize_act_q4_tc_e5m2(torch_bf16(x), rotate=n)
+    y = h32.q4_0_x_q4_gemm_tc_widen(wq, wd, xw5, xdt5, M=M)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    rxq, rxd = oracle.quantize_act_q4(x, n)
+    r32, _, _ = oracle.gemm(rwq, rwd, rxq, rxd, K)
+    assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32)), "widen"
     xq, xd = h32.h32_quantize_act_q4(torch_bf16(x), rotate=n)
     y = h32.q4_0_x_q4_gemm(wq, wd, xq, xd)
     torch.cuda.synchronize()

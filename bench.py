@@ -904,17 +904,32 @@ def suite_tiny(torch, h32, dev, stream, steps, warmup, pk):
     for bits in (4, 8):
         q = h32.h32_quantize_act_q4_tc if bits == 4 else h32.h32_quantize_act_q8_tc
         g = h32.q4_0_x_q4_gemm_tc if bits == 4 else h32.q4_0_x_q8_gemm_tc
+        xw = torch.empty((64, p.K * bits // 4), dtype=torch.uint8, device=dev)
+        xdt = torch.zeros((p.K // 32, 64), dtype=torch.float32, device=dev)
 
         def step():
-            xw, xdt = q(x, stream=stream)
+            q(x, xw=xw, xdt=xdt, stream=stream)
             g(wp, wsc, xw, xdt, M=64, y=y, stream=stream)
-        ms = _events_time(torch, step, steps, warmup, stream)
+        ms_eager = _events_time(torch, step, steps, warmup, stream)
+        # the same two launches captured once in a CUDA graph and replayed: the
+        # step's device time without the binding's per-call host work between them
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            step()
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        ms = _events_time(torch, graph.replay, steps, warmup, stream)
+        if h32.h32_device_status(stream) != 0:
+            raise RuntimeError("device status not OK after the tiny configuration")
         ints, alu, nbytes = chain_work([p], 64, bits)
         nbytes += 64 * p.K * 2   # fp32 activations: twice the bf16 bytes counted
         out.append({"suite": f"tiny_64x256x256_q{bits}", "value": round(64 / (ms / 1e3), 1),
                     "unit": UNIT, "ms_per_step": round(ms, 5),
+                    "ms_per_step_eager": round(ms_eager, 5),
                     **pk.fields(ms, ints, alu, nbytes),
-                    "note": "two launches of a few microseconds each: launch-bound"})
+                    "note": "quantize + GEMM captured in a CUDA graph and replayed; eager: "
+                            "each call through the Python binding"})
     return out
 
 

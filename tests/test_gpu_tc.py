@@ -650,3 +650,43 @@ def test_back_to_back_launches_reuse_buffers(h32):
         xq, xd = oracle.quantize_act_q4(x)
         r32, _, _ = oracle.gemm(wq, wd, xq, xd, K)
         assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
+
+
+def test_chain_step_captured_in_a_cuda_graph(h32):
+    """Quantize + tc GEMM captured once in a CUDA graph (the launches carry the
+    programmatic-dependency attribute) and replayed on new inputs written into
+    the same buffers: every replay bit-exact against the oracle."""
+    import torch
+    M, N, K = 64, 256, 512
+    w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, 700)
+    rwq, rwd = oracle.quantize_weights_q4_0(w)
+    wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(rwq), torch_of(rwd.view(np.int16)))
+    x = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    xw = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    xdt = torch.zeros((K // 32, M), dtype=torch.float32, device="cuda")
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step():
+        h32.h32_quantize_act_q4_tc(x, xw=xw, xdt=xdt, stream=s)
+        h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M, y=y, stream=s)
+
+    x.copy_(torch_of(wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, 701)))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        step()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for tid in (702, 703):
+        xh = wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, tid)
+        x.copy_(torch_of(xh))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.replay()
+        s.synchronize()
+        assert h32.h32_device_status(s) == 0
+        rxq, rxd = oracle.quantize_act_q4(xh)
+        r32, _, _ = oracle.gemm(rwq, rwd, rxq, rxd, K)
+        assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32)), tid

@@ -336,3 +336,30 @@ def moe_combine(y: np.ndarray, row_of: np.ndarray, topk_w: np.ndarray) -> np.nda
     out = np.empty((T, H), np.float32)
     _load().o_moe_combine(_ptr(y), H, _ptr(row_of), _ptr(topk_w), T, k, H, _ptr(out))
     return out
+
+
+# --------------------------------------------------------------------------
+# Q4_0 interchange: the file format's blocks <-> the two planes of the path
+# ("Qwen3.8-27B at 45.7 tok/s ...", section "Prompt processing: 4-bit
+# activations, rotated first": the route reads plain Q4_0 files).  Reading
+# taken: a block is 18 bytes, the fp16 scale d (little endian) and then the 16
+# code bytes in Q4_0 nibble order, the layout of a Q4_0 block in those files.
+# --------------------------------------------------------------------------
+def q4_0_planes_from_blocks(blocks: np.ndarray, N: int, K: int):
+    """blocks u8 [N][K/32][18] -> (wq [N][K/2] u8, wd [N][K/32] fp16 bits as u16)."""
+    b = np.asarray(blocks, np.uint8).reshape(N, K // 32, 18)
+    wd = b[:, :, 0].astype(np.uint16) | (b[:, :, 1].astype(np.uint16) << 8)
+    wq = np.ascontiguousarray(b[:, :, 2:]).reshape(N, K // 2)
+    return wq, wd
+
+
+def q4_0_blocks_from_planes(wq: np.ndarray, wd: np.ndarray) -> np.ndarray:
+    """(wq [N][K/2], wd [N][K/32] u16) -> blocks u8 [N][K/32][18]."""
+    wq = np.asarray(wq, np.uint8)
+    wd = np.asarray(wd, np.uint16)
+    N, nb = wd.shape
+    out = np.empty((N, nb, 18), np.uint8)
+    out[:, :, 0] = (wd & 0xFF).astype(np.uint8)
+    out[:, :, 1] = (wd >> 8).astype(np.uint8)
+    out[:, :, 2:] = wq.reshape(N, nb, 16)
+    return out

@@ -643,3 +643,23 @@ def test_larger_rotation_stage_order(n):
     y = oracle.fwht_n(x, n)
     assert y[0] == 0 and y[1] == -c
     assert y[n // 2] == np.float32(2.0 ** 25) * c and y[n // 2 + 1] == np.float32(2.0 ** 25) * c
+
+
+def test_q4_0_block_layout_pins():
+    """A Q4_0 block built by hand from its layout (fp16 d = 0.5 as bytes 00 38,
+    then byte j holding element j in its low nibble and element j + 16 in its
+    high one): the planes decode to the values the layout gives, and the two
+    conversions are inverse to each other."""
+    blk = np.zeros((1, 1, 18), np.uint8)
+    blk[0, 0, 0], blk[0, 0, 1] = 0x00, 0x38          # fp16 0.5, little endian
+    for j in range(16):
+        blk[0, 0, 2 + j] = j | ((15 - j) << 4)
+    wq, wd = oracle.q4_0_planes_from_blocks(blk, 1, 32)
+    assert oracle.f16_to_f32(wd)[0, 0] == np.float32(0.5)
+    vals = oracle.decode_w4(wq, 32)[0]
+    assert list(vals[:16]) == [j - 8 for j in range(16)]
+    assert list(vals[16:]) == [7 - j for j in range(16)]
+    rng = np.random.default_rng(5)
+    blocks = rng.integers(0, 256, (7, 5, 18), dtype=np.uint8)
+    wq, wd = oracle.q4_0_planes_from_blocks(blocks, 7, 160)
+    assert np.array_equal(oracle.q4_0_blocks_from_planes(wq, wd), blocks)

@@ -61,6 +61,8 @@ _SIGS = {
                                             _I64, _P, _P, _I64, _INT, _P]),
     "h32_quantize_act_q8_tc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _I64, _INT, _P]),
     "q4_0_x_q8_gemm_tc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P]),
+    "h32_q4_0_blocks_to_planes": (_INT, [_P, _I64, _I64, _P, _P, _P]),
+    "h32_q4_0_planes_to_blocks": (_INT, [_P, _P, _I64, _I64, _P, _P]),
     "h32_quantize_act_q4_tc_e5m2": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _I64, _INT, _P]),
     "h32_quantize_act_q4_tc_e5m2_gather": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _P,
                                                   _I64, _INT, _P]),
@@ -288,6 +290,46 @@ def h32_rotate_quantize_weights_q4_0(w, rotate=True, wq=None, wd=None, stream=No
 # --------------------------------------------------------------------------
 # GEMMs
 # --------------------------------------------------------------------------
+def h32_q4_0_blocks_to_planes(blocks, wq=None, wd=None, stream=None):
+    """Q4_0 file blocks uint8 [N][K/32][18] (fp16 d, then 16 code bytes) -> the planes
+    (wq [N][K/2] uint8, wd [N][K/32] int16 fp16 bits)."""
+    torch = _torch()
+    if blocks.dim() != 3 or blocks.shape[2] != 18:
+        raise ValueError("blocks must be [N][K/32][18]")
+    N, nb = blocks.shape[0], blocks.shape[1]
+    K = nb * 32
+    dev = blocks.device
+    _need(blocks, "blocks", (torch.uint8,), (N, nb, 18))
+    if wq is None:
+        wq = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    if wd is None:
+        wd = torch.empty((N, nb), dtype=torch.int16, device=dev)
+    _need(wq, "wq", (torch.uint8,), (N, K // 2))
+    _need(wd, "wd", _fp16_bits(), (N, nb))
+    _same_gpu(("blocks", blocks), ("wq", wq), ("wd", wd))
+    st = lib().h32_q4_0_blocks_to_planes(_ptr(blocks), N, K, _ptr(wq), _ptr(wd), _stream(stream))
+    _check("h32_q4_0_blocks_to_planes", st)
+    return wq, wd
+
+
+def h32_q4_0_planes_to_blocks(wq, wd, blocks=None, stream=None):
+    """The planes (wq [N][K/2], wd [N][K/32]) -> Q4_0 file blocks uint8 [N][K/32][18]."""
+    torch = _torch()
+    if wq.dim() != 2:
+        raise ValueError("wq must be 2-D [N][K/2]")
+    N, K = wq.shape[0], wq.shape[1] * 2
+    dev = wq.device
+    _need(wq, "wq", (torch.uint8,), (N, K // 2))
+    _need(wd, "wd", _fp16_bits(), (N, K // 32))
+    if blocks is None:
+        blocks = torch.empty((N, K // 32, 18), dtype=torch.uint8, device=dev)
+    _need(blocks, "blocks", (torch.uint8,), (N, K // 32, 18))
+    _same_gpu(("wq", wq), ("wd", wd), ("blocks", blocks))
+    st = lib().h32_q4_0_planes_to_blocks(_ptr(wq), _ptr(wd), N, K, _ptr(blocks), _stream(stream))
+    _check("h32_q4_0_planes_to_blocks", st)
+    return blocks
+
+
 def _gemm(fn_name, wq, wd, xq, xd, y, block_sums, stream):
     torch = _torch()
     if wq.dim() != 2 or xq.dim() != 2:

@@ -379,6 +379,43 @@ __global__ void __launch_bounds__(256) prepack_w_tc_kernel(const uint8_t *__rest
     }
 }
 
+// Q4_0 interchange: the file format's 18-byte blocks (fp16 d, then the 16
+// code bytes) <-> the planes wq [N][K/2], wd [N][K/32].  A block starts on a
+// 2-byte boundary only, so it moves as nine 2-byte words; the planes as one
+// 16-byte word and one 2-byte word.
+__global__ void __launch_bounds__(256) q4_0_blocks_to_planes_kernel(
+    const uint16_t *__restrict__ blocks, uint32_t nblk, uint8_t *__restrict__ wq,
+    uint16_t *__restrict__ wd) {
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < nblk; g += stride) {
+        const uint16_t *b = blocks + int64_t(g) * 9;
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = static_cast<uint32_t>(__ldg(b + 1 + 2 * k)) |
+                   (static_cast<uint32_t>(__ldg(b + 2 + 2 * k)) << 16);
+        *reinterpret_cast<uint4 *>(wq + int64_t(g) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        wd[g] = __ldg(b);
+    }
+}
+
+__global__ void __launch_bounds__(256) q4_0_planes_to_blocks_kernel(
+    const uint8_t *__restrict__ wq, const uint16_t *__restrict__ wd, uint32_t nblk,
+    uint16_t *__restrict__ blocks) {
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < nblk; g += stride) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(wq + int64_t(g) * 16));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        uint16_t *b = blocks + int64_t(g) * 9;
+        b[0] = __ldg(wd + g);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            b[1 + 2 * k] = static_cast<uint16_t>(w[k]);
+            b[2 + 2 * k] = static_cast<uint16_t>(w[k] >> 16);
+        }
+    }
+}
+
 int grid_for(uint32_t nblk, int sm_count) {
     const uint32_t want = (nblk + 255) / 256;
     const uint32_t cap = static_cast<uint32_t>(sm_count) * 8;
@@ -579,5 +616,47 @@ extern "C" h32_status h32_prepack_weights_q4_0_tc(const uint8_t *wq, const uint1
     prepack_w_tc_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         wq, wd, static_cast<uint32_t>(N), static_cast<uint32_t>(K / 32),
         static_cast<uint32_t>(ldws), wp, wsc);
+    return launch_status(cudaGetLastError());
+}
+
+namespace h32 {
+namespace {
+h32_status q4_0_layout_args(const void *blocks, const uint8_t *wq, const uint16_t *wd, int64_t N,
+                            int64_t K) {
+    if (N < 0 || K <= 0 || (K % 32) != 0) return H32_ERR_INVALID_ARG;
+    if (N == 0) return H32_OK;
+    if (!blocks || !wq || !wd) return H32_ERR_INVALID_ARG;
+    if (!aligned16(blocks) || !aligned16(wq) || !aligned16(wd)) return H32_ERR_ALIGNMENT;
+    if (N * (K / 32) > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
+    return H32_OK;
+}
+}  // namespace
+}  // namespace h32
+
+extern "C" h32_status h32_q4_0_blocks_to_planes(const uint8_t *blocks, int64_t N, int64_t K,
+                                                uint8_t *wq, uint16_t *wd, void *stream) {
+    using namespace h32;
+    H32_TRY(q4_0_layout_args(blocks, wq, wd, N, K));
+    if (N == 0) return H32_OK;
+    int sms = 0;
+    H32_TRY(check_device(&sms));
+    const uint32_t nblk = static_cast<uint32_t>(N * (K / 32));
+    q4_0_blocks_to_planes_kernel<<<grid_for(nblk, sms), 256, 0,
+                                   reinterpret_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const uint16_t *>(blocks), nblk, wq, wd);
+    return launch_status(cudaGetLastError());
+}
+
+extern "C" h32_status h32_q4_0_planes_to_blocks(const uint8_t *wq, const uint16_t *wd, int64_t N,
+                                                int64_t K, uint8_t *blocks, void *stream) {
+    using namespace h32;
+    H32_TRY(q4_0_layout_args(blocks, wq, wd, N, K));
+    if (N == 0) return H32_OK;
+    int sms = 0;
+    H32_TRY(check_device(&sms));
+    const uint32_t nblk = static_cast<uint32_t>(N * (K / 32));
+    q4_0_planes_to_blocks_kernel<<<grid_for(nblk, sms), 256, 0,
+                                   reinterpret_cast<cudaStream_t>(stream)>>>(
+        wq, wd, nblk, reinterpret_cast<uint16_t *>(blocks));
     return launch_status(cudaGetLastError());
 }

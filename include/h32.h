@@ -113,6 +113,22 @@ h32_status h32_rotate_quantize_weights_q4_0(const float *w, int64_t N, int64_t K
                                             uint8_t *wq, uint16_t *wd, void *stream);
 
 /*
+ * Q4_0 interchange with the file format ("Qwen3.8-27B at 45.7 tok/s ...",
+ * section "Prompt processing: 4-bit activations, rotated first": the route
+ * reads plain Q4_0 files).  A file block is 18 bytes: the fp16 scale d (little
+ * endian), then the 16 code bytes in Q4_0 nibble order.  Every entry point of
+ * this library takes the two planes instead (the 18-byte blocks do not sit on
+ * the 16-byte boundaries the tensor copies need):
+ *   blocks  [N][K/32][18] bytes, the base 16-byte aligned
+ *   wq      [N][K/2] codes;  wd [N][K/32] fp16 bit patterns
+ * Requires K % 32 == 0.  Pure moves: the bytes are unchanged.
+ */
+h32_status h32_q4_0_blocks_to_planes(const uint8_t *blocks, int64_t N, int64_t K, uint8_t *wq,
+                                     uint16_t *wd, void *stream);
+h32_status h32_q4_0_planes_to_blocks(const uint8_t *wq, const uint16_t *wd, int64_t N, int64_t K,
+                                     uint8_t *blocks, void *stream);
+
+/*
  * Block-scaled integer product of Q4_0 weights and 4-bit activations (the
  * W4A4 matrix product of "Why prompts are a matrix-unit problem").
  *   y[m][n] = sum over b = 0 .. nb-1, in that order, of

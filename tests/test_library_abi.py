@@ -155,6 +155,18 @@ def test_widen_bad_arguments(lib):
                  s) == h32.H32_ERR_ALIGNMENT
 
 
+def test_q4_0_layout_bad_arguments(lib):
+    p = ctypes.c_void_p(256)
+    bad = ctypes.c_void_p(258)
+    s = ctypes.c_void_p(0)
+    assert _call("h32_q4_0_blocks_to_planes", p, 4, 48, p, p, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_q4_0_blocks_to_planes", None, 4, 64, p, p, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_q4_0_blocks_to_planes", bad, 4, 64, p, p, s) == h32.H32_ERR_ALIGNMENT
+    assert _call("h32_q4_0_planes_to_blocks", p, p, 4, 48, p, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_q4_0_planes_to_blocks", p, None, 4, 64, p, s) == h32.H32_ERR_INVALID_ARG
+    assert _call("h32_q4_0_planes_to_blocks", p, p, 0, 64, p, s) == h32.H32_OK
+
+
 def test_rotation_size_validated(lib):
     p = ctypes.c_void_p(256)
     s = ctypes.c_void_p(0)

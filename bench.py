@@ -640,21 +640,37 @@ def cpu_baseline(sample_tokens: int):
                       f"`value_one_core` single-threaded"}
 
 
+REF_BUDGET_S = 120.0   # the reference arm's whole --steps + --warmup run, about
+
+
+def ref_tokens_for(steps: int, warmup: int, secs_per_token: float) -> int:
+    """Tokens per reference step (1 to 16) that keep steps + warmup passes near
+    REF_BUDGET_S seconds at the measured time of one token."""
+    per_step = REF_BUDGET_S / (max(steps + warmup, 1) * max(secs_per_token, 1e-9))
+    return int(max(1, min(16, per_step)))
+
+
 def run_reference(args):
     """The reference arm: the CPU oracle on the host cores (every granted core),
-    each step a bounded sample (`--ref-tokens` tokens) of the pp512 chain."""
+    each step a bounded sample of the pp512 chain: `--ref-tokens` tokens, or by
+    default as many (1 to 16) as keep the whole --steps + --warmup run near
+    REF_BUDGET_S seconds, from the time of one calibration step of one token."""
     from concurrent.futures import ThreadPoolExecutor
     rank, world, local = dist_env()
     if rank != 0:
         return None
-    prepared = oracle_prepare(args.ref_tokens)
     cores = host_cores()
+    tokens = args.ref_tokens
     with ThreadPoolExecutor(cores) as pool:
+        if tokens is None:
+            tokens = ref_tokens_for(args.steps, args.warmup,
+                                    oracle_step(oracle_prepare(1), pool, cores))
+        prepared = oracle_prepare(tokens)
         for _ in range(args.warmup):
             oracle_step(prepared, pool, cores)
         secs = sum(oracle_step(prepared, pool, cores) for _ in range(args.steps))
-    value = args.ref_tokens * args.steps / secs
-    sample = (f"{args.ref_tokens} of the 512 tokens per step through the whole chain "
+    value = tokens * args.steps / secs
+    sample = (f"{tokens} of the 512 tokens per step through the whole chain "
               f"(3 quantizations + 3 full GEMMs), C oracle, each GEMM's output columns split "
               f"over {cores} threads")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
@@ -662,7 +678,7 @@ def run_reference(args):
             "ms_per_step": round(1e3 * secs / args.steps, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int64 block sums, fp32 epilogue",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "tokens_per_step": args.ref_tokens,
+            "config": {"workload": WORKLOAD, "tokens_per_step": tokens,
                        "note": "each step is a bounded sample of the pp512 chain"},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
@@ -1323,7 +1339,9 @@ def main(argv=None):
     ap.add_argument("--form", choices=list(FORMS), default="tc",
                     help="operand form of the chain (default: tensor-core form)")
     ap.add_argument("--cpu-tokens", type=int, default=24)
-    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--ref-tokens", type=int, default=None,
+                    help="tokens per reference step (default: sized so that the whole "
+                         "reference run takes about two minutes)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true",
                     help="measure the other configurations (8-bit and unrotated routes, MoE, "

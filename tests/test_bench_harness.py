@@ -65,3 +65,14 @@ def test_reference_arm_line():
               "higher_is_better", "cpu_baseline", "e2e"):
         assert k in line
     assert line["value"] > 0 and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_step_sizing():
+    """The reference arm's default sample keeps the whole run near its budget:
+    16 tokens a step for a short run, down to 1 token for the default 2000 steps."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.ref_tokens_for(20, 3, 0.04) == 16
+    assert bench.ref_tokens_for(2000, 20, 0.04) == 1
+    n = bench.ref_tokens_for(200, 10, 0.04)
+    assert 1 <= n <= 16 and (200 + 10) * n * 0.04 <= bench.REF_BUDGET_S

@@ -155,14 +155,6 @@ __device__ __forceinline__ void set_abort(volatile int *misc) {
     record(kStatusTimeout);
 }
 
-// every lane of a warp waits; the outcome is made warp-uniform so warp-wide
-// instructions (tcgen05.ld, votes) after it are reached by all lanes or none
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t limit,
-                                          volatile int *abort) {
-    const bool ok = mbar_wait_bounded(bar, parity, limit, abort);
-    return __all_sync(0xFFFFFFFFu, ok);
-}
-
 __device__ __forceinline__ Tile decode_tile(int t, int E, const int *s_off, const int *s_tpre,
                                             int bn) {
     int lo = 0, hi = E;  // invariant: s_tpre[lo] <= t < s_tpre[hi]

@@ -173,23 +173,6 @@ __device__ __forceinline__ void set_abort(volatile int *misc) {
     record(kStatusTimeout);
 }
 
-// A warp waits for a phase: the common case, the phase already complete for
-// every lane, costs one test and one vote (measured 2-3% faster on every pp512
-// shape than entering the bounded loop first); otherwise the bounded wait.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t limit,
-                                          volatile int *abort) {
-    uint32_t all;
-    asm volatile(
-        "{\n.reg .pred p, q;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "vote.sync.all.pred q, p, 0xffffffff;\nselp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(all)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    if (all) return true;
-    const bool ok = mbar_wait_bounded(bar, parity, limit, abort);
-    return __all_sync(0xFFFFFFFFu, ok);
-}
-
 // K-major operand in 128B-swizzled 8-row x 128-byte atoms, as TMA writes it
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     uint64_t d = 0;

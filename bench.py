@@ -46,6 +46,10 @@ WORKLOAD = ("pp512 GEMM chain, rotated 4-bit route: 512 tokens through attention
 # widened into tensor-core bytes in shared memory by the GEMM, activations in
 # tensor-core form
 FORMS = ("tc", "q4_0", "widen")
+# the tc GEMMs' workspace argument: None lets the binding split the last wave's
+# pieces along K where the schedule gains; --no-split passes False (the
+# schedule without the split, for comparison)
+TC_WS = None
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 _CSRC = os.path.join(ROOT, "hadamard_rotated_bit_gb300", "csrc")
 PROFILE_SUMMARY = {"tc": os.path.join(ROOT, "profiles", "gemm_tc_w4a4_pp512_ffn_gate_up.md"),
@@ -271,7 +275,7 @@ class Chain:
                                                      M=M_TOKENS, y=p["y"], stream=stream)
         if tc:
             return lambda: h.q4_0_x_q4_gemm_tc(p["wq"], p["wd"], p["xq"], p["xd"], M=M_TOKENS,
-                                               y=p["y"], stream=stream)
+                                               y=p["y"], stream=stream, workspace=TC_WS)
         return lambda: h.q4_0_x_q4_gemm(p["wq"], p["wd"], p["xq"], p["xd"], y=p["y"],
                                         stream=stream)
 
@@ -296,7 +300,7 @@ class Chain:
                                           y=p["y"], stream=stream)
             elif tc:
                 h.q4_0_x_q4_gemm_tc(p["wq"], p["wd"], p["xq"], p["xd"], M=M_TOKENS, y=p["y"],
-                                    stream=stream)
+                                    stream=stream, workspace=TC_WS)
             else:
                 h.q4_0_x_q4_gemm(p["wq"], p["wd"], p["xq"], p["xd"], y=p["y"], stream=stream)
             if events is not None:
@@ -494,6 +498,7 @@ def run_gpu(args):
         "dtype": "int4 codes (exact products), fp32 epilogue", "data": "synthetic",
         "config": {"workload": WORKLOAD, "tokens_per_step": M_TOKENS,
                    "operand_form": args.form,
+                   "last_wave_k_split": args.form == "tc" and not args.no_split,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: two alternating input sets of 193 MB each"},
         "roofline": roofline,
@@ -774,7 +779,7 @@ def run_only_gemm(args):
         xq, xd = h32.h32_quantize_act_q4_tc(x)
 
         def gemm():
-            h32.q4_0_x_q4_gemm_tc(wq, wd, xq, xd, M=M_TOKENS, y=y)
+            h32.q4_0_x_q4_gemm_tc(wq, wd, xq, xd, M=M_TOKENS, y=y, workspace=TC_WS)
     elif args.form == "widen":
         xq, xd = h32.h32_quantize_act_q4_tc_e5m2(x)
 
@@ -798,7 +803,8 @@ def run_only_gemm(args):
         raise RuntimeError("device status not OK")
     ms = t0.elapsed_time(t1) / args.steps
     alg = algorithmic(p, args.form)
-    return {"only_gemm": p.name, "form": args.form, "ms_per_launch": round(ms, 5),
+    return {"only_gemm": p.name, "form": args.form, "k_split": args.form == "tc" and not args.no_split,
+            "ms_per_launch": round(ms, 5),
             "eff_TOPS": round(alg["gemm_int_ops"] / (ms / 1e3) / 1e12, 1),
             "steps": args.steps, "warmup": args.warmup}
 
@@ -925,7 +931,7 @@ def suite_tiny(torch, h32, dev, stream, steps, warmup, pk):
 
         def step():
             q(x, xw=xw, xdt=xdt, stream=stream)
-            g(wp, wsc, xw, xdt, M=64, y=y, stream=stream)
+            g(wp, wsc, xw, xdt, M=64, y=y, stream=stream, workspace=TC_WS)
         ms_eager = _events_time(torch, step, steps, warmup, stream)
         # the same two launches captured once in a CUDA graph and replayed: the
         # step's device time without the binding's per-call host work between them
@@ -974,13 +980,15 @@ def suite_chain_routes(torch, h32, dev, stream, steps, warmup, pk):
             for wq, wd, x, y in bufs:
                 if route == "q8_rotated_tc":
                     xw8, xdt = h32.h32_quantize_act_q8_tc(x, rotate=rot, stream=stream)
-                    h32.q4_0_x_q8_gemm_tc(wq, wd, xw8, xdt, M=M_TOKENS, y=y, stream=stream)
+                    h32.q4_0_x_q8_gemm_tc(wq, wd, xw8, xdt, M=M_TOKENS, y=y, stream=stream,
+                                          workspace=TC_WS)
                 elif route.startswith("q8"):
                     xq, xd = h32.h32_quantize_act_q8(x, rotate=rot, stream=stream)
                     h32.q4_0_x_q8_gemm(wq, wd, xq, xd, y=y, stream=stream)
                 elif tc:
                     xw, xdt = h32.h32_quantize_act_q4_tc(x, rotate=rot, stream=stream)
-                    h32.q4_0_x_q4_gemm_tc(wq, wd, xw, xdt, M=M_TOKENS, y=y, stream=stream)
+                    h32.q4_0_x_q4_gemm_tc(wq, wd, xw, xdt, M=M_TOKENS, y=y, stream=stream,
+                                          workspace=TC_WS)
                 elif route == "q4_rotated_widen":
                     xw, xdt = h32.h32_quantize_act_q4_tc_e5m2(x, rotate=rot, stream=stream)
                     h32.q4_0_x_q4_gemm_tc_widen(wq, wd, xw, xdt, M=M_TOKENS, y=y, stream=stream)
@@ -1021,7 +1029,8 @@ def suite_rotations(torch, h32, dev, stream, steps, warmup):
         def step():
             for wp, wsc, x, y in bufs:
                 xw, xdt = h32.h32_quantize_act_q4_tc(x, rotate=rot, stream=stream)
-                h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M_TOKENS, y=y, stream=stream)
+                h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M_TOKENS, y=y, stream=stream,
+                                      workspace=TC_WS)
         ms = _events_time(torch, step, steps, warmup, stream)
         y_att = bufs[0][3][torch.from_numpy(rows).to(dev)].cpu().numpy().astype(np.float64)
         rel = float(np.linalg.norm(y_att - exact) / np.linalg.norm(exact))
@@ -1048,7 +1057,7 @@ def suite_fused_producer(torch, h32, dev, stream, steps, warmup):
     xnd = torch.zeros((p.N // 32, M_TOKENS), dtype=torch.float32, device=dev)
 
     def separate():
-        h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M_TOKENS, y=y, stream=stream)
+        h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M_TOKENS, y=y, stream=stream, workspace=TC_WS)
         h32.h32_quantize_act_q4_tc(y, xw=xn, xdt=xnd, stream=stream)
 
     def fused_y():
@@ -1060,7 +1069,7 @@ def suite_fused_producer(torch, h32, dev, stream, steps, warmup):
                                          xdt_next=xnd, stream=stream)
 
     def gemm_alone():
-        h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M_TOKENS, y=y, stream=stream)
+        h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M_TOKENS, y=y, stream=stream, workspace=TC_WS)
     out = {}
     for name, fn in (("gemm_alone", gemm_alone), ("separate", separate), ("fused_with_y", fused_y),
                      ("fused", fused)):
@@ -1255,7 +1264,8 @@ def suite_long(torch, h32, dev, stream, steps, warmup, pk):
                 m = min(mb, M - s0)
                 for (wp, wsc), x, y in zip(weights, xs, ys):
                     xw, xdt = h32.h32_quantize_act_q4_tc(x[s0:s0 + m], stream=stream)
-                    h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=m, y=y[:m], stream=stream)
+                    h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=m, y=y[:m], stream=stream,
+                                          workspace=TC_WS)
         ms = _events_time(torch, step, max(1, steps // max(1, M // 1024)), max(1, warmup // 4),
                           stream)
         ints, alu, nbytes = 0, 0, 0
@@ -1343,6 +1353,8 @@ def main(argv=None):
                     help="tokens per reference step (default: sized so that the whole "
                          "reference run takes about two minutes)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-split", action="store_true",
+                    help="tc GEMMs without the K split of the last wave (schedule comparison)")
     ap.add_argument("--suite", action="store_true",
                     help="measure the other configurations (8-bit and unrotated routes, MoE, "
                          "long prompts, streaming quantizer), one JSON line each")
@@ -1361,6 +1373,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    global TC_WS
+    TC_WS = False if args.no_split else None
     if args.peaks:
         for ln in run_peaks(args):
             print(json.dumps(ln), flush=True)

@@ -61,6 +61,12 @@ _SIGS = {
                                             _I64, _P, _P, _I64, _INT, _P]),
     "h32_quantize_act_q8_tc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _I64, _INT, _P]),
     "q4_0_x_q8_gemm_tc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P]),
+    "h32_gemm_tc_workspace_bytes": (_INT, [_I64, _I64, _I64, ctypes.POINTER(ctypes.c_size_t)]),
+    "h32_gemm_tc_schedule": (_INT, [_I64, _I64, _I64, _I32, _I32, ctypes.POINTER(ctypes.c_int64)]),
+    "q4_0_x_q4_gemm_tc_ws": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P,
+                                    _P, ctypes.c_size_t, _P]),
+    "q4_0_x_q8_gemm_tc_ws": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P,
+                                    _P, ctypes.c_size_t, _P]),
     "h32_q4_0_blocks_to_planes": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "h32_q4_0_planes_to_blocks": (_INT, [_P, _P, _I64, _I64, _P, _P]),
     "h32_quantize_act_q4_tc_e5m2": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _I64, _INT, _P]),
@@ -473,14 +479,68 @@ def h32_prepack_weights_q4_0_tc(wq, wd, wp=None, wsc=None, stream=None):
     return wp, wsc
 
 
-def q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=None, y=None, block_sums=None, stream=None):
-    """The W4A4 product on tc-form operands (bit-identical to q4_0_x_q4_gemm)."""
-    return _gemm_tc("q4_0_x_q4_gemm_tc", wp, wsc, xw, xdt, M, y, block_sums, stream)
+def q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=None, y=None, block_sums=None, stream=None,
+                      workspace=None):
+    """The W4A4 product on tc-form operands (bit-identical to q4_0_x_q4_gemm).
+
+    workspace: None (default) lets shapes whose schedule splits the last wave's
+    pieces along K use a workspace the binding keeps per device and stream; False
+    calls q4_0_x_q4_gemm_tc (no split); a uint8 CUDA tensor (zero-filled before
+    its first use, used by one call at a time) is passed as given."""
+    return _gemm_tc("q4_0_x_q4_gemm_tc", wp, wsc, xw, xdt, M, y, block_sums, stream, workspace)
 
 
-def q4_0_x_q8_gemm_tc(wp, wsc, xw8, xdt, M=None, y=None, block_sums=None, stream=None):
-    """The W4A8 product on tc-form operands (bit-identical to q4_0_x_q8_gemm)."""
-    return _gemm_tc("q4_0_x_q8_gemm_tc", wp, wsc, xw8, xdt, M, y, block_sums, stream)
+def q4_0_x_q8_gemm_tc(wp, wsc, xw8, xdt, M=None, y=None, block_sums=None, stream=None,
+                      workspace=None):
+    """The W4A8 product on tc-form operands (bit-identical to q4_0_x_q8_gemm);
+    workspace as for q4_0_x_q4_gemm_tc."""
+    return _gemm_tc("q4_0_x_q8_gemm_tc", wp, wsc, xw8, xdt, M, y, block_sums, stream, workspace)
+
+
+def h32_gemm_tc_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Workspace bytes q4_0_x_q4_gemm_tc_ws / q4_0_x_q8_gemm_tc_ws use for an
+    M x N x K product on the current device (0: the schedule does not split)."""
+    n = ctypes.c_size_t(0)
+    _check("h32_gemm_tc_workspace_bytes",
+           lib().h32_gemm_tc_workspace_bytes(int(M), int(N), int(K), ctypes.byref(n)))
+    return int(n.value)
+
+
+TC_SCHEDULE_KEYS = ("bn", "tail_k", "tail_first", "total", "grid", "split_p", "split_kh",
+                    "ws_ld", "ws_bytes")
+
+
+def h32_gemm_tc_schedule(M: int, N: int, K: int, sms: int, with_workspace: bool = True) -> dict:
+    """The dense tc GEMM's schedule for an M x N x K product on `sms` SMs (host
+    arithmetic, no device): tile width, the cut and the K split of the last wave."""
+    out = (ctypes.c_int64 * 9)()
+    _check("h32_gemm_tc_schedule", lib().h32_gemm_tc_schedule(int(M), int(N), int(K), int(sms),
+                                                             int(bool(with_workspace)), out))
+    return dict(zip(TC_SCHEDULE_KEYS, (int(v) for v in out)))
+
+
+# workspaces kept per (device, stream); a grown workspace keeps the old one
+# alive, since a captured CUDA graph may still use it
+_workspaces = {}
+_retired_workspaces = []
+
+
+def _workspace_for(M, N, K, dev, stream):
+    torch = _torch()
+    need = h32_gemm_tc_workspace_bytes(M, N, K)
+    if need == 0:
+        return None
+    if torch.cuda.is_current_stream_capturing():
+        # inside a capture: a workspace of the graph's own, zeroed on every replay
+        return torch.zeros(need, dtype=torch.uint8, device=dev)
+    key = (dev.index, _stream(stream).value)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        if ws is not None:
+            _retired_workspaces.append(ws)
+        ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+        _workspaces[key] = ws
+    return ws
 
 
 def _tc_operands(wp, wsc, xw, xdt, rows, bytes_per_code, weight_rows=None):
@@ -497,7 +557,7 @@ def _tc_operands(wp, wsc, xw, xdt, rows, bytes_per_code, weight_rows=None):
     return N, K
 
 
-def _gemm_tc(fn, wp, wsc, xw, xdt, M, y, block_sums, stream):
+def _gemm_tc(fn, wp, wsc, xw, xdt, M, y, block_sums, stream, workspace=False):
     torch = _torch()
     if M is None:
         M = xw.shape[0]
@@ -509,8 +569,21 @@ def _gemm_tc(fn, wp, wsc, xw, xdt, M, y, block_sums, stream):
     ldy = _rows(y, "y")
     S = _sums(block_sums, M, N, K // 32, dev)
     _same_gpu(("wp", wp), ("wsc", wsc), ("xw", xw), ("xdt", xdt), ("y", y), ("S", S))
-    st = getattr(lib(), fn)(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt), xdt.shape[1],
-                            M, N, K, _ptr(y), ldy, _ptr(S), _stream(stream))
+    ws = None
+    if workspace is None and S is None and M > 0:
+        ws = _workspace_for(M, N, K, dev, stream)
+    elif workspace is not None and workspace is not False:
+        _need(workspace, "workspace", (torch.uint8,), (_ge(0),))
+        _same_gpu(("wp", wp), ("workspace", workspace))
+        ws = workspace
+    if ws is None:
+        st = getattr(lib(), fn)(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt),
+                                xdt.shape[1], M, N, K, _ptr(y), ldy, _ptr(S), _stream(stream))
+    else:
+        fn = fn + "_ws"
+        st = getattr(lib(), fn)(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt),
+                                xdt.shape[1], M, N, K, _ptr(y), ldy, _ptr(S), _ptr(ws),
+                                ws.numel(), _stream(stream))
     _check(fn, st)
     return (y, S) if S is not None else y
 

@@ -88,6 +88,7 @@ constexpr int kBufs = 4 / kGroup;          // hand-off buffers in TMEM (4 blocks
 constexpr int kTmemCols = 512;       // kBufs hand-off buffers x kGroup blocks x 128 columns
 constexpr uint64_t kDrainPolls = 1ull << 22;
 constexpr int kMaxExperts = 1024;
+constexpr int kSplitMaxP = 128;      // pieces of a K split (flags in the workspace)
 
 // XB = 4: one activation byte per code.  XB = 8: two bytes per code, the e4m3
 // bytes of 16 h and of l where the 8-bit code is 16 h + l (0 <= l <= 15), so a
@@ -153,6 +154,13 @@ struct TcArgs {
     // dense only: tiles from tail_first on (the last partial wave) are each cut
     // into tail_k pieces along the tokens; tail_k = 1 cuts nothing
     int32_t tail_first, tail_k;
+    // dense only, the K split of the cut pieces (split_p pieces, 0 = none):
+    // the first split_kh K stages of piece p run on CTA p, the rest on CTA
+    // split_p + p; the partial sums pass through the caller's workspace (a
+    // header, ws_flag[p][16], ws_acc[p][128][ws_ld])
+    unsigned long long *ws_hdr, *ws_flag;
+    float *ws_acc;
+    int32_t split_p, split_kh, ws_ld;
     uint64_t wait_limit;
 };
 
@@ -250,6 +258,78 @@ __device__ __forceinline__ TcTile tc_tile(int t, const TcArgs &a, const int *s_o
     return ti;
 }
 
+// The CTA's work items in order.  Without the K split: tiles t = blockIdx.x,
+// + gridDim.x, ... below `total`, every K stage.  With it, each cut piece of the
+// last partial wave runs in two parts along K on two CTAs: CTA p < split_p
+// starts with stages [0, split_kh) of piece p and leaves its partial sums in the
+// workspace (mode 1), CTA split_p + p ends with stages [split_kh, nst) of piece
+// p, starting from those sums (mode 2), and the uncut tiles t < tail_first go
+// round robin in between (mode 0).  Every output still takes its blocks in
+// order: the second part continues the first part's accumulators.
+struct TcItem {
+    int t, st0, st1, mode;
+};
+
+template <bool kSplit>
+__device__ __forceinline__ int tc_item_count(const TcArgs &a, int total) {
+    const int b = blockIdx.x, g = gridDim.x;
+    if constexpr (kSplit) {
+        if (a.split_p > 0) {
+            const int main = b < a.tail_first ? (a.tail_first - 1 - b) / g + 1 : 0;
+            return main + (b < a.split_p ? 1 : 0) + (b >= a.split_p && b < 2 * a.split_p ? 1 : 0);
+        }
+    }
+    return b < total ? (total - 1 - b) / g + 1 : 0;
+}
+
+template <bool kSplit>
+__device__ __forceinline__ TcItem tc_item(const TcArgs &a, int k, int nst) {
+    const int b = blockIdx.x, g = gridDim.x;
+    if constexpr (kSplit) {
+        if (a.split_p > 0) {
+            if (b < a.split_p) {
+                if (k == 0) return TcItem{a.tail_first + b, 0, a.split_kh, 1};
+                --k;
+            }
+            const int t = b + k * g;
+            if (t < a.tail_first) return TcItem{t, 0, nst, 0};
+            return TcItem{a.tail_first + b - a.split_p, a.split_kh, nst, 2};
+        }
+    }
+    return TcItem{b + k * g, 0, nst, 0};
+}
+
+// The handoff of a split piece's partial sums between the two CTAs, per
+// epilogue warp (its 32 rows x its columns of the piece): the first part stores
+// its accumulators and then, after a fence, the launch's generation number in
+// its flag (release); the second part waits for that number (acquire, bounded)
+// and loads them.  The launch's number is the workspace header's value plus
+// one; the header changes only when the last CTA to finish advances it, so
+// flags left by an earlier launch (or a replay of the same graph node) never
+// match.
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_cg_v2(uint64_t *p, uint64_t x, uint64_t y) {
+    asm volatile("st.global.cg.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(x), "l"(y) : "memory");
+}
+__device__ __forceinline__ void ld_cg_v2(const uint64_t *p, uint64_t &x, uint64_t &y) {
+    asm volatile("ld.global.cg.v2.b64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
+}
+
 // The weight scales of the thread's row for the four blocks of K stage `st`
 // held in shared-memory stage `s`: fp32 [128 rows][4] from the repacked form,
 // or (widening instance) fp16 [128 rows][8], the scales of stages st & ~1 and
@@ -272,141 +352,228 @@ __device__ __forceinline__ void stage_dw(const float *s_sa, int s, int row, int 
     }
 }
 
-// The epilogue of one warp over all of its tiles, without block sums: ring
-// positions of the shared-memory stages and TMEM buffers are carried as
-// counters and phase bits, arrivals come from one elected lane.  Returns false
-// when a wait gave up.  A warp holds its lane quarter's 32 weight rows (one a
-// thread, the 32x32b TMEM fragment) times its share of the tile's columns.
-template <int EPQ, int XB, bool kQN, bool kTail, bool kWQ>
-__device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const int *s_off,
-                                               const int *s_tpre, uint64_t *bars, const float *s_sa,
-                                               const float *s_sb, float *s_q, uint32_t tmem,
-                                               int warp, int lane, volatile int *abort_flag) {
+// The ring positions of an epilogue warp: shared-memory stage and TMEM buffer,
+// each a counter and a phase bit.
+struct EpiRing {
+    uint32_t s, sph, gb, gph;
+};
+
+// One work item of an epilogue warp, without block sums: tile (or piece) t,
+// K stages [st0, st0 + nstage).  kMode 0: the whole K range, from zero, to y;
+// 1: the first part of a split piece, its accumulators to the workspace; 2: the
+// second part, starting from the first part's accumulators, to y.  Arrivals
+// come from one elected lane.  Returns false when a wait gave up.  A warp holds
+// its lane quarter's 32 weight rows (one a thread, the 32x32b TMEM fragment)
+// times its share of the tile's columns.
+template <int EPQ, int XB, bool kQN, bool kTail, bool kWQ, int kMode>
+__device__ __forceinline__ bool epi_item(const TcArgs &a, int t, int st0, int nstage,
+                                         const int *s_off, const int *s_tpre, uint64_t *bars,
+                                         const float *s_sa, const float *s_sb, float *s_q,
+                                         uint32_t tmem, int warp, int lane,
+                                         volatile int *abort_flag, EpiRing &r) {
     using C = TcCfg<EPQ, XB, kQN, kWQ>;
     const int ew = warp - C::kProdWarps;
     const int quad = warp & 3;                 // TMEM lanes 32 quad .. 32 quad + 31
     const int part = ew >> 2;                  // share of the columns
     const int row = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    const int nst = a.nb / 4;
     const uint64_t lim = a.wait_limit;
-    uint32_t s = 0, sph = 0, gb = 0, gph = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const TcTile ti = tc_tile<kTail>(t, a, s_off, s_tpre);
-        if (kTail && ti.ncols == 0) continue;   // an empty piece: no role touches it
-        const int n16 = ti.ncols >> 4;
-        const int base = n16 / EPQ, rem = n16 % EPQ;
-        const int nch = base + (part < rem ? 1 : 0);
-        const int c0 = 16 * (part * base + min(part, rem));
-        const uint32_t tcol_base = tmem + lane_addr + c0;
-        uint64_t acc[8 * C::kMaxChunks];
+    const TcTile ti = tc_tile<kTail>(t, a, s_off, s_tpre);
+    if (kTail && ti.ncols == 0) return true;   // an empty piece: no role touches it
+    const int n16 = ti.ncols >> 4;
+    const int base = n16 / EPQ, rem = n16 % EPQ;
+    const int nch = base + (part < rem ? 1 : 0);
+    const int c0 = 16 * (part * base + min(part, rem));
+    const uint32_t tcol_base = tmem + lane_addr + c0;
+    uint64_t acc[8 * C::kMaxChunks];
 #pragma unroll
-        for (int i = 0; i < 8 * C::kMaxChunks; ++i) acc[i] = 0ull;
-        for (int st = 0; st < nst; ++st) {
-            if (!warp_wait(&bars[kBarFull + s], sph, lim, abort_flag)) return false;
-            float dws[4];
-            stage_dw<kWQ>(s_sa, s, row, st, dws);
-            const float *sb = s_sb + s * (kScaleBytes / 4) + c0;   // [4 blocks][bn tokens]
-#pragma unroll
-            for (int j0 = 0; j0 < 4; j0 += kGroup) {
-                if (!warp_wait(&bars[kBarSFull + gb], gph, lim, abort_flag)) return false;
-                tc_fence_after();
-                const uint32_t tcol0 = tcol_base + gb * (kGroup * 128);
-                // one 16-column chunk of one block per TMEM wait (measured: fewer
-                // live load registers beat fewer waits, and every reordering that
-                // overlaps loads with folds measured slower); every accumulator
-                // takes the blocks in order
-#pragma unroll
-                for (int c = 0; c < C::kMaxChunks; ++c) {
-                    if (c < nch) {
-#pragma unroll
-                        for (int i = 0; i < kGroup; ++i) {
-                            uint32_t v[16];
-                            tmem_ld_x16(tcol0 + i * 128 + c * 16, v);
-                            tmem_ld_wait();
-                            fold16(acc + 8 * c, dws[j0 + i], sb + (j0 + i) * a.bn + 16 * c, v);
-                        }
-                    }
-                }
-                // the warp-wide wait above: every lane's TMEM reads of the buffer are done
-                tc_fence_before();
-                elect_arrive(&bars[kBarSEmpty + gb]);
-                if (++gb == kBufs) {
-                    gb = 0;
-                    gph ^= 1;
-                }
+    for (int i = 0; i < 8 * C::kMaxChunks; ++i) acc[i] = 0ull;
+    if constexpr (kMode == 2) {
+        if (nch > 0) {
+            // the first part's accumulators, once its flag holds this launch's number
+            const int p = t - a.tail_first;
+            const unsigned long long *flag = a.ws_flag + p * 16 + ew;
+            uint64_t polls = 0;
+            const unsigned long long want = ld_relaxed_u64(a.ws_hdr) + 1;
+            while (!__all_sync(0xFFFFFFFFu, ld_acquire_u64(flag) == want)) {
+                if (++polls > lim || *abort_flag) return false;
             }
-            __syncwarp();
-            elect_arrive(&bars[kBarEmpty + s]);
-            if (++s == C::kStages) {
-                s = 0;
-                sph ^= 1;
-            }
-        }
-        const int64_t n = ti.n0 + row;
-        if (n < a.N && (!kQN || a.y)) {
+            const uint64_t *src = reinterpret_cast<const uint64_t *>(
+                a.ws_acc + (static_cast<int64_t>(p) * kBM + row) * a.ws_ld + c0);
 #pragma unroll
             for (int c = 0; c < C::kMaxChunks; ++c) {
                 if (c < nch) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int col = c0 + c * 16 + 2 * q;
-                        const uint64_t pr = acc[8 * c + q];
-                        if (col >= ti.clo && col < ti.chi)
-                            a.y[(ti.g0 + col) * a.ldy + n] = __uint_as_float(static_cast<uint32_t>(pr));
-                        if (col + 1 >= ti.clo && col + 1 < ti.chi)
-                            a.y[(ti.g0 + col + 1) * a.ldy + n] =
-                                __uint_as_float(static_cast<uint32_t>(pr >> 32));
-                    }
+                    for (int q = 0; q < 8; q += 2)
+                        ld_cg_v2(src + 8 * c + q, acc[8 * c + q], acc[8 * c + q + 1]);
                 }
             }
         }
-        // the output quantized for the next projection.  The warp's 32 lanes are 32
-        // consecutive output features, one 32-block of the next projection's input
-        // for every token column (N % 32 == 0: a block is all inside or all outside
-        // the N rows).  The warp turns its 32 rows x 32 columns around through a
-        // 4 KB staging tile (16-byte chunks of a column XOR-swizzled by the column,
-        // so writes and reads are free of bank conflicts); then lane t holds token
-        // column t's whole block and rotates and quantizes it in registers, the
-        // step the activation quantizer takes, with the same arithmetic.
-        if constexpr (kQN) {
-            float *stg = s_q + (warp - C::kProdWarps) * 1024;
+    }
+    for (int si = 0; si < nstage; ++si) {
+        const int st = st0 + si;
+        if (!warp_wait(&bars[kBarFull + r.s], r.sph, lim, abort_flag)) return false;
+        float dws[4];
+        stage_dw<kWQ>(s_sa, r.s, row, st, dws);
+        const float *sb = s_sb + r.s * (kScaleBytes / 4) + c0;   // [4 blocks][bn tokens]
+#pragma unroll
+        for (int j0 = 0; j0 < 4; j0 += kGroup) {
+            if (!warp_wait(&bars[kBarSFull + r.gb], r.gph, lim, abort_flag)) return false;
+            tc_fence_after();
+            const uint32_t tcol0 = tcol_base + r.gb * (kGroup * 128);
+            // one 16-column chunk of one block per TMEM wait (measured: fewer
+            // live load registers beat fewer waits, and every reordering that
+            // overlaps loads with folds measured slower); every accumulator
+            // takes the blocks in order
 #pragma unroll
             for (int c = 0; c < C::kMaxChunks; ++c) {
                 if (c < nch) {
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const int t = c * 16 + q;
-                        const uint64_t pr = acc[8 * c + (q >> 1)];
-                        stg[t * 32 + ((((lane >> 2) ^ (t & 7))) << 2) + (lane & 3)] =
-                            __uint_as_float(static_cast<uint32_t>(pr >> (32 * (q & 1))));
+                    for (int i = 0; i < kGroup; ++i) {
+                        uint32_t v[16];
+                        tmem_ld_x16(tcol0 + i * 128 + c * 16, v);
+                        tmem_ld_wait();
+                        fold16(acc + 8 * c, dws[j0 + i], sb + (j0 + i) * a.bn + 16 * c, v);
                     }
                 }
             }
-            __syncwarp();
-            const int col = c0 + lane;
-            if (lane < 16 * nch && col >= ti.clo && col < ti.chi && ti.n0 + quad * 32 < a.N) {
-                float v[32];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float4 f = *reinterpret_cast<const float4 *>(
-                        stg + lane * 32 + ((k ^ (lane & 7)) << 2));
-                    v[4 * k] = f.x;
-                    v[4 * k + 1] = f.y;
-                    v[4 * k + 2] = f.z;
-                    v[4 * k + 3] = f.w;
-                }
-                if (a.qn_rot) rotate32(v);
-                uint32_t w[8];
-                const float d = quant_block_tc4(v, w);
-                const int64_t g = ti.g0 + col;
-                uint4 *dst = reinterpret_cast<uint4 *>(a.qn + g * a.N + ti.n0 + quad * 32);
-                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                a.qnd[((ti.n0 + quad * 32) >> 5) * a.ldqnd + g] = d;
+            // the warp-wide wait above: every lane's TMEM reads of the buffer are done
+            tc_fence_before();
+            elect_arrive(&bars[kBarSEmpty + r.gb]);
+            if (++r.gb == kBufs) {
+                r.gb = 0;
+                r.gph ^= 1;
             }
-            __syncwarp();   // the staging tile is free for the next tile
         }
+        __syncwarp();
+        elect_arrive(&bars[kBarEmpty + r.s]);
+        if (++r.s == C::kStages) {
+            r.s = 0;
+            r.sph ^= 1;
+        }
+    }
+    if constexpr (kMode == 1) {
+        // the first part of a piece: its accumulators to the workspace, then the flag
+        if (nch > 0) {
+            const int p = t - a.tail_first;
+            uint64_t *dst = reinterpret_cast<uint64_t *>(
+                a.ws_acc + (static_cast<int64_t>(p) * kBM + row) * a.ws_ld + c0);
+#pragma unroll
+            for (int c = 0; c < C::kMaxChunks; ++c) {
+                if (c < nch) {
+#pragma unroll
+                    for (int q = 0; q < 8; q += 2)
+                        st_cg_v2(dst + 8 * c + q, acc[8 * c + q], acc[8 * c + q + 1]);
+                }
+            }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_u64(a.ws_flag + p * 16 + ew, ld_relaxed_u64(a.ws_hdr) + 1);
+        }
+        return true;
+    }
+    const int64_t n = ti.n0 + row;
+    if (n < a.N && (!kQN || a.y)) {
+#pragma unroll
+        for (int c = 0; c < C::kMaxChunks; ++c) {
+            if (c < nch) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int col = c0 + c * 16 + 2 * q;
+                    const uint64_t pr = acc[8 * c + q];
+                    if (col >= ti.clo && col < ti.chi)
+                        a.y[(ti.g0 + col) * a.ldy + n] = __uint_as_float(static_cast<uint32_t>(pr));
+                    if (col + 1 >= ti.clo && col + 1 < ti.chi)
+                        a.y[(ti.g0 + col + 1) * a.ldy + n] =
+                            __uint_as_float(static_cast<uint32_t>(pr >> 32));
+                }
+            }
+        }
+    }
+    // the output quantized for the next projection.  The warp's 32 lanes are 32
+    // consecutive output features, one 32-block of the next projection's input
+    // for every token column (N % 32 == 0: a block is all inside or all outside
+    // the N rows).  The warp turns its 32 rows x 32 columns around through a
+    // 4 KB staging tile (16-byte chunks of a column XOR-swizzled by the column,
+    // so writes and reads are free of bank conflicts); then lane t holds token
+    // column t's whole block and rotates and quantizes it in registers, the
+    // step the activation quantizer takes, with the same arithmetic.
+    if constexpr (kQN) {
+        float *stg = s_q + (warp - C::kProdWarps) * 1024;
+#pragma unroll
+        for (int c = 0; c < C::kMaxChunks; ++c) {
+            if (c < nch) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int t = c * 16 + q;
+                    const uint64_t pr = acc[8 * c + (q >> 1)];
+                    stg[t * 32 + ((((lane >> 2) ^ (t & 7))) << 2) + (lane & 3)] =
+                        __uint_as_float(static_cast<uint32_t>(pr >> (32 * (q & 1))));
+                }
+            }
+        }
+        __syncwarp();
+        const int col = c0 + lane;
+        if (lane < 16 * nch && col >= ti.clo && col < ti.chi && ti.n0 + quad * 32 < a.N) {
+            float v[32];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float4 f = *reinterpret_cast<const float4 *>(
+                    stg + lane * 32 + ((k ^ (lane & 7)) << 2));
+                v[4 * k] = f.x;
+                v[4 * k + 1] = f.y;
+                v[4 * k + 2] = f.z;
+                v[4 * k + 3] = f.w;
+            }
+            if (a.qn_rot) rotate32(v);
+            uint32_t w[8];
+            const float d = quant_block_tc4(v, w);
+            const int64_t g = ti.g0 + col;
+            uint4 *dst = reinterpret_cast<uint4 *>(a.qn + g * a.N + ti.n0 + quad * 32);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            a.qnd[((ti.n0 + quad * 32) >> 5) * a.ldqnd + g] = d;
+        }
+        __syncwarp();   // the staging tile is free for the next tile
+    }
+    return true;
+}
+
+// The epilogue of one warp over all of the CTA's work items (TcItem): the
+// uncut tiles and pieces, each over the whole K range, in one loop (measured:
+// a loop over items whose K range is a variable made every tile of the
+// instance about 6% slower), the two parts of a split piece before and after
+// it.
+template <int EPQ, int XB, bool kQN, bool kTail, bool kWQ, bool kSplit>
+__device__ __forceinline__ bool epilogue_tiles(const TcArgs &a, int total, const int *s_off,
+                                               const int *s_tpre, uint64_t *bars, const float *s_sa,
+                                               const float *s_sb, float *s_q, uint32_t tmem,
+                                               int warp, int lane, volatile int *abort_flag) {
+    const int b = blockIdx.x, g = gridDim.x;
+    const int nst = a.nb / 4;
+    EpiRing r{0u, 0u, 0u, 0u};
+    int main_end = total;
+    if constexpr (kSplit) {
+        if (a.split_p > 0) {
+            main_end = a.tail_first;
+            if (b < a.split_p &&
+                !epi_item<EPQ, XB, kQN, kTail, kWQ, 1>(a, a.tail_first + b, 0, a.split_kh, s_off,
+                                                        s_tpre, bars, s_sa, s_sb, s_q, tmem, warp,
+                                                        lane, abort_flag, r))
+                return false;
+        }
+    }
+    const int nit = b < main_end ? (main_end - 1 - b) / g + 1 : 0;
+    for (int k = 0; k < nit; ++k)
+        if (!epi_item<EPQ, XB, kQN, kTail, kWQ, 0>(a, b + k * g, 0, nst, s_off, s_tpre, bars, s_sa,
+                                                    s_sb, s_q, tmem, warp, lane, abort_flag, r))
+            return false;
+    if constexpr (kSplit) {
+        if (a.split_p > 0 && b >= a.split_p && b < 2 * a.split_p &&
+            !epi_item<EPQ, XB, kQN, kTail, kWQ, 2>(a, a.tail_first + b - a.split_p, a.split_kh,
+                                                    nst - a.split_kh, s_off, s_tpre, bars, s_sa,
+                                                    s_sb, s_q, tmem, warp, lane, abort_flag, r))
+            return false;
     }
     return true;
 }
@@ -464,12 +631,16 @@ __device__ __forceinline__ bool widen_tiles(const TcArgs &a, int total, const in
 // kEpi: 0 = y only, 1 = y and the block sums, 2 = y (optional) and the output
 // quantized for the next projection.  kTail: the last partial wave's tiles are
 // cut into pieces (TcArgs::tail_first, tail_k).  kWQ: the widening instance
-// (map_a over the Q4_0 nibbles, map_sa over the fp16 scales).
-template <int EPQ, int XB, int kEpi, bool kTail = false, bool kWQ = false>
+// (map_a over the Q4_0 nibbles, map_sa over the fp16 scales).  kSplit: the cut
+// pieces also run in two parts along K (TcArgs::split_p, TcItem); an instance
+// of its own, as the cut instance without that code measured about 4% faster
+// on GB300.
+template <int EPQ, int XB, int kEpi, bool kTail = false, bool kWQ = false, bool kSplit = false>
 __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2, kWQ>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_sa,
                    const __grid_constant__ CUtensorMap map_sb, const TcArgs a) {
+    static_assert(!kSplit || (kTail && kEpi == 0 && !kWQ), "the K split: plain output, cut tail");
     using C = TcCfg<EPQ, XB, kEpi == 2, kWQ>;
     constexpr int kStages = C::kStages;
     constexpr bool kSums = kEpi == 1;
@@ -572,7 +743,7 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2, kWQ>::kThreads, 1)
         return;
     }
     const int total = misc[kMiscTotal];
-    if (static_cast<int>(blockIdx.x) >= total) return;
+    if (a.split_p == 0 && static_cast<int>(blockIdx.x) >= total) return;
     if (warp == 1) {
         __syncwarp();
         tmem_alloc(reinterpret_cast<uint32_t *>(const_cast<int *>(&misc[kMiscTmem])), kTmemCols);
@@ -594,10 +765,12 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2, kWQ>::kThreads, 1)
             prefetch_tmap(&map_sb);
             uint32_t ks = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TcTile ti = tc_tile<kTail>(t, a, s_off, s_tpre);
+            const int nit = tc_item_count<kSplit>(a, total);
+            for (int k = 0; k < nit && ok; ++k) {
+                const TcItem it = tc_item<kSplit>(a, k, nst);
+                const TcTile ti = tc_tile<kTail>(it.t, a, s_off, s_tpre);
                 if (kTail && ti.ncols == 0) continue;
-                for (int st = 0; st < nst; ++st, ++ks) {
+                for (int st = it.st0; st < it.st1; ++st, ++ks) {
                     const int s = ks % kStages;
                     if (!mbar_wait_bounded(&bars[kBarEmpty + s], ((ks / kStages) & 1) ^ 1, lim,
                                            abort_flag)) {
@@ -634,12 +807,14 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2, kWQ>::kThreads, 1)
         if (lane == 0) {
             uint32_t ks = 0, kg = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TcTile ti = tc_tile<kTail>(t, a, s_off, s_tpre);
+            const int nit = tc_item_count<kSplit>(a, total);
+            for (int k = 0; k < nit && ok; ++k) {
+                const TcItem it = tc_item<kSplit>(a, k, nst);
+                const TcTile ti = tc_tile<kTail>(it.t, a, s_off, s_tpre);
                 if (kTail && ti.ncols == 0) continue;
                 const uint32_t idesc =
                     kWQ ? idesc_e4m3_e5m2_f32(kBM, ti.ncols) : idesc_e4m3_f32(kBM, ti.ncols);
-                for (int st = 0; st < nst && ok; ++st, ++ks) {
+                for (int st = it.st0; st < it.st1 && ok; ++st, ++ks) {
                     const int s = ks % kStages;
                     // the widening instance's weight tile is ready once the widening
                     // warps, which waited for the stage themselves, have written it
@@ -704,8 +879,8 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2, kWQ>::kThreads, 1)
     } else if constexpr (!kSums) {
         // ------------------------------------------------------- epilogue
         if constexpr (C::kRegSplit) reg_alloc<C::kEpiRegs>();
-        if (!epilogue_tiles<EPQ, XB, kEpi == 2, kTail, kWQ>(a, total, s_off, s_tpre, bars, s_sa,
-                                                            s_sb, s_q, tmem, warp, lane, abort_flag))
+        if (!epilogue_tiles<EPQ, XB, kEpi == 2, kTail, kWQ, kSplit>(
+                a, total, s_off, s_tpre, bars, s_sa, s_sb, s_q, tmem, warp, lane, abort_flag))
             set_abort(misc);
     } else {
         // ------------------------------------ epilogue with block sums
@@ -815,6 +990,20 @@ __global__ void __launch_bounds__(TcCfg<EPQ, XB, kEpi == 2, kWQ>::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    if constexpr (kSplit) {
+        // the last CTA to finish advances the generation: the header holds this
+        // launch's number until then (every CTA reads it before it counts itself
+        // done)
+        if (tid == 0 && a.ws_hdr) {
+            unsigned int *done = reinterpret_cast<unsigned int *>(a.ws_hdr + 1);
+            __threadfence();
+            if (atomicAdd(done, 1u) == gridDim.x - 1) {
+                *done = 0u;
+                st_relaxed_u64(a.ws_hdr, ld_relaxed_u64(a.ws_hdr) + 1);
+                __threadfence();
+            }
+        }
+    }
 }
 
 // ----------------------------------------------------------------------------
@@ -865,6 +1054,9 @@ h32_status make_map(CUtensorMap *map, CUtensorMapDataType type, int esize, const
 struct TcPlan {
     int bn, tail_k;
     int64_t tail_first, total, grid;
+    // the K split of the cut pieces (split_p = 0: none): pieces split_p,
+    // stages [0, split_kh) first, piece width (the workspace's row stride) ws_ld
+    int64_t split_p = 0, split_kh = 0, ws_ld = 0;
 };
 
 // a tile costs its MMA width plus a fixed part that is about the work of 80
@@ -882,59 +1074,90 @@ inline int64_t width_factor(int bn) {   // percent
     }
 }
 
-inline int64_t plan_makespan(int64_t M, int64_t nt, int sms, int bn, int k, TcPlan *plan) {
+// The simulated makespan of a plan, in tile-cost units times the nst K stages
+// (a piece run in two parts costs its share of the stages in each).  With
+// `split`, every cut piece runs in two parts (TcItem); that needs a full wave
+// of uncut tiles (so the second part of a piece starts after its first part
+// has ended) and two CTAs a piece; returns -1 where a plan does not apply.
+inline int64_t plan_makespan(int64_t M, int64_t nt, int sms, int bn, int k, int64_t nst,
+                             bool split, TcPlan *plan) {
     const int64_t chunks = (M + bn - 1) / bn;
     const int64_t T = nt * chunks;
     const int64_t r = T % sms;   // tiles of the last partial wave
-    const int64_t tail_first = (k > 1 && r > 0) ? T - r : T;
+    const int64_t tail_first = ((k > 1 || split) && r > 0) ? T - r : T;
     const int64_t total = tail_first + (T - tail_first) * k;
     const int64_t grid = total < sms ? total : sms;
+    const int64_t P = total - tail_first;   // cut pieces
+    const int64_t kh = nst / 2;
+    if (split && (P == 0 || P > kSplitMaxP || 2 * P > grid || tail_first < grid || kh < 1)) return -1;
     auto width = [&](int64_t t) {
         const int64_t ch = t % chunks;
         return ch == chunks - 1 ? M - ch * bn : static_cast<int64_t>(bn);
     };
+    int64_t pw_max = 0;
+    auto piece_cost = [&](int64_t p) {   // piece p of the cut tiles
+        const int64_t sub = p % k;
+        const int64_t w = width(tail_first + p / k);
+        const int64_t pw = ((w + k - 1) / k + 15) / 16 * 16;
+        const int64_t wp = w - sub * pw < pw ? w - sub * pw : pw;
+        if (pw > pw_max) pw_max = pw;
+        return tile_cost(wp > 0 ? wp : 0);
+    };
     int64_t worst = 0;
     for (int64_t c = 0; c < grid; ++c) {
         int64_t cost = 0;
-        for (int64_t t = c; t < total; t += grid) {
-            if (t < tail_first) {
-                cost += tile_cost(width(t));
-            } else {
-                const int64_t p = t - tail_first, sub = p % k;
-                const int64_t w = width(tail_first + p / k);
-                const int64_t pw = ((w + k - 1) / k + 15) / 16 * 16;
-                const int64_t wp = w - sub * pw < pw ? w - sub * pw : pw;
-                cost += tile_cost(wp > 0 ? wp : 0);
-            }
+        if (split) {
+            if (c < P) cost += piece_cost(c) * kh;
+            for (int64_t t = c; t < tail_first; t += grid) cost += tile_cost(width(t)) * nst;
+            if (c >= P && c < 2 * P) cost += piece_cost(c - P) * (nst - kh);
+        } else {
+            for (int64_t t = c; t < total; t += grid)
+                cost += (t < tail_first ? tile_cost(width(t)) : piece_cost(t - tail_first)) * nst;
         }
         if (cost > worst) worst = cost;
     }
-    if (plan) *plan = TcPlan{bn, k, tail_first, total, grid};
+    if (plan) {
+        *plan = TcPlan{bn, k, tail_first, total, grid};
+        if (split) {
+            plan->split_p = P;
+            plan->split_kh = kh;
+            plan->ws_ld = pw_max;
+        }
+    }
     return worst * width_factor(bn);
 }
 
-TcPlan plan_tc_uncached(int64_t M, int64_t N, int sms, bool allow_cut) {
+TcPlan plan_tc_uncached(int64_t M, int64_t N, int sms, bool allow_cut, bool allow_split,
+                        int64_t nst) {
     const int64_t nt = (N + kBM - 1) / kBM;
     TcPlan plan{};
     int64_t best = INT64_MAX;
     for (int bn = kBNMax; bn >= 32; bn -= 16) {
         TcPlan p{};
-        const int64_t m = plan_makespan(M, nt, sms, bn, 1, &p);
+        const int64_t m = plan_makespan(M, nt, sms, bn, 1, nst, false, &p);
         if (m < best) {
             best = m;
             plan = p;
         }
     }
     // then a cut of the last partial wave, at any width, kept where the
-    // simulation shortens the best uncut makespan by at least 1%
-    const int64_t uncut = best;
-    for (int bn = kBNMax; allow_cut && bn >= 32; bn -= 16) {
-        for (int k = 2; k <= 8 && bn / k >= 16; k *= 2) {
-            TcPlan p{};
-            const int64_t m = plan_makespan(M, nt, sms, bn, k, &p);
-            if (m < best && m * 100 <= uncut * 99) {
-                best = m;
-                plan = p;
+    // simulation shortens the best uncut makespan by at least 1%; then the same
+    // pieces run in two parts along K, kept where that shortens the best plan
+    // so far by at least 10% (measured on GB300: the instance with the split
+    // runs its tiles a few percent slower, and pieces running beside full tiles
+    // slow those down, so the pp512 attention and FFN-down shapes (16% by the
+    // simulation) gain 11-12% and FFN gate/up (3%) loses)
+    for (int split = 0; split <= (allow_split ? 1 : 0); ++split) {
+        const int64_t before = best;
+        const int64_t keep = split ? 90 : 99;
+        for (int bn = kBNMax; allow_cut && bn >= 32; bn -= 16) {
+            for (int k = split ? 1 : 2; k <= 8 && bn / k >= 16; k *= 2) {
+                TcPlan p{};
+                const int64_t m = plan_makespan(M, nt, sms, bn, k, nst, split != 0, &p);
+                if (m >= 0 && m < best && m * 100 <= before * keep) {
+                    best = m;
+                    plan = p;
+                }
             }
         }
     }
@@ -943,27 +1166,40 @@ TcPlan plan_tc_uncached(int64_t M, int64_t N, int sms, bool allow_cut) {
 
 // the simulation costs O(tiles) host time per candidate: remember the plan of
 // each shape (a bounded table, emptied when full)
-TcPlan plan_tc(int64_t M, int64_t N, int sms, bool allow_cut) {
+TcPlan plan_tc(int64_t M, int64_t N, int sms, bool allow_cut, bool allow_split, int64_t nst) {
     static std::mutex mu;
-    static std::map<std::tuple<int64_t, int64_t, int, bool>, TcPlan> plans;
-    const auto key = std::make_tuple(M, N, sms, allow_cut);
+    static std::map<std::tuple<int64_t, int64_t, int, bool, bool, int64_t>, TcPlan> plans;
+    if (!allow_split) nst = 1;   // the plan does not depend on K then
+    const auto key = std::make_tuple(M, N, sms, allow_cut, allow_split, nst);
     {
         std::lock_guard<std::mutex> lock(mu);
         const auto it = plans.find(key);
         if (it != plans.end()) return it->second;
     }
-    const TcPlan plan = plan_tc_uncached(M, N, sms, allow_cut);
+    const TcPlan plan = plan_tc_uncached(M, N, sms, allow_cut, allow_split, nst);
     std::lock_guard<std::mutex> lock(mu);
     if (plans.size() >= 4096) plans.clear();
     plans.emplace(key, plan);
     return plan;
 }
 
-template <int EPQ, int XB, int kEpi, bool kTail = false, bool kWQ = false>
+// The workspace of a plan with the K split, at fixed offsets whatever the plan
+// (so that a workspace reused by plans of other shapes never finds partial sums
+// where it looks for flags): a 256-byte header (the generation number, the
+// count of finished CTAs), flags [kSplitMaxP][16] (generation numbers), then the
+// partial sums [split_p][128][ws_ld] (fp32).
+constexpr int64_t kSplitFlagOff = 256;
+constexpr int64_t kSplitAccOff = kSplitFlagOff + kSplitMaxP * 16 * 8;
+inline size_t split_ws_bytes(const TcPlan &p) {
+    if (p.split_p == 0) return 0;
+    return static_cast<size_t>(kSplitAccOff) + static_cast<size_t>(p.split_p) * kBM * p.ws_ld * 4;
+}
+
+template <int EPQ, int XB, int kEpi, bool kTail = false, bool kWQ = false, bool kSplit = false>
 h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStream_t s) {
     using C = TcCfg<EPQ, XB, kEpi == 2, kWQ>;
     constexpr int kSmem = C::kSmem;
-    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi, kTail, kWQ>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPQ, XB, kEpi, kTail, kWQ, kSplit>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return launch_status(e);
     if constexpr (C::kRegSplit) {
@@ -972,7 +1208,8 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
         // (read once per kernel; a failed read leaves -1 and refuses every launch)
         static const int regs = [] {
             cudaFuncAttributes fa{};
-            return cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi, kTail, kWQ>) == cudaSuccess
+            return cudaFuncGetAttributes(&fa, gemm_tc_kernel<EPQ, XB, kEpi, kTail, kWQ, kSplit>) ==
+                           cudaSuccess
                        ? fa.numRegs
                        : -1;
         }();
@@ -981,7 +1218,7 @@ h32_status launch_tc(const CUtensorMap *maps, const TcArgs &a, int grid, cudaStr
             return H32_ERR_UNSUPPORTED;
         }
     }
-    const cudaError_t el = launch_pdl(gemm_tc_kernel<EPQ, XB, kEpi, kTail, kWQ>, dim3(grid), dim3(C::kThreads),
+    const cudaError_t el = launch_pdl(gemm_tc_kernel<EPQ, XB, kEpi, kTail, kWQ, kSplit>, dim3(grid), dim3(C::kThreads),
                                       kSmem, s, maps[0], maps[1], maps[2], maps[3], a);
     return launch_status(el != cudaSuccess ? el : cudaGetLastError());
 }
@@ -1014,7 +1251,7 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
                        const int32_t *expert_off, int64_t M, int64_t N, int64_t K, float *y,
                        int64_t ldy, int32_t *block_sums, void *stream, uint8_t *qn = nullptr,
                        float *qnd = nullptr, int64_t ldqnd = 0, int qn_rot = 0,
-                       const uint16_t *wd16 = nullptr) {
+                       const uint16_t *wd16 = nullptr, void *ws = nullptr, size_t ws_bytes = 0) {
     if (wd16) ldws = K / 32;
     if (M < 0 || N <= 0 || K <= 0 || (K % 128) != 0 || (N % 16) != 0 || (y && ldy < N) ||
         ldws < K / 32 || (ldws % 4) != 0 || ldxd < M || (ldxd % 4) != 0 || E < 1 ||
@@ -1047,7 +1284,11 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
             return H32_ERR_INVALID_ARG;
     } else {
         if (((N + kBM - 1) / kBM) * ((M + 15) / 16) * 8 > 0x7FFFFFFFll) return H32_ERR_INVALID_ARG;
-        plan = plan_tc(M, N, sms, !block_sums);
+        plan = plan_tc(M, N, sms, !block_sums, ws && !block_sums && !qn && !wd16, K / 128);
+        if (plan.split_p > 0) {
+            if (ws_bytes < split_ws_bytes(plan)) return H32_ERR_INVALID_ARG;
+            if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return H32_ERR_ALIGNMENT;
+        }
     }
     const int bn = plan.bn;
     const int64_t grid = plan.grid;
@@ -1083,6 +1324,17 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     a.E = static_cast<int32_t>(E);
     a.tail_first = static_cast<int32_t>(plan.tail_first);
     a.tail_k = plan.tail_k;
+    if (plan.split_p > 0) {
+        // the planner splits only with a workspace of the plan's size (checked above)
+        if (!ws) return H32_ERR_INVALID_ARG;
+        uint8_t *w = static_cast<uint8_t *>(ws);
+        a.ws_hdr = reinterpret_cast<unsigned long long *>(w);
+        a.ws_flag = reinterpret_cast<unsigned long long *>(w + kSplitFlagOff);
+        a.ws_acc = reinterpret_cast<float *>(w + kSplitAccOff);
+        a.split_p = static_cast<int32_t>(plan.split_p);
+        a.split_kh = static_cast<int32_t>(plan.split_kh);
+        a.ws_ld = static_cast<int32_t>(plan.ws_ld);
+    }
     a.wait_limit = wait_limit();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int g = static_cast<int>(grid);
@@ -1093,6 +1345,7 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     }
     if (xbits == 8) {
         if (block_sums) return launch_tc<H32_TC_EPI_PER_QUAD, 8, 1>(maps, a, g, s);
+        if (plan.split_p > 0) return launch_tc<H32_TC_EPI_PER_QUAD, 8, 0, true, false, true>(maps, a, g, s);
         return plan.tail_k > 1 ? launch_tc<H32_TC_EPI_PER_QUAD, 8, 0, true>(maps, a, g, s)
                                : launch_tc<H32_TC_EPI_PER_QUAD, 8, 0>(maps, a, g, s);
     }
@@ -1106,6 +1359,9 @@ h32_status run_gemm_tc(int xbits, const uint8_t *wp, const float *wsc, int64_t l
     // shapes), 16 otherwise
     const int n16 = bn / 16;
     const bool narrow = n16 % 4 == 1 || n16 % 4 == 2;
+    if (plan.split_p > 0)
+        return narrow ? launch_tc<3, 4, 0, true, false, true>(maps, a, g, s)
+                      : launch_tc<H32_TC_EPI_PER_QUAD, 4, 0, true, false, true>(maps, a, g, s);
     if (plan.tail_k > 1)
         return narrow ? launch_tc<3, 4, 0, true>(maps, a, g, s)
                       : launch_tc<H32_TC_EPI_PER_QUAD, 4, 0, true>(maps, a, g, s);
@@ -1122,6 +1378,53 @@ extern "C" h32_status q4_0_x_q4_gemm_tc(const uint8_t *wp, const float *wsc, int
                                         int32_t *block_sums, void *stream) {
     return h32::run_gemm_tc(4, wp, wsc, ldws, 1, xw, xdt, ldxd, nullptr, M, N, K, y, ldy,
                             block_sums, stream);
+}
+
+extern "C" h32_status h32_gemm_tc_schedule(int64_t M, int64_t N, int64_t K, int32_t sms,
+                                           int32_t with_workspace, int64_t *out) {
+    if (!out || sms < 1 || M < 1 || N <= 0 || K <= 0 || (K % 128) != 0 || (N % 16) != 0 ||
+        M > 0x7FFFFFFFll || N > 0x7FFFFFFFll || K > 0x7FFFFFFFll ||
+        ((N + 127) / 128) * ((M + 15) / 16) * 8 > 0x7FFFFFFFll)
+        return H32_ERR_INVALID_ARG;
+    const h32::TcPlan p = h32::plan_tc(M, N, sms, true, with_workspace != 0, K / 128);
+    const int64_t v[9] = {p.bn, p.tail_k, p.tail_first, p.total, p.grid,
+                          p.split_p, p.split_kh, p.ws_ld,
+                          static_cast<int64_t>(h32::split_ws_bytes(p))};
+    for (int i = 0; i < 9; ++i) out[i] = v[i];
+    return H32_OK;
+}
+
+extern "C" h32_status h32_gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes) {
+    if (!bytes) return H32_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (M < 0 || N <= 0 || K <= 0 || (K % 128) != 0 || (N % 16) != 0 || M > 0x7FFFFFFFll ||
+        N > 0x7FFFFFFFll || K > 0x7FFFFFFFll || ((N + 127) / 128) * ((M + 15) / 16) * 8 > 0x7FFFFFFFll)
+        return H32_ERR_INVALID_ARG;
+    if (M == 0) return H32_OK;
+    int sms = 0;
+    H32_TRY(h32::check_device(&sms));
+    *bytes = h32::split_ws_bytes(h32::plan_tc(M, N, sms, true, true, K / 128));
+    return H32_OK;
+}
+
+extern "C" h32_status q4_0_x_q4_gemm_tc_ws(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                           const uint8_t *xw, const float *xdt, int64_t ldxd,
+                                           int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
+                                           int32_t *block_sums, void *workspace,
+                                           size_t workspace_bytes, void *stream) {
+    return h32::run_gemm_tc(4, wp, wsc, ldws, 1, xw, xdt, ldxd, nullptr, M, N, K, y, ldy,
+                            block_sums, stream, nullptr, nullptr, 0, 0, nullptr, workspace,
+                            workspace_bytes);
+}
+
+extern "C" h32_status q4_0_x_q8_gemm_tc_ws(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                           const uint8_t *xw8, const float *xdt, int64_t ldxd,
+                                           int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
+                                           int32_t *block_sums, void *workspace,
+                                           size_t workspace_bytes, void *stream) {
+    return h32::run_gemm_tc(8, wp, wsc, ldws, 1, xw8, xdt, ldxd, nullptr, M, N, K, y, ldy,
+                            block_sums, stream, nullptr, nullptr, 0, 0, nullptr, workspace,
+                            workspace_bytes);
 }
 
 extern "C" h32_status q4_0_x_q4_gemm_tc_quant_next(const uint8_t *wp, const float *wsc,

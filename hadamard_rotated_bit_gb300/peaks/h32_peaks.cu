@@ -13,6 +13,10 @@
 //   quantizer_launch_floor  an empty kernel and a copy with the activation
 //             quantizer's access pattern on its grid at the pp512 sizes
 //             (512 x 5120 and 512 x 17408 bf16), L2 flushed before each launch
+//   tma_read  bulk asynchronous copies (the TMA engine) of 16 KB chunks from a
+//             buffer held in L2 (32 MB) and from one in HBM (2 GB) into a ring of
+//             shared-memory stages, one thread a CTA, every SM: bytes per clock
+//             per SM and the aggregate rate (the operand stream of the tc GEMM)
 // Every wait is bounded; nothing here depends on another kernel or rank.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -263,6 +267,47 @@ __global__ void __launch_bounds__(512, 1) k_sm(int iters, long long *cyc, uint32
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tm) : "memory");
 }
 
+// ------------------------------------------------ TMA reads (L2 and HBM)
+// One thread a CTA keeps kTmaStages bulk copies of 16 KB in flight; CTA b reads
+// the chunks b, b + gridDim.x, ... of the buffer, wrapping at `span` bytes.
+constexpr int kTmaStages = 8;
+constexpr int kTmaChunk = 16384;
+__global__ void __launch_bounds__(32, 1) k_tma(const uint8_t *src, long long span, int iters,
+                                               long long *cyc) {
+    extern __shared__ __align__(1024) uint8_t tsm[];
+    __shared__ __align__(8) uint64_t bars[kTmaStages];
+    if (threadIdx.x != 0) return;
+    for (int s = 0; s < kTmaStages; ++s) mbar_init(&bars[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const long long nchunks = span / kTmaChunk;
+    long long c = blockIdx.x;
+    auto issue = [&](int s) {
+        const uint8_t *g = src + (c % nchunks) * kTmaChunk;
+        c += gridDim.x;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(&bars[s])),
+                     "r"(kTmaChunk)
+                     : "memory");
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                su32(tsm + s * kTmaChunk)),
+            "l"(g), "r"(kTmaChunk), "r"(su32(&bars[s]))
+            : "memory");
+    };
+    const long long t0 = clock64();
+    for (int s = 0; s < kTmaStages; ++s) issue(s);
+    for (int i = 0; i < iters; ++i)
+        for (int s = 0; s < kTmaStages; ++s) {
+            if (!mbar_wait(&bars[s], i & 1)) {
+                // gave up (g_err is set): wait, bounded, for the copies still in flight
+                for (int r = s; r < kTmaStages; ++r) mbar_wait(&bars[r], i & 1);
+                for (int r = 0; r < s && i + 1 < iters; ++r) mbar_wait(&bars[r], (i + 1) & 1);
+                return;
+            }
+            if (i + 1 < iters) issue(s);
+        }
+    cyc[blockIdx.x] = clock64() - t0;
+}
+
 // ---------------------------------------- launch floor of the pp512 quantizer sizes
 __global__ void k_empty() {}
 
@@ -383,6 +428,39 @@ int main() {
                "\"clocks_per_instruction_per_sm\": %.2f}\n", l / 128.0);
         const double b = run_sm<4, 128>(sms, 64, 20000, cyc, sink) / 20000.0;
         printf("{\"probe\": \"mbarrier\", \"clocks_per_hop\": %.0f}\n", b / 2.0);
+    }
+    // TMA reads: a 32 MB buffer (L2-resident after the first pass) and a 2 GB one
+    {
+        uint8_t *buf;
+        const long long big = 2ll << 30, small = 32ll << 20;
+        CK(cudaMalloc(&buf, big));
+        CK(cudaMemset(buf, 1, big));
+        CK(cudaFuncSetAttribute(k_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kTmaStages * kTmaChunk));
+        cudaEvent_t e0, e1;
+        CK(cudaEventCreate(&e0));
+        CK(cudaEventCreate(&e1));
+        const long long spans[2] = {small, big};
+        const char *names[2] = {"l2_32MB", "hbm_2GB"};
+        for (int m = 0; m < 2; ++m) {
+            // HBM: each CTA streams its share of the 2 GB once
+            const int iters = m == 0 ? 400 : static_cast<int>(big / kTmaChunk / sms / kTmaStages);
+            float ms = 0;
+            for (int rep = 0; rep < 2; ++rep) {
+                CK(cudaEventRecord(e0));
+                k_tma<<<sms, 32, kTmaStages * kTmaChunk>>>(buf, spans[m], iters, cyc);
+                CK(cudaGetLastError());
+                CK(cudaEventRecord(e1));
+                CK(cudaEventSynchronize(e1));
+                CK(cudaEventElapsedTime(&ms, e0, e1));
+            }
+            const double bytes = static_cast<double>(sms) * iters * kTmaStages * kTmaChunk;
+            const double c = mean_cycles(cyc, sms);
+            printf("{\"probe\": \"tma_read\", \"source\": \"%s\", \"bytes_per_clock_per_sm\": %.1f, "
+                   "\"aggregate_GBps\": %.0f}\n",
+                   names[m], bytes / sms / c, bytes / (ms * 1e-3) / 1e9);
+        }
+        CK(cudaFree(buf));
     }
     // the quantizer's launch floor at the pp512 sizes: median of 25 launches, each
     // after a 256 MB write that flushes L2, on the grid the quantizer uses

@@ -38,6 +38,7 @@
 #ifndef H32_H
 #define H32_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -353,6 +354,65 @@ h32_status q4_0_x_q8_gemm_tc(const uint8_t *wp, const float *wsc, int64_t ldws,
                              const uint8_t *xw8, const float *xdt, int64_t ldxd, int64_t M,
                              int64_t N, int64_t K, float *y, int64_t ldy, int32_t *block_sums,
                              void *stream);
+
+/*
+ * ---------------------------------------------------------------------------
+ * The K split of the last wave.  The tc GEMMs run one persistent block per SM
+ * over 128 x (up to 128)-token tiles; where the tiles do not fill the last
+ * wave, its tiles are cut along the tokens, and with a workspace each cut piece
+ * also runs in two parts along K on two SMs: the first part before that SM's
+ * full tiles, the second after another SM's, continuing the first part's
+ * accumulators.  Every output still takes its 32-blocks in order, so the result
+ * is bit-identical to q4_0_x_q4_gemm_tc; only the schedule changes (on the
+ * 512-token projections of the chain the last wave shrinks from about half a
+ * tile to a quarter).
+ * ---------------------------------------------------------------------------
+ */
+
+/*
+ * Workspace bytes the _ws entry points need for an M x N x K product on the
+ * current device: 0 when the schedule does not split (then no workspace is
+ * used).  The plan depends on M, N, K and the device's SM count only.
+ * Returns H32_ERR_INVALID_ARG for shapes the GEMMs reject (K % 128, N % 16).
+ */
+h32_status h32_gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes);
+
+/*
+ * The schedule the dense tc GEMMs (plain output) take for an M x N x K product
+ * on a device of `sms` SMs, with a workspace (with_workspace != 0) or without:
+ * host arithmetic only, no device call.  out[9] receives: tokens per tile,
+ * pieces per cut tile, the first cut tile, the number of work units (uncut
+ * tiles + pieces), the grid, the pieces split along K (0: none), the K stages
+ * (of 128) of a piece's first part, the piece width (workspace row stride) and
+ * the workspace bytes.  Requires M >= 1, K % 128 == 0, N % 16 == 0.
+ */
+h32_status h32_gemm_tc_schedule(int64_t M, int64_t N, int64_t K, int32_t sms,
+                                int32_t with_workspace, int64_t *out);
+
+/*
+ * q4_0_x_q4_gemm_tc / q4_0_x_q8_gemm_tc with a caller-owned workspace for the
+ * K split (same arguments, same results, bit for bit):
+ *   workspace        device memory, 256-byte aligned, or null (no split: the
+ *                    plain entry point's schedule); zero-filled once before its
+ *                    first use, after which every call leaves it valid for the
+ *                    next (a header with a generation number that the kernel
+ *                    advances, so flags of earlier calls, or of earlier replays
+ *                    of a captured graph, never match)
+ *   workspace_bytes  its size; below h32_gemm_tc_workspace_bytes(M, N, K) ->
+ *                    H32_ERR_INVALID_ARG
+ * A workspace serves one call at a time: calls that share one must be ordered
+ * (one stream, or events).  With block_sums the schedule never splits.  The
+ * second part of a piece waits, bounded, for the first part's flag; a timeout
+ * is reported as H32_ERR_TIMEOUT like every other wait of the kernel.
+ */
+h32_status q4_0_x_q4_gemm_tc_ws(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                const uint8_t *xw, const float *xdt, int64_t ldxd, int64_t M,
+                                int64_t N, int64_t K, float *y, int64_t ldy, int32_t *block_sums,
+                                void *workspace, size_t workspace_bytes, void *stream);
+h32_status q4_0_x_q8_gemm_tc_ws(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                const uint8_t *xw8, const float *xdt, int64_t ldxd, int64_t M,
+                                int64_t N, int64_t K, float *y, int64_t ldy, int32_t *block_sums,
+                                void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Expert-batched W4A4 product on tc-form operands (the tc counterpart of

@@ -76,18 +76,42 @@ def _exact_small_case(h32):
     assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
 
 
-@pytest.mark.parametrize("kind", ["q4_tc", "q8_tc", "experts_tc", "widen", "widen_experts"])
+def _exact_split_case(h32):
+    """A product whose last wave is split along K, through the binding's
+    workspace of the stream the timed-out launches used: exact, so the
+    generation the aborted launches left behind is consistent."""
+    M, N, K = 64, 20480, 256
+    x = wl.f32_to_bf16_bits(wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, 124))
+    w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, 125)
+    rwq, rwd = oracle.quantize_weights_q4_0(w)
+    rxq, rxd = oracle.quantize_act_q4(x)
+    from tests._gpu import torch_bf16
+    wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(rwq), torch_of(rwd.view(np.int16)))
+    xw, xdt = h32.h32_quantize_act_q4_tc(torch_bf16(x))
+    y = h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M)
+    assert h32.h32_device_status() == 0
+    r32, _, _ = oracle.gemm(rwq, rwd, rxq, rxd, K)
+    assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
+
+
+@pytest.mark.parametrize("kind", ["q4_tc", "q8_tc", "experts_tc", "widen", "widen_experts",
+                                  "q4_tc_split", "q8_tc_split"])
 def test_tc_gemm_one_poll_wait_bound(h32, kind):
     """The tensor-core-form GEMM (the chain's kernel, its 8-bit and its expert
-    instances, and the instances that widen Q4_0 planes in shared memory) under
-    a one-poll wait bound: the TMA, MMA, widening and epilogue roles that give
-    up record H32_ERR_TIMEOUT, drain their copies and MMAs, free TMEM and
-    return; the status is reported once and the same context then computes
-    exact results."""
+    instances, the instances that widen Q4_0 planes in shared memory, and the
+    instances whose last wave is split along K, whose second parts also wait
+    for the first parts' flags) under a one-poll wait bound: the TMA, MMA,
+    widening and epilogue roles that give up record H32_ERR_TIMEOUT, drain
+    their copies and MMAs, free TMEM and return; the status is reported once
+    and the same context then computes exact results."""
     import torch
     M, N, K = 512, 4096, 2048
+    if kind.endswith("_split"):
+        N = 5120   # 160 tiles: a full wave and 8 tiles cut and split
+        if h32.h32_gemm_tc_workspace_bytes(M, N, K) == 0:
+            pytest.skip("this device's schedule does not split the case")
     wp, wsc = _tc_ones(h32, N, K, 0.0625)
-    xb = 2 if kind == "q8_tc" else 1
+    xb = 2 if kind.startswith("q8_tc") else 1
     xw = torch.full((M, K * xb), 0x38, dtype=torch.uint8, device="cuda")
     xdt = torch.ones((K // 32, M), dtype=torch.float32, device="cuda")
     E = 8
@@ -100,9 +124,9 @@ def test_tc_gemm_one_poll_wait_bound(h32, kind):
     h32.h32_set_wait_limit(1)
     try:
         for _ in range(3):
-            if kind == "q4_tc":
+            if kind in ("q4_tc", "q4_tc_split"):
                 h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M)
-            elif kind == "q8_tc":
+            elif kind in ("q8_tc", "q8_tc_split"):
                 h32.q4_0_x_q8_gemm_tc(wp, wsc, xw, xdt, M=M)
             elif kind == "experts_tc":
                 h32.q4_0_x_q4_gemm_tc_experts(wpe, wsce, xw, xdt, off, 512, R=M)
@@ -117,3 +141,5 @@ def test_tc_gemm_one_poll_wait_bound(h32, kind):
     assert h32.h32_device_status() == 0
     torch.cuda.synchronize()
     _exact_small_case(h32)
+    if kind.endswith("_split"):
+        _exact_split_case(h32)

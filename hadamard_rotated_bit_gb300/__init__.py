@@ -25,6 +25,11 @@ __all__ = [
     "q4_0_x_q4_gemm_tc", "h32_quantize_act_q4_tc_gather", "q4_0_x_q4_gemm_tc_experts",
     "h32_quantize_act_q8_tc", "q4_0_x_q8_gemm_tc", "q4_0_x_q4_gemm_tc_quant_next",
     "h32_moe_route", "h32_moe_combine",
+    "h32_quantize_act_q4_tc_e5m2", "h32_quantize_act_q4_tc_e5m2_gather",
+    "q4_0_x_q4_gemm_tc_widen", "q4_0_x_q4_gemm_tc_widen_experts",
+    "h32_q4_0_blocks_to_planes", "h32_q4_0_planes_to_blocks",
+    "h32_gemm_tc_workspace_bytes", "h32_gemm_tc_schedule",
+    "q4_0_x_q4_gemm_tc_noalloc", "q4_0_x_q8_gemm_tc_noalloc",
 ]
 
 
@@ -63,6 +68,10 @@ _SIGS = {
     "q4_0_x_q8_gemm_tc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P]),
     "h32_gemm_tc_workspace_bytes": (_INT, [_I64, _I64, _I64, ctypes.POINTER(ctypes.c_size_t)]),
     "h32_gemm_tc_schedule": (_INT, [_I64, _I64, _I64, _I32, _I32, ctypes.POINTER(ctypes.c_int64)]),
+    "q4_0_x_q4_gemm_tc_noalloc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64,
+                                         _P, _P]),
+    "q4_0_x_q8_gemm_tc_noalloc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64,
+                                         _P, _P]),
     "q4_0_x_q4_gemm_tc_ws": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P,
                                     _P, ctypes.c_size_t, _P]),
     "q4_0_x_q8_gemm_tc_ws": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P,
@@ -497,6 +506,17 @@ def q4_0_x_q8_gemm_tc(wp, wsc, xw8, xdt, M=None, y=None, block_sums=None, stream
     return _gemm_tc("q4_0_x_q8_gemm_tc", wp, wsc, xw8, xdt, M, y, block_sums, stream, workspace)
 
 
+def q4_0_x_q4_gemm_tc_noalloc(wp, wsc, xw, xdt, M=None, y=None, block_sums=None, stream=None):
+    """q4_0_x_q4_gemm_tc with the K split on the library's static per-device
+    workspace: no allocation by the call (calls sharing a device are ordered)."""
+    return _gemm_tc("q4_0_x_q4_gemm_tc", wp, wsc, xw, xdt, M, y, block_sums, stream, "noalloc")
+
+
+def q4_0_x_q8_gemm_tc_noalloc(wp, wsc, xw8, xdt, M=None, y=None, block_sums=None, stream=None):
+    """q4_0_x_q8_gemm_tc on the library's static workspace (as the 4-bit form)."""
+    return _gemm_tc("q4_0_x_q8_gemm_tc", wp, wsc, xw8, xdt, M, y, block_sums, stream, "noalloc")
+
+
 def h32_gemm_tc_workspace_bytes(M: int, N: int, K: int) -> int:
     """Workspace bytes q4_0_x_q4_gemm_tc_ws / q4_0_x_q8_gemm_tc_ws use for an
     M x N x K product on the current device (0: the schedule does not split)."""
@@ -569,6 +589,12 @@ def _gemm_tc(fn, wp, wsc, xw, xdt, M, y, block_sums, stream, workspace=False):
     ldy = _rows(y, "y")
     S = _sums(block_sums, M, N, K // 32, dev)
     _same_gpu(("wp", wp), ("wsc", wsc), ("xw", xw), ("xdt", xdt), ("y", y), ("S", S))
+    if isinstance(workspace, str) and workspace == "noalloc":
+        fn = fn + "_noalloc"
+        st = getattr(lib(), fn)(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt),
+                                xdt.shape[1], M, N, K, _ptr(y), ldy, _ptr(S), _stream(stream))
+        _check(fn, st)
+        return (y, S) if S is not None else y
     ws = None
     if workspace is None and S is None and M > 0:
         ws = _workspace_for(M, N, K, dev, stream)
@@ -819,6 +845,10 @@ _COMPUTE_CALLS = (
     "h32_quantize_act_q8_tc", "h32_prepack_weights_q4_0_tc", "q4_0_x_q4_gemm_tc",
     "q4_0_x_q8_gemm_tc", "h32_quantize_act_q4_tc_gather", "q4_0_x_q4_gemm_tc_experts",
     "q4_0_x_q4_gemm_tc_quant_next", "h32_moe_route", "h32_moe_combine",
+    "h32_quantize_act_q4_tc_e5m2", "h32_quantize_act_q4_tc_e5m2_gather",
+    "q4_0_x_q4_gemm_tc_widen", "q4_0_x_q4_gemm_tc_widen_experts",
+    "h32_q4_0_blocks_to_planes", "h32_q4_0_planes_to_blocks",
+    "q4_0_x_q4_gemm_tc_noalloc", "q4_0_x_q8_gemm_tc_noalloc",
 )
 for _name in _COMPUTE_CALLS:
     globals()[_name] = _trace.traced(_name)(globals()[_name])

@@ -1427,6 +1427,59 @@ extern "C" h32_status q4_0_x_q8_gemm_tc_ws(const uint8_t *wp, const float *wsc, 
                             workspace_bytes);
 }
 
+// The no-alloc entry points' workspace: one static array per device, zero at
+// module load (a valid workspace), never allocated or freed by a call.
+namespace h32 {
+namespace {
+constexpr size_t kStaticWsBytes = 4u << 20;
+__device__ __align__(256) uint8_t g_tc_static_ws[kStaticWsBytes];
+
+h32_status static_workspace(void **ptr) {
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return H32_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        const cudaError_t e = cudaGetSymbolAddress(&addr[dev], g_tc_static_ws);
+        if (e != cudaSuccess) return launch_status(e);
+    }
+    *ptr = addr[dev];
+    return H32_OK;
+}
+
+h32_status run_noalloc(int xbits, const uint8_t *wp, const float *wsc, int64_t ldws,
+                       const uint8_t *xw, const float *xdt, int64_t ldxd, int64_t M, int64_t N,
+                       int64_t K, float *y, int64_t ldy, int32_t *block_sums, void *stream) {
+    size_t need = 0;
+    if (!block_sums) {
+        const h32_status st = h32_gemm_tc_workspace_bytes(M, N, K, &need);
+        if (st != H32_OK) return st;
+    }
+    if (need > kStaticWsBytes) return H32_ERR_UNSUPPORTED;   // never allocates
+    void *ws = nullptr;
+    if (need > 0) H32_TRY(static_workspace(&ws));
+    return run_gemm_tc(xbits, wp, wsc, ldws, 1, xw, xdt, ldxd, nullptr, M, N, K, y, ldy,
+                       block_sums, stream, nullptr, nullptr, 0, 0, nullptr, ws,
+                       need > 0 ? kStaticWsBytes : 0);
+}
+}  // namespace
+}  // namespace h32
+
+extern "C" h32_status q4_0_x_q4_gemm_tc_noalloc(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                                const uint8_t *xw, const float *xdt, int64_t ldxd,
+                                                int64_t M, int64_t N, int64_t K, float *y,
+                                                int64_t ldy, int32_t *block_sums, void *stream) {
+    return h32::run_noalloc(4, wp, wsc, ldws, xw, xdt, ldxd, M, N, K, y, ldy, block_sums, stream);
+}
+
+extern "C" h32_status q4_0_x_q8_gemm_tc_noalloc(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                                const uint8_t *xw8, const float *xdt, int64_t ldxd,
+                                                int64_t M, int64_t N, int64_t K, float *y,
+                                                int64_t ldy, int32_t *block_sums, void *stream) {
+    return h32::run_noalloc(8, wp, wsc, ldws, xw8, xdt, ldxd, M, N, K, y, ldy, block_sums, stream);
+}
+
 extern "C" h32_status q4_0_x_q4_gemm_tc_quant_next(const uint8_t *wp, const float *wsc,
                                                    int64_t ldws, const uint8_t *xw,
                                                    const float *xdt, int64_t ldxd, int64_t M,

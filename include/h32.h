@@ -415,6 +415,25 @@ h32_status q4_0_x_q8_gemm_tc_ws(const uint8_t *wp, const float *wsc, int64_t ldw
                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * q4_0_x_q4_gemm_tc / q4_0_x_q8_gemm_tc with the K split, without a caller's
+ * workspace and without allocating: the workspace is a 4 MB array the library
+ * holds in each device's static memory (zero when the library's module is
+ * loaded, kept valid by every call).  Same arguments and results as the plain
+ * entry points.  A product whose schedule needs more than 4 MB of workspace
+ * is refused with H32_ERR_UNSUPPORTED (nothing is allocated in its place); on
+ * 152 SMs the pp512 chain's shapes need 0.5 MB.  All calls on one device share
+ * the array: calls that may overlap must be ordered (one stream, or events).
+ */
+h32_status q4_0_x_q4_gemm_tc_noalloc(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                     const uint8_t *xw, const float *xdt, int64_t ldxd,
+                                     int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
+                                     int32_t *block_sums, void *stream);
+h32_status q4_0_x_q8_gemm_tc_noalloc(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                     const uint8_t *xw8, const float *xdt, int64_t ldxd,
+                                     int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
+                                     int32_t *block_sums, void *stream);
+
+/*
  * Expert-batched W4A4 product on tc-form operands (the tc counterpart of
  * q4_0_x_q4_gemm_experts): rows r in [expert_off[e], expert_off[e+1]) of
  * xw/xdt (already in grouped order, e.g. from h32_quantize_act_q4_tc_gather)

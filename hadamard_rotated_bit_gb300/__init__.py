@@ -68,6 +68,8 @@ _SIGS = {
     "q4_0_x_q8_gemm_tc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P]),
     "h32_gemm_tc_workspace_bytes": (_INT, [_I64, _I64, _I64, ctypes.POINTER(ctypes.c_size_t)]),
     "h32_gemm_tc_schedule": (_INT, [_I64, _I64, _I64, _I32, _I32, ctypes.POINTER(ctypes.c_int64)]),
+    "q4_0_x_q4_gemm_tc_quant_next_ws": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P,
+                                               _I64, _P, _P, _I64, _INT, _P, ctypes.c_size_t, _P]),
     "q4_0_x_q4_gemm_tc_noalloc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64,
                                          _P, _P]),
     "q4_0_x_q8_gemm_tc_noalloc": (_INT, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64,
@@ -744,10 +746,10 @@ def q4_0_x_q4_gemm_tc_experts(wp, wsc, xw, xdt, expert_off, N, R=None, y=None, b
 
 
 def q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=None, y=None, want_y=True, rotate_next=True,
-                                 xw_next=None, xdt_next=None, stream=None):
+                                 xw_next=None, xdt_next=None, stream=None, workspace=None):
     """The tc W4A4 product with its output also quantized for the next projection
     in the same kernel.  Returns (y or None, xw_next [M][N] uint8, xdt_next
-    [N/32][ldxd] fp32)."""
+    [N/32][ldxd] fp32).  workspace as for q4_0_x_q4_gemm_tc (the K split)."""
     torch = _torch()
     if M is None:
         M = xw.shape[0]
@@ -766,11 +768,25 @@ def q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=None, y=None, want_y=True, 
     _need(xdt_next, "xdt_next", (torch.float32,), (_ge(N // 32), _ge(M)))
     _same_gpu(("wp", wp), ("wsc", wsc), ("xw", xw), ("xdt", xdt),
               ("y", y), ("xw_next", xw_next), ("xdt_next", xdt_next))
-    st = lib().q4_0_x_q4_gemm_tc_quant_next(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt),
-                                            xdt.shape[1], M, N, K, _ptr(y), ldy, _ptr(xw_next),
-                                            _ptr(xdt_next), xdt_next.shape[1],
-                                            _rot_arg(rotate_next), _stream(stream))
-    _check("q4_0_x_q4_gemm_tc_quant_next", st)
+    ws = None
+    if workspace is None and M > 0:
+        ws = _workspace_for(M, N, K, dev, stream)
+    elif workspace is not None and workspace is not False:
+        _need(workspace, "workspace", (torch.uint8,), (_ge(0),))
+        _same_gpu(("wp", wp), ("workspace", workspace))
+        ws = workspace
+    if ws is None:
+        st = lib().q4_0_x_q4_gemm_tc_quant_next(
+            _ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt), xdt.shape[1], M, N, K, _ptr(y),
+            ldy, _ptr(xw_next), _ptr(xdt_next), xdt_next.shape[1], _rot_arg(rotate_next),
+            _stream(stream))
+        _check("q4_0_x_q4_gemm_tc_quant_next", st)
+    else:
+        st = lib().q4_0_x_q4_gemm_tc_quant_next_ws(
+            _ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt), xdt.shape[1], M, N, K, _ptr(y),
+            ldy, _ptr(xw_next), _ptr(xdt_next), xdt_next.shape[1], _rot_arg(rotate_next),
+            _ptr(ws), ws.numel(), _stream(stream))
+        _check("q4_0_x_q4_gemm_tc_quant_next_ws", st)
     return y, xw_next, xdt_next
 
 

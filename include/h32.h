@@ -273,6 +273,18 @@ h32_status q4_0_x_q4_gemm_tc_quant_next(const uint8_t *wp, const float *wsc, int
                                         int rotate_next, void *stream);
 
 /*
+ * q4_0_x_q4_gemm_tc_quant_next with a caller-owned workspace for the K split of
+ * the last wave (the workspace as for q4_0_x_q4_gemm_tc_ws below; same results
+ * bit for bit, the output and its next-projection quantization both).
+ */
+h32_status q4_0_x_q4_gemm_tc_quant_next_ws(const uint8_t *wp, const float *wsc, int64_t ldws,
+                                           const uint8_t *xw, const float *xdt, int64_t ldxd,
+                                           int64_t M, int64_t N, int64_t K, float *y, int64_t ldy,
+                                           uint8_t *xw_next, float *xdt_next, int64_t ldxd_next,
+                                           int rotate_next, void *workspace,
+                                           size_t workspace_bytes, void *stream);
+
+/*
  * ---------------------------------------------------------------------------
  * Widening form.  The GEMMs below read the Q4_0 weight planes themselves
  * (half the weight bytes of the tc form; no repack) and widen each K stage's

@@ -213,3 +213,29 @@ def test_split_workspace_checks(h32):
     assert e.value.status == h32.H32_ERR_ALIGNMENT
     torch.cuda.synchronize()
     assert h32.h32_device_status() == 0
+
+
+@pytest.mark.parametrize("rot", [True, False])
+def test_split_fused_producer_bit_exact(h32, rot):
+    """The fused producer (output also quantized for the next projection) with
+    the K split: y, the next projection's codes and scales all equal the
+    oracle's quantizer on the oracle's output, with and without y."""
+    import torch
+    from tests.test_gpu_tc import e4m3_value
+    M, N, K = SMALL
+    if h32.h32_gemm_tc_workspace_bytes(M, N, K) == 0:
+        pytest.skip("this device's schedule does not split the case")
+    (wq, wd, xq, xd), (wp, wsc, xw, xdt) = _operands(h32, M, N, K, 985)
+    y, xn, xnd = h32.q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=M, rotate_next=rot)
+    torch.cuda.synchronize()
+    assert h32.h32_device_status() == 0
+    r32, _, _ = oracle.gemm(wq, wd, xq, xd, K)
+    assert np.array_equal(np_of(y).view(np.uint32), r32.view(np.uint32))
+    nq, nd = oracle.quantize_act_q4(r32, rot)
+    assert np.array_equal(e4m3_value(np_of(xn)), oracle.decode_act4(nq, N).astype(np.float64))
+    assert np.array_equal(np_of(xnd)[:, :M].T.view(np.uint32), nd.view(np.uint32))
+    y2, xn2, xnd2 = h32.q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=M, want_y=False,
+                                                      rotate_next=rot)
+    torch.cuda.synchronize()
+    assert y2 is None
+    assert np.array_equal(np_of(xn2), np_of(xn)) and np.array_equal(np_of(xnd2), np_of(xnd))

@@ -323,12 +323,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ void st_cg_v2(uint64_t *p, uint64_t x, uint64_t y) {
-    asm volatile("st.global.cg.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(x), "l"(y) : "memory");
-}
-__device__ __forceinline__ void ld_cg_v2(const uint64_t *p, uint64_t &x, uint64_t &y) {
-    asm volatile("ld.global.cg.v2.b64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
-}
 
 // The weight scales of the thread's row for the four blocks of K stage `st`
 // held in shared-memory stage `s`: fp32 [128 rows][4] from the repacked form,
@@ -398,14 +392,18 @@ __device__ __forceinline__ bool epi_item(const TcArgs &a, int t, int st0, int ns
             while (!__all_sync(0xFFFFFFFFu, ld_acquire_u64(flag) == want)) {
                 if (++polls > lim || *abort_flag) return false;
             }
-            const uint64_t *src = reinterpret_cast<const uint64_t *>(
-                a.ws_acc + (static_cast<int64_t>(p) * kBM + row) * a.ws_ld + c0);
+            // [piece][column][128 rows], the layout of y: a column's 32 rows are
+            // one coalesced access of the warp
+            const float *src = a.ws_acc + (static_cast<int64_t>(p) * a.ws_ld + c0) * kBM + row;
 #pragma unroll
             for (int c = 0; c < C::kMaxChunks; ++c) {
                 if (c < nch) {
 #pragma unroll
-                    for (int q = 0; q < 8; q += 2)
-                        ld_cg_v2(src + 8 * c + q, acc[8 * c + q], acc[8 * c + q + 1]);
+                    for (int q = 0; q < 8; ++q) {
+                        const float lo = __ldcg(src + (16 * c + 2 * q) * kBM);
+                        const float hi = __ldcg(src + (16 * c + 2 * q + 1) * kBM);
+                        acc[8 * c + q] = pair_of(__float_as_uint(lo), __float_as_uint(hi));
+                    }
                 }
             }
         }
@@ -456,14 +454,17 @@ __device__ __forceinline__ bool epi_item(const TcArgs &a, int t, int st0, int ns
         // the first part of a piece: its accumulators to the workspace, then the flag
         if (nch > 0) {
             const int p = t - a.tail_first;
-            uint64_t *dst = reinterpret_cast<uint64_t *>(
-                a.ws_acc + (static_cast<int64_t>(p) * kBM + row) * a.ws_ld + c0);
+            float *dst = a.ws_acc + (static_cast<int64_t>(p) * a.ws_ld + c0) * kBM + row;
 #pragma unroll
             for (int c = 0; c < C::kMaxChunks; ++c) {
                 if (c < nch) {
 #pragma unroll
-                    for (int q = 0; q < 8; q += 2)
-                        st_cg_v2(dst + 8 * c + q, acc[8 * c + q], acc[8 * c + q + 1]);
+                    for (int q = 0; q < 8; ++q) {
+                        const uint64_t pr = acc[8 * c + q];
+                        __stcg(dst + (16 * c + 2 * q) * kBM, __uint_as_float(static_cast<uint32_t>(pr)));
+                        __stcg(dst + (16 * c + 2 * q + 1) * kBM,
+                               __uint_as_float(static_cast<uint32_t>(pr >> 32)));
+                    }
                 }
             }
             __threadfence();
@@ -1335,7 +1336,7 @@ TcPlan plan_tc(int64_t M, int64_t N, int sms, bool allow_cut, bool allow_split, 
 // (so that a workspace reused by plans of other shapes never finds partial sums
 // where it looks for flags): a 256-byte header (the generation number, the
 // count of finished CTAs), flags [kSplitMaxP][16] (generation numbers), then the
-// partial sums [split_p][128][ws_ld] (fp32).
+// partial sums [split_p][ws_ld columns][128 rows] (fp32).
 constexpr int64_t kSplitFlagOff = 256;
 constexpr int64_t kSplitAccOff = kSplitFlagOff + kSplitMaxP * 16 * 8;
 inline size_t split_ws_bytes(const TcPlan &p) {

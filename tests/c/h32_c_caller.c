@@ -6,9 +6,13 @@
  * repack them, the W4A4 GEMM) and writes y [M][N] fp32 to the output file;
  * when K % 256 == 0 it then runs the widening route on the same Q4_0 planes
  * (activations as e5m2 bytes, the GEMM that widens the nibbles itself) and
- * appends its y [M][N].
+ * appends its y [M][N]; when the schedule splits the last wave along K on
+ * this device, it also runs the tensor-core GEMM with a workspace of its own
+ * (cudaMalloc'd, zeroed once, used twice) and the no-alloc form, appending
+ * their y [M][N].
  *
  * Input file: int64 M, N, K, then x and w as fp32, row-major.
+ * Output file: int64 R (the number of results), then R results y [M][N] fp32.
  * Usage: h32_c_caller <input> <output>.  Exit status 0 = success, 1 = a
  * library status that is not H32_OK (printed), 2 = I/O or CUDA runtime error.
  * Test infrastructure: built and run by tests/test_c_caller.py.
@@ -52,7 +56,7 @@ int main(int argc, char **argv) {
     if (fread(dims, sizeof(int64_t), 3, f) != 3) return 2;
     const int64_t M = dims[0], N = dims[1], K = dims[2], nb = K / 32;
     float *hx = malloc(sizeof(float) * M * K), *hw = malloc(sizeof(float) * N * K);
-    float *hy = malloc(sizeof(float) * M * N * 2);
+    float *hy = malloc(sizeof(float) * M * N * 5);
     if (!hx || !hw || !hy) return 2;
     if (fread(hx, sizeof(float), M * K, f) != (size_t)(M * K)) return 2;
     if (fread(hw, sizeof(float), N * K, f) != (size_t)(N * K)) return 2;
@@ -72,7 +76,7 @@ int main(int argc, char **argv) {
     CUDA_OK(cudaMalloc((void **)&wd, sizeof(uint16_t) * N * nb));
     CUDA_OK(cudaMalloc((void **)&wp, (size_t)(N * K)));
     CUDA_OK(cudaMalloc((void **)&wsc, sizeof(float) * N * ldws));
-    CUDA_OK(cudaMalloc((void **)&y, sizeof(float) * M * N * 2));
+    CUDA_OK(cudaMalloc((void **)&y, sizeof(float) * M * N * 5));
     CUDA_OK(cudaMemsetAsync(xdt, 0, sizeof(float) * nb * ldxd, stream));
     CUDA_OK(cudaMemcpyAsync(x, hx, sizeof(float) * M * K, cudaMemcpyHostToDevice, stream));
     CUDA_OK(cudaMemcpyAsync(w, hw, sizeof(float) * N * K, cudaMemcpyHostToDevice, stream));
@@ -81,19 +85,38 @@ int main(int argc, char **argv) {
     H32_OK_OR_FAIL(h32_prepack_weights_q4_0_tc(wq, wd, N, K, wp, wsc, ldws, stream));
     H32_OK_OR_FAIL(h32_quantize_act_q4_tc(x, H32_IN_F32, M, K, K, xw, xdt, ldxd, 1, stream));
     H32_OK_OR_FAIL(q4_0_x_q4_gemm_tc(wp, wsc, ldws, xw, xdt, ldxd, M, N, K, y, N, NULL, stream));
-    const int widen = (K % 256) == 0;
-    if (widen) {
+    int64_t routes = 1;
+    size_t ws_bytes = 0;
+    H32_OK_OR_FAIL(h32_gemm_tc_workspace_bytes(M, N, K, &ws_bytes));
+    if (ws_bytes > 0) {
+        void *ws;
+        CUDA_OK(cudaMalloc(&ws, ws_bytes));
+        CUDA_OK(cudaMemsetAsync(ws, 0, ws_bytes, stream));
+        for (int i = 0; i < 2; ++i)   /* the second call finds the workspace as the first left it */
+            H32_OK_OR_FAIL(q4_0_x_q4_gemm_tc_ws(wp, wsc, ldws, xw, xdt, ldxd, M, N, K,
+                                                y + routes * M * N, N, NULL, ws, ws_bytes, stream));
+        ++routes;
+        H32_OK_OR_FAIL(q4_0_x_q4_gemm_tc_noalloc(wp, wsc, ldws, xw, xdt, ldxd, M, N, K,
+                                                 y + routes * M * N, N, NULL, stream));
+        ++routes;
+        CUDA_OK(cudaStreamSynchronize(stream));
+        cudaFree(ws);
+    }
+    if ((K % 256) == 0) {
         H32_OK_OR_FAIL(h32_quantize_act_q4_tc_e5m2(x, H32_IN_F32, M, K, K, xw, xdt, ldxd, 1, stream));
-        H32_OK_OR_FAIL(q4_0_x_q4_gemm_tc_widen(wq, wd, xw, xdt, ldxd, M, N, K, y + M * N, N, NULL,
-                                               stream));
+        H32_OK_OR_FAIL(q4_0_x_q4_gemm_tc_widen(wq, wd, xw, xdt, ldxd, M, N, K, y + routes * M * N,
+                                               N, NULL, stream));
+        ++routes;
     }
     H32_OK_OR_FAIL(h32_device_status(stream));
 
-    const int64_t nout = M * N * (widen ? 2 : 1);
+    const int64_t nout = M * N * routes;
     CUDA_OK(cudaMemcpyAsync(hy, y, sizeof(float) * nout, cudaMemcpyDeviceToHost, stream));
     CUDA_OK(cudaStreamSynchronize(stream));
     f = fopen(argv[2], "wb");
-    if (!f || fwrite(hy, sizeof(float), nout, f) != (size_t)nout) return 2;
+    if (!f || fwrite(&routes, sizeof(int64_t), 1, f) != 1 ||
+        fwrite(hy, sizeof(float), nout, f) != (size_t)nout)
+        return 2;
     fclose(f);
     cudaFree(x); cudaFree(w); cudaFree(xw); cudaFree(xdt); cudaFree(wq);
     cudaFree(wd); cudaFree(wp); cudaFree(wsc); cudaFree(y);

@@ -38,15 +38,16 @@ def test_c_caller_builds(tmp_path):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("K", [384, 512])
-def test_c_caller_matches_the_oracle(tmp_path, K):
-    """K = 384: the tensor-core route; K = 512: also the widening route (its
-    output appended), both bit-exact."""
+@pytest.mark.parametrize("M,N,K", [(70, 144, 384), (70, 144, 512), (64, 20480, 256)])
+def test_c_caller_matches_the_oracle(tmp_path, M, N, K):
+    """K = 384: the tensor-core route; K = 512: also the widening route; 64 x
+    20480 x 256 (a full wave and 8 tiles over on 152 SMs): also the K split with
+    the caller's workspace (twice) and the no-alloc form.  Every result
+    bit-exact."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     exe = _compile(tmp_path)
-    M, N = 70, 144
     x = wl.act_normal_outliers(M, K, 0.01, 20.0, 0, wl.CFG_TEST, 290)
     w = wl.weights_normal(N, K, 0.02, 0, wl.CFG_TEST, 291)
     inp, out = tmp_path / "in.bin", tmp_path / "out.bin"
@@ -56,8 +57,12 @@ def test_c_caller_matches_the_oracle(tmp_path, K):
         f.write(np.ascontiguousarray(w, np.float32).tobytes())
     r = subprocess.run([exe, str(inp), str(out)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
-    routes = 2 if K % 256 == 0 else 1
-    ys = np.fromfile(out, np.float32).reshape(routes, M, N)
+    raw = np.fromfile(out, np.uint8)
+    routes = int(raw[:8].view(np.int64)[0])
+    expect = 1 + (K % 256 == 0) + (2 if N == 20480 and torch.cuda.get_device_properties(0)
+                                   .multi_processor_count == 152 else 0)
+    assert routes == expect
+    ys = raw[8:].view(np.float32).reshape(routes, M, N)
     wq, wd = oracle.quantize_weights_q4_0(w)
     xq, xd = oracle.quantize_act_q4(x)
     r32, _, _ = oracle.gemm(wq, wd, xq, xd, K)

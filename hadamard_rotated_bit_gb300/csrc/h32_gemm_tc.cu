@@ -157,7 +157,7 @@ struct TcArgs {
     // dense only, the K split of the cut pieces (split_p pieces, 0 = none):
     // the first split_kh K stages of piece p run on CTA p, the rest on CTA
     // split_p + p; the partial sums pass through the caller's workspace (a
-    // header, ws_flag[p][16], ws_acc[p][128][ws_ld])
+    // header, ws_flag[p][16], ws_acc[p][ws_ld columns][128 rows])
     unsigned long long *ws_hdr, *ws_flag;
     float *ws_acc;
     int32_t split_p, split_kh, ws_ld;

@@ -90,36 +90,37 @@ def test_split_all_outputs_bit_exact(h32, bits):
     assert np.array_equal(np_of(y0).view(np.uint32), r32.view(np.uint32))
 
 
-@pytest.mark.parametrize("proj", ["attn", "ffn_down", "ffn_gate_up"])
-def test_split_pieces_pp512_sampled(h32, proj):
-    """The pp512 projections as the chain runs them (split last wave): outputs
-    sampled inside the split pieces (the last two weight-row tiles' tokens of
-    attention and FFN down; the last tiles of gate/up) and elsewhere, against
-    the oracle, bit for bit."""
+@pytest.mark.parametrize("proj,M", [("attn", 512), ("ffn_down", 512), ("ffn_gate_up", 512),
+                                    ("attn", 1024), ("ffn_down", 1024)])
+def test_split_pieces_pp512_sampled(h32, proj, M):
+    """The chain's projections as the chain runs them (split last wave), at
+    512 tokens and at the long prompts' 1024-token micro-batch: outputs sampled
+    inside the cut tiles (split along K where the schedule splits) and
+    elsewhere, against the oracle, bit for bit."""
     import torch
     p = {q.name: q for q in (wl.ATTN, wl.FFN_GATE_UP, wl.FFN_DOWN)}[proj]
     cid = wl.CFG_ATTN if p is wl.ATTN else wl.CFG_FFN
-    x = p.activations(512, 1, cid)
+    x = p.activations(M, 1, cid)
     w = p.weights(0, cid)
     wq, wd = oracle.quantize_weights_q4_0(w)
     xq, xd = oracle.quantize_act_q4(x)
     wp, wsc = h32.h32_prepack_weights_q4_0_tc(torch_of(wq), torch_of(wd.view(np.int16)))
     xw, xdt = h32.h32_quantize_act_q4_tc(torch_bf16(x))
-    sch = h32.h32_gemm_tc_schedule(512, p.N, p.K, _sms(), True)
-    y = np_of(h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=512))
+    sch = h32.h32_gemm_tc_schedule(M, p.N, p.K, _sms(), True)
+    y = np_of(h32.q4_0_x_q4_gemm_tc(wp, wsc, xw, xdt, M=M))
     torch.cuda.synchronize()
     assert h32.h32_device_status() == 0
     r = np.random.default_rng(11)
     # the cut tiles: tile t covers weight rows 128 (t // chunks) and tokens
     # bn (t % chunks) onward
-    chunks = (512 + sch["bn"] - 1) // sch["bn"]
+    chunks = (M + sch["bn"] - 1) // sch["bn"]
     cut = np.arange(sch["tail_first"], (sch["total"] - sch["tail_first"]) // max(sch["tail_k"], 1)
                     + sch["tail_first"])
     n_in = 128 * (cut // chunks)
     m_in = sch["bn"] * (cut % chunks)
     pick = r.integers(0, len(cut), 2000) if len(cut) else np.zeros(0, dtype=np.int64)
-    mi = np.concatenate([np.minimum(m_in[pick] + r.integers(0, sch["bn"], len(pick)), 511),
-                         r.integers(0, 512, 1000), [511]])
+    mi = np.concatenate([np.minimum(m_in[pick] + r.integers(0, sch["bn"], len(pick)), M - 1),
+                         r.integers(0, M, 1000), [M - 1]])
     ni = np.concatenate([np.minimum(n_in[pick] + r.integers(0, 128, len(pick)), p.N - 1),
                          r.integers(0, p.N, 1000), [p.N - 1]])
     r32, _, _ = oracle.gemm_sampled(wq, wd, xq, xd, p.K, mi, ni)

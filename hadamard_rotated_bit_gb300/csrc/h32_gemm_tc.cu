@@ -43,7 +43,9 @@
 // Schedule: one persistent CTA per SM takes tiles t = blockIdx.x, + gridDim.x,
 // ...  The host simulates that assignment once per shape to choose the token
 // width of a tile and, where it pays, a second kernel instance whose last
-// partial wave of tiles is cut into narrower pieces.  Kernels are launched with
+// partial wave of tiles is cut into narrower pieces, and (with a workspace) a
+// third whose cut pieces also run in two parts along K on two CTAs, the second
+// part continuing the first's accumulators (TcItem).  Kernels are launched with
 // programmatic dependent launch: nothing touches global memory before the
 // previous kernel of the stream has completed.
 

@@ -17,7 +17,8 @@
  * Conventions for every call:
  *   Ownership  All array pointers are device pointers owned by the caller.
  *              The library keeps no pointer after a call returns and allocates
- *              no device memory.
+ *              no device memory (the K split's workspace is the caller's, or,
+ *              for the _noalloc calls, a static array of the library's own).
  *   Streams    `stream` is a cudaStream_t (0 = the legacy default stream).
  *              Every compute call only enqueues work on it and returns.
  *   Errors     Argument, shape and alignment errors are returned at once,

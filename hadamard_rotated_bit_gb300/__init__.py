@@ -590,7 +590,11 @@ def _gemm_tc(fn, wp, wsc, xw, xdt, M, y, block_sums, stream, workspace=False):
     _need(y, "y", (torch.float32,), (_ge(M), _ge(N)), pitched=True)
     ldy = _rows(y, "y")
     S = _sums(block_sums, M, N, K // 32, dev)
-    _same_gpu(("wp", wp), ("wsc", wsc), ("xw", xw), ("xdt", xdt), ("y", y), ("S", S))
+    explicit_ws = workspace is not None and workspace is not False and not isinstance(workspace, str)
+    if explicit_ws:
+        _need(workspace, "workspace", (torch.uint8,), (_ge(0),))
+    _same_gpu(("wp", wp), ("wsc", wsc), ("xw", xw), ("xdt", xdt), ("y", y), ("S", S),
+              ("workspace", workspace if explicit_ws else None))
     if isinstance(workspace, str) and workspace == "noalloc":
         fn = fn + "_noalloc"
         st = getattr(lib(), fn)(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt),
@@ -600,9 +604,7 @@ def _gemm_tc(fn, wp, wsc, xw, xdt, M, y, block_sums, stream, workspace=False):
     ws = None
     if workspace is None and S is None and M > 0:
         ws = _workspace_for(M, N, K, dev, stream)
-    elif workspace is not None and workspace is not False:
-        _need(workspace, "workspace", (torch.uint8,), (_ge(0),))
-        _same_gpu(("wp", wp), ("workspace", workspace))
+    elif explicit_ws:
         ws = workspace
     if ws is None:
         st = getattr(lib(), fn)(_ptr(wp), _ptr(wsc), wsc.shape[1], _ptr(xw), _ptr(xdt),
@@ -766,14 +768,16 @@ def q4_0_x_q4_gemm_tc_quant_next(wp, wsc, xw, xdt, M=None, y=None, want_y=True, 
     if xdt_next is None:
         xdt_next = torch.zeros((N // 32, _round4(M)), dtype=torch.float32, device=dev)
     _need(xdt_next, "xdt_next", (torch.float32,), (_ge(N // 32), _ge(M)))
+    explicit_ws = workspace is not None and workspace is not False
+    if explicit_ws:
+        _need(workspace, "workspace", (torch.uint8,), (_ge(0),))
     _same_gpu(("wp", wp), ("wsc", wsc), ("xw", xw), ("xdt", xdt),
-              ("y", y), ("xw_next", xw_next), ("xdt_next", xdt_next))
+              ("y", y), ("xw_next", xw_next), ("xdt_next", xdt_next),
+              ("workspace", workspace if explicit_ws else None))
     ws = None
     if workspace is None and M > 0:
         ws = _workspace_for(M, N, K, dev, stream)
-    elif workspace is not None and workspace is not False:
-        _need(workspace, "workspace", (torch.uint8,), (_ge(0),))
-        _same_gpu(("wp", wp), ("workspace", workspace))
+    elif explicit_ws:
         ws = workspace
     if ws is None:
         st = lib().q4_0_x_q4_gemm_tc_quant_next(

@@ -37,6 +37,13 @@ def test_tc_gemm_operands():
     _raises("y must be 2-D with contiguous", h32.q4_0_x_q4_gemm_tc, wp, wsc, xw, xdt, y=y_t)
     _raises("block_sums: shape", h32.q4_0_x_q4_gemm_tc, wp, wsc, xw, xdt,
             block_sums=torch.zeros((8, 32, 3), dtype=i32))
+    # the K split's workspace: bytes, one flat array
+    _raises("workspace: dtype", h32.q4_0_x_q4_gemm_tc, wp, wsc, xw, xdt,
+            workspace=torch.zeros(64, dtype=f32))
+    _raises("workspace: shape", h32.q4_0_x_q8_gemm_tc, wp, wsc, torch.zeros((8, 256), dtype=u8),
+            xdt, workspace=torch.zeros((8, 8), dtype=u8))
+    _raises("workspace: dtype", h32.q4_0_x_q4_gemm_tc_quant_next, *_tc_operands(N=64),
+            workspace=torch.zeros(64, dtype=i32))
 
 
 def test_direct_and_quantizer_outputs():

@@ -97,3 +97,40 @@ def test_need_shapes():
     _raises("t: shape", h32._need, t, "t", (f32,), (5, 8))
     _raises("t: shape", h32._need, t, "t", (f32,), (4, h32._ge(9)))
     _raises("t: shape", h32._need, t, "t", (f32,), (4, 8, 1))
+
+
+def test_workspace_cache_per_stream(monkeypatch):
+    """The binding's K-split workspaces (host logic, faked sizes, CPU tensors):
+    one zeroed workspace per (device, stream), kept across calls; a larger need
+    replaces it and keeps the old one alive (a captured graph may still use
+    it); no workspace when the schedule does not split; inside a graph capture
+    a fresh one per call, not cached."""
+    need = {"bytes": 1000}
+    monkeypatch.setattr(h32, "h32_gemm_tc_workspace_bytes", lambda M, N, K: need["bytes"])
+    monkeypatch.setattr(torch.cuda, "is_current_stream_capturing", lambda: False)
+    monkeypatch.setattr(h32, "_workspaces", {})
+    monkeypatch.setattr(h32, "_retired_workspaces", [])
+
+    class S1:
+        cuda_stream = 1234
+
+    class S2:
+        cuda_stream = 5678
+
+    dev = torch.device("cpu")
+    a = h32._workspace_for(1, 1, 1, dev, S1())
+    assert a.dtype == u8 and a.numel() == 1000 and int(a.sum()) == 0
+    assert h32._workspace_for(1, 1, 1, dev, S1()) is a
+    assert h32._workspace_for(1, 1, 1, dev, S2()) is not a
+    need["bytes"] = 4000
+    b = h32._workspace_for(1, 1, 1, dev, S1())
+    assert b.numel() == 4000 and any(r is a for r in h32._retired_workspaces)
+    need["bytes"] = 256
+    assert h32._workspace_for(1, 1, 1, dev, S1()) is b     # large enough already
+    need["bytes"] = 0
+    assert h32._workspace_for(1, 1, 1, dev, S1()) is None
+    need["bytes"] = 500
+    monkeypatch.setattr(torch.cuda, "is_current_stream_capturing", lambda: True)
+    c, d = h32._workspace_for(1, 1, 1, dev, S1()), h32._workspace_for(1, 1, 1, dev, S1())
+    assert c is not d and c.numel() == 500 and int(c.sum()) == 0
+    assert h32._workspaces[(None, 1234)] is b
